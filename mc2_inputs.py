@@ -1,0 +1,148 @@
+"""Seeded synthetic inputs for the MC2 fused-linear workloads.
+
+This module is shared by the tests, the benchmark and the smoke check.  It
+holds shapes, value distributions and a fixed draw order, and none of the
+method's arithmetic (no gather, permute, quant or matmul).  Everything is
+drawn on the CPU with ``torch.Generator().manual_seed(seed)`` in this order:
+the per-rank chunks r = 0 .. R-1, then x2 (or w), then the scales, then the
+bias.  Callers copy the tensors to the device themselves.
+
+Workloads (names used throughout the repository):
+
+  ag-tiny    AllGatherMatmul, 8 ranks x (16, 512) fp16 ~N(0,1), x2 (512, 64)
+             fp16 ~N(0,1), gathered output on.  Shapes of the example on the
+             page "torch_npu.npu_all_gather_base_mm" (调用示例).
+  ag-8x1024  AllGatherMatmul bf16, 8 ranks x (1024, 4096) ~N(0,1),
+             x2 (4096, 4096) ~N(0, std k^-1/2), gathered output on, no bias.
+  ag-4x4096  AllGatherMatmul bf16, 4 ranks x (4096, 8192) ~N(0,1), nn.Linear
+             weight w (7168, 8192) ~N(0, std k^-1/2) passed as x2 = w^T,
+             bias (7168) bf16 ~N(0, 0.02), gathered output on.
+  a2a-dyn    AlltoAllQuantMatmul, quant mode 7 (per-token dynamic), 8 ranks x
+             (4096, 1024) bf16 ~N(0,1) with 0.1% of elements x20, smooth scale
+             (8192) bf16 ~U(0.5, 1.5), x2 int8 (8192, 4096) uniform on
+             [-127, 127], x2 scale (4096) fp32 ~U(1e-3, 1e-2), bias (4096) fp32
+             ~N(0, 0.1).
+  a2a-dyn-small  the same with chunks (512, 1024).
+  a2a-full   AlltoAllQuantMatmul, quant mode 3 (pre-quantised int8), 8 ranks x
+             (16384, 4096) int8 uniform on [-127, 127], per-token x1 scale
+             (16384) fp32 ~U(1e-3, 1e-2), x2 int8 (32768, 7168), x2 scale
+             (7168) fp32 ~U(1e-3, 1e-2), bias (7168) fp32 ~N(0, 0.1).
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, replace
+from typing import Optional
+
+import torch
+
+
+@dataclass(frozen=True)
+class AGShape:
+    world_size: int
+    m_local: int
+    k: int
+    n: int
+    dtype: torch.dtype = torch.bfloat16
+    x2_is_nk: bool = False          # x2 given as the nn.Linear weight w (n, k)
+    bias: bool = False
+    gather_output: bool = True
+    x_std: float = 1.0
+    w_std: Optional[float] = None   # None: k ** -0.5
+    bias_std: float = 0.02
+
+    @property
+    def m(self) -> int:
+        return self.world_size * self.m_local
+
+    @property
+    def flops(self) -> float:
+        return 2.0 * self.m * self.n * self.k
+
+
+@dataclass(frozen=True)
+class A2AShape:
+    rank_size: int
+    bs_local: int                   # BS / rankSize: rows of the permuted matrix
+    h: int                          # hidden size of one received chunk
+    n: int
+    quant_mode: int                 # 7 per-token dynamic, 3 per-token (pre-quantised)
+    x1_dtype: torch.dtype = torch.bfloat16   # for mode 7; mode 3 chunks are int8
+    smooth: bool = True             # mode 7: pass the smooth scale x1ScaleOptional
+    outlier_p: float = 0.001
+    outlier_mult: float = 20.0
+    bias: bool = True
+
+    @property
+    def k(self) -> int:
+        return self.rank_size * self.h
+
+    @property
+    def ops(self) -> float:
+        return 2.0 * self.bs_local * self.n * self.k
+
+
+WORKLOADS = {
+    "ag-tiny": AGShape(world_size=8, m_local=16, k=512, n=64, dtype=torch.float16, w_std=1.0),
+    "ag-8x1024": AGShape(world_size=8, m_local=1024, k=4096, n=4096),
+    "ag-4x4096": AGShape(world_size=4, m_local=4096, k=8192, n=7168, x2_is_nk=True, bias=True),
+    "a2a-dyn": A2AShape(rank_size=8, bs_local=4096, h=1024, n=4096, quant_mode=7),
+    "a2a-dyn-small": A2AShape(rank_size=8, bs_local=512, h=1024, n=4096, quant_mode=7),
+    "a2a-full": A2AShape(rank_size=8, bs_local=16384, h=4096, n=7168, quant_mode=3),
+}
+
+
+def scaled(shape, **kw):
+    """A copy of a workload shape with some fields changed (smaller test cases)."""
+    return replace(shape, **kw)
+
+
+def _gen(seed: int) -> torch.Generator:
+    g = torch.Generator()
+    g.manual_seed(seed)
+    return g
+
+
+def _randint8(g, shape):
+    return torch.randint(-127, 128, shape, generator=g, dtype=torch.int8)
+
+
+def ag_inputs(s: AGShape, seed: int = 0) -> dict:
+    """chunks (list of R (m_local, k)), x2 ((k, n) or w (n, k)), bias (n) or None."""
+    g = _gen(seed)
+    chunks = [(torch.randn(s.m_local, s.k, generator=g) * s.x_std).to(s.dtype)
+              for _ in range(s.world_size)]
+    w_std = s.k ** -0.5 if s.w_std is None else s.w_std
+    wshape = (s.n, s.k) if s.x2_is_nk else (s.k, s.n)
+    x2 = (torch.randn(*wshape, generator=g) * w_std).to(s.dtype)
+    bias = (torch.randn(s.n, generator=g) * s.bias_std).to(s.dtype) if s.bias else None
+    return {"chunks": chunks, "x2": x2, "bias": bias}
+
+
+def a2a_inputs(s: A2AShape, seed: int = 0) -> dict:
+    """chunks (R x (bs_local, h)), x1_scale (smooth (R*h) or per-token (bs_local)),
+    x2 int8 (R*h, n), x2_scale fp32 (n), bias fp32 (n) or None."""
+    g = _gen(seed)
+    chunks = []
+    for _ in range(s.rank_size):
+        if s.quant_mode == 7:
+            v = torch.randn(s.bs_local, s.h, generator=g)
+            hit = torch.rand(s.bs_local, s.h, generator=g) < s.outlier_p
+            v = torch.where(hit, v * s.outlier_mult, v)
+            chunks.append(v.to(s.x1_dtype))
+        else:
+            chunks.append(_randint8(g, (s.bs_local, s.h)))
+    x2 = _randint8(g, (s.k, s.n))
+    if s.quant_mode == 7:
+        x1_scale = (torch.rand(s.k, generator=g) + 0.5).to(s.x1_dtype) if s.smooth else None
+    else:
+        x1_scale = torch.rand(s.bs_local, generator=g) * 9e-3 + 1e-3
+    x2_scale = torch.rand(s.n, generator=g) * 9e-3 + 1e-3
+    bias = torch.randn(s.n, generator=g) * 0.1 if s.bias else None
+    return {"chunks": chunks, "x1_scale": x1_scale, "x2": x2, "x2_scale": x2_scale, "bias": bias}
+
+
+def sample_rows(total: int, count: int, seed: int = 1) -> torch.Tensor:
+    """A seeded subset of row indices (sorted) for checking very large outputs."""
+    g = _gen(seed)
+    count = min(count, total)
+    return torch.sort(torch.randperm(total, generator=g)[:count]).values

@@ -1,0 +1,246 @@
+"""CPU oracle for the MC2 fused-linear hot path -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline / reference
+arm of ``bench.py`` may import this package.  The product library never
+loads it and shares no code with it.  The arithmetic lives in plain C
+(``mc2_oracle.c``: fp64-accumulated bf16/fp16 matmul, exact int64-accumulated
+int8 matmul, fp32 per-token quant and dequant, 16-bit conversions written from
+the IEEE layouts); this module only marshals torch CPU tensors into it.
+
+Pages followed (title -- section):
+  * "torch_npu.npu_all_gather_base_mm" -- 功能说明, 接口原型, 输出说明, 约束说明
+  * "aclnnAlltoAllQuantMatmul" -- 功能说明 / 计算公式 (dynamic- and full-quant)
+  * "hyper_parallel .../tensor_parallel/mc2.py" -- AllGatherMatmulFunction.forward
+
+Every function here is pinned by ``tests/test_oracle_*.py`` against closed
+forms, brute force and independent library routines.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from typing import Optional, Sequence
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "mc2_oracle.c")
+_LIB = os.path.join(_HERE, "libmc2_oracle.so")
+_lib = None
+
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_INT = ctypes.c_int
+
+
+def build(force: bool = False) -> str:
+    """Compile the C oracle with gcc (OpenMP, no FMA contraction)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-std=c11", "-O2", "-fopenmp", "-ffp-contract=off", "-fno-fast-math",
+               "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        lib = ctypes.CDLL(_LIB)
+        lib.oracle_decode16.restype = ctypes.c_double
+        lib.oracle_decode16.argtypes = [ctypes.c_uint16, _INT]
+        lib.oracle_encode16_rne.restype = ctypes.c_uint16
+        lib.oracle_encode16_rne.argtypes = [ctypes.c_double, _INT]
+        lib.oracle_decode16_array.argtypes = [_P, _I64, _INT, _P]
+        lib.oracle_encode16_array.argtypes = [_P, _I64, _INT, _P]
+        lib.oracle_gather.argtypes = [_P, _INT, _I64, _I64, _P]
+        lib.oracle_all_gather_mm.argtypes = [_P, _INT, _I64, _I64, _P, _I64, _INT, _P, _INT, _P, _I64, _P]
+        lib.oracle_permute.argtypes = [_P, _INT, _I64, _I64, _INT, _P, _I64, _P]
+        lib.oracle_quant_pertoken_dynamic.argtypes = [_P, _I64, _I64, _P, _INT, _P, _P]
+        lib.oracle_int8_mm.argtypes = [_P, _I64, _I64, _P, _I64, _P]
+        lib.oracle_dequant.argtypes = [_P, _I64, _I64, _P, _P, _P, _P]
+        lib.oracle_alltoall_quant_mm.argtypes = [_P, _INT, _I64, _I64, _INT, _INT, _P, _P, _P, _P,
+                                                 _I64, _P, _I64, _P, _P, _P, _P]
+        lib.oracle_num_threads.restype = _INT
+        _lib = lib
+    return _lib
+
+
+def num_threads() -> int:
+    return int(_load().oracle_num_threads())
+
+
+# --------------------------------------------------------------------------- helpers
+def _is_bf16(dtype: torch.dtype) -> int:
+    if dtype == torch.bfloat16:
+        return 1
+    if dtype == torch.float16:
+        return 0
+    raise TypeError(f"expected a bf16 or fp16 tensor, got {dtype}")
+
+
+def _c(t: torch.Tensor) -> torch.Tensor:
+    assert t.device.type == "cpu", "the oracle runs on CPU tensors only"
+    return t.contiguous()
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _ptr_array(ts: Sequence[torch.Tensor]):
+    arr = (ctypes.c_void_p * len(ts))(*[t.data_ptr() for t in ts])
+    return arr
+
+
+def _rows_arg(rows):
+    if rows is None:
+        return None, 0
+    r = torch.as_tensor(rows, dtype=torch.int64).contiguous()
+    return r, int(r.numel())
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        raise RuntimeError(f"oracle {what} failed with code {rc}")
+
+
+# --------------------------------------------------------------------------- conversions
+def decode16(bits: torch.Tensor, is_bf16: bool) -> torch.Tensor:
+    """int16/uint16 bit patterns -> exact float64 values."""
+    b = _c(bits.view(torch.int16))
+    out = torch.empty(b.shape, dtype=torch.float64)
+    _load().oracle_decode16_array(b.data_ptr(), b.numel(), int(is_bf16), out.data_ptr())
+    return out
+
+
+def encode16(values: torch.Tensor, is_bf16: bool) -> torch.Tensor:
+    """float64 values -> 16-bit tensor (bf16 or fp16), round to nearest even."""
+    v = _c(values.to(torch.float64))
+    out = torch.empty(v.shape, dtype=torch.int16)
+    _load().oracle_encode16_array(v.data_ptr(), v.numel(), int(is_bf16), out.data_ptr())
+    return out.view(torch.bfloat16 if is_bf16 else torch.float16)
+
+
+# --------------------------------------------------------------------------- AllGatherMatmul
+def gather(chunks: Sequence[torch.Tensor]) -> torch.Tensor:
+    """AllGather along m of the per-rank shards, by explicit copy."""
+    cs = [_c(c) for c in chunks]
+    m_local, k = cs[0].shape
+    out = torch.empty((len(cs) * m_local, k), dtype=cs[0].dtype)
+    _check(_load().oracle_gather(_ptr_array(cs), len(cs), m_local, k, out.data_ptr()), "gather")
+    return out
+
+
+def all_gather_mm(chunks: Sequence[torch.Tensor], x2: torch.Tensor, *, x2_is_nk: bool = False,
+                  bias: Optional[torch.Tensor] = None, rows=None, gather_output: bool = True):
+    """out = AllGather_m(chunks) @ x2 (+ bias), rounded once; returns (out, gathered|None).
+
+    With ``rows`` only those gathered rows of ``out`` are computed (in order).
+    """
+    cs = [_c(c) for c in chunks]
+    dt = cs[0].dtype
+    isb = _is_bf16(dt)
+    m_local, k = cs[0].shape
+    x2c = _c(x2)
+    n = x2c.shape[0] if x2_is_nk else x2c.shape[1]
+    b = None if bias is None else _c(bias.to(dt))
+    r, nr = _rows_arg(rows)
+    nrows = nr if r is not None else len(cs) * m_local
+    out = torch.empty((nrows, n), dtype=dt)
+    rc = _load().oracle_all_gather_mm(_ptr_array(cs), len(cs), m_local, k, x2c.data_ptr(), n,
+                                      int(x2_is_nk), _ptr(b), isb, _ptr(r), nr, out.data_ptr())
+    _check(rc, "all_gather_mm")
+    return out, (gather(cs) if gather_output else None)
+
+
+# --------------------------------------------------------------------------- AlltoAllQuantMatmul
+def permute(chunks: Sequence[torch.Tensor], rows=None) -> torch.Tensor:
+    """permutedOut[t, r*H + h] = chunk_r[t, h] for the requested rows t."""
+    cs = [_c(c) for c in chunks]
+    bs_local, h = cs[0].shape
+    eb = cs[0].element_size()
+    r, nr = _rows_arg(rows)
+    nrows = nr if r is not None else bs_local
+    out = torch.empty((nrows, len(cs) * h), dtype=cs[0].dtype)
+    _check(_load().oracle_permute(_ptr_array(cs), len(cs), bs_local, h, eb, _ptr(r), nr,
+                                  out.data_ptr()), "permute")
+    return out
+
+
+def quant_pertoken_dynamic(permuted: torch.Tensor, smooth: Optional[torch.Tensor] = None):
+    """Per-token dynamic int8 quant: returns (q int8, x1_scale fp32)."""
+    p = _c(permuted)
+    isb = _is_bf16(p.dtype)
+    rows, cols = p.shape
+    s = None if smooth is None else _c(smooth.to(p.dtype))
+    q = torch.empty((rows, cols), dtype=torch.int8)
+    sc = torch.empty((rows,), dtype=torch.float32)
+    _check(_load().oracle_quant_pertoken_dynamic(p.data_ptr(), rows, cols, _ptr(s), isb,
+                                                 q.data_ptr(), sc.data_ptr()), "quant")
+    return q, sc
+
+
+def int8_mm(a: torch.Tensor, x2: torch.Tensor) -> torch.Tensor:
+    """Exact int8 x int8 matmul, int32 result (error if a sum leaves int32)."""
+    ac, bc = _c(a), _c(x2)
+    rows, k = ac.shape
+    n = bc.shape[1]
+    acc = torch.empty((rows, n), dtype=torch.int32)
+    _check(_load().oracle_int8_mm(ac.data_ptr(), rows, k, bc.data_ptr(), n, acc.data_ptr()), "int8_mm")
+    return acc
+
+
+def dequant(acc: torch.Tensor, x1_scale: torch.Tensor, x2_scale: torch.Tensor,
+            bias: Optional[torch.Tensor]) -> torch.Tensor:
+    """bf16(((float(acc) * x1s[t]) * x2s[n]) + bias[n]) in fp32, one op at a time."""
+    a = _c(acc)
+    rows, n = a.shape
+    s1, s2 = _c(x1_scale.float()), _c(x2_scale.float())
+    b = None if bias is None else _c(bias.float())
+    out = torch.empty((rows, n), dtype=torch.int16)
+    _check(_load().oracle_dequant(a.data_ptr(), rows, n, s1.data_ptr(), s2.data_ptr(), _ptr(b),
+                                  out.data_ptr()), "dequant")
+    return out.view(torch.bfloat16)
+
+
+def alltoall_quant_mm(chunks: Sequence[torch.Tensor], x2: torch.Tensor, x2_scale: torch.Tensor,
+                      bias: Optional[torch.Tensor], *, quant_mode: int,
+                      x1_scale: Optional[torch.Tensor] = None, rows=None) -> dict:
+    """The whole AlltoAllQuantMatmul path for the requested permuted rows.
+
+    quant_mode 7: chunks bf16/fp16, ``x1_scale`` = optional smooth scale (R*H).
+    quant_mode 3: chunks int8, ``x1_scale`` = per-token fp32 scale (BS/R).
+    Returns dict(out bf16, q int8, x1_scale fp32, acc int32) for those rows.
+    """
+    cs = [_c(c) for c in chunks]
+    R = len(cs)
+    bs_local, h = cs[0].shape
+    x2c = _c(x2)
+    n = x2c.shape[1]
+    if quant_mode == 7:
+        isb = _is_bf16(cs[0].dtype)
+        s_in = None if x1_scale is None else _c(x1_scale.to(cs[0].dtype))
+    elif quant_mode == 3:
+        isb = 1
+        s_in = _c(x1_scale.float())
+    else:
+        raise ValueError("quant_mode must be 3 or 7")
+    r, nr = _rows_arg(rows)
+    nrows = nr if r is not None else bs_local
+    out = torch.empty((nrows, n), dtype=torch.int16)
+    q = torch.empty((nrows, R * h), dtype=torch.int8)
+    sc = torch.empty((nrows,), dtype=torch.float32)
+    acc = torch.empty((nrows, n), dtype=torch.int32)
+    b = None if bias is None else _c(bias.float())
+    s2 = _c(x2_scale.float())
+    rc = _load().oracle_alltoall_quant_mm(_ptr_array(cs), R, bs_local, h, quant_mode, isb, _ptr(s_in),
+                                          x2c.data_ptr(), s2.data_ptr(), _ptr(b), n,
+                                          _ptr(r), nr, out.data_ptr(), q.data_ptr(), sc.data_ptr(),
+                                          acc.data_ptr())
+    _check(rc, "alltoall_quant_mm")
+    return {"out": out.view(torch.bfloat16), "q": q, "x1_scale": sc, "acc": acc}
