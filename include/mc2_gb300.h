@@ -1,0 +1,156 @@
+/*
+ * mc2_gb300.h -- C ABI of the GB300 (sm_103a) MC2 fused-linear library.
+ *
+ * Two operations, each the compute hot path of one communication-compute
+ * fused linear.  The world_size (rankSize) shards that a collective would
+ * deliver are separate device buffers on one GPU; the library reads them in
+ * place and never runs a collective.
+ *
+ * Conventions shared by every call
+ *   - Every tensor is a DEVICE pointer, row-major and contiguous, owned by the
+ *     caller.  Arrays of per-rank pointers (x_chunks, chunks) are HOST arrays
+ *     of device pointers.
+ *   - Work is enqueued on `stream` (a cudaStream_t passed as void*; NULL is the
+ *     legacy default stream) and the call returns without synchronising.  The
+ *     library keeps no state between calls and never allocates device memory:
+ *     scratch space is the caller's `workspace`.
+ *   - Arguments are validated before anything is launched.  A violated
+ *     constraint returns a negative mc2_status and launches nothing;
+ *     mc2_last_error() then describes which argument failed (thread-local).
+ *   - Outputs are deterministic: no atomics, no split-K.
+ *   - Pointers must be 16-byte aligned and row pitches multiples of 16 bytes
+ *     (the tensor-memory-accelerator copies need it); otherwise
+ *     MC2_ERR_UNSUPPORTED.
+ */
+#ifndef MC2_GB300_H
+#define MC2_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MC2_OK = 0,
+    MC2_ERR_NULL = -1,        /* a required pointer is NULL */
+    MC2_ERR_SHAPE = -2,       /* a size breaks a constraint of the op */
+    MC2_ERR_DTYPE = -3,       /* a dtype or quant-mode combination is not allowed */
+    MC2_ERR_UNSUPPORTED = -4, /* allowed by the op but not by this kernel (alignment, box shape) */
+    MC2_ERR_WORKSPACE = -5,   /* workspace missing or smaller than the query returned */
+    MC2_ERR_CUDA = -6,        /* a CUDA runtime/driver call failed (no device, launch error) */
+    MC2_ERR_TIMEOUT = -7      /* a bounded device-side wait gave up (see mc2_device_status) */
+} mc2_status;
+
+typedef enum { MC2_F16 = 1, MC2_BF16 = 2, MC2_F32 = 3, MC2_I8 = 4 } mc2_dtype;
+
+/* Quant-mode enumeration of "aclnnAlltoAllQuantMatmul" (函数原型, the
+ * x1QuantMode / x2QuantMode / commQuantMode values). */
+typedef enum {
+    MC2_QUANT_NONE = 0,
+    MC2_QUANT_PERTENSOR = 1,
+    MC2_QUANT_PERCHANNEL = 2,
+    MC2_QUANT_PERTOKEN = 3,
+    MC2_QUANT_PERGROUP = 4,
+    MC2_QUANT_PERBLOCK = 5,
+    MC2_QUANT_MX = 6,
+    MC2_QUANT_PERTOKEN_DYNAMIC = 7
+} mc2_quant_mode;
+
+/*
+ * AllGatherMatmul  ("torch_npu.npu_all_gather_base_mm": 功能说明, 接口原型,
+ * 输出说明, 约束说明; x2 passed as w^T as in hyper_parallel mc2.py
+ * AllGatherMatmulFunction.forward).
+ *
+ *   gathered = concat_m(x_chunks[0], ..., x_chunks[world_size-1])   (m, k)
+ *   out      = gathered @ x2 (+ bias)                                (m, n)
+ *   m = world_size * m_local.  Accumulation is fp32; out is rounded once
+ *   (nearest-even) to `dtype`.  bias, if given, is added in fp32 before the
+ *   rounding.
+ *
+ *   x_chunks      host array of world_size device pointers, each (m_local, k)
+ *   world_size    2, 4 or 8
+ *   m_local       rows per rank, >= 1 (this kernel: a multiple of 8)
+ *   k             contraction size, 256 <= k < 65535 (this kernel: k % 8 == 0)
+ *   x2            (k, n) row-major, or with x2_is_nk != 0 the nn.Linear weight
+ *                 w (n, k) row-major such that x2 = w^T
+ *   n             output columns, >= 1 (this kernel: n % 8 == 0)
+ *   bias          NULL or (n) of `dtype`
+ *   dtype         MC2_F16 or MC2_BF16, the type of chunks, x2, bias and out
+ *   gather_output nonzero: also write `gathered` (m, k); zero: gathered must be NULL
+ *   out           (m, n) of `dtype`
+ *
+ * Returns MC2_OK or a negative mc2_status; nothing is launched on error.
+ */
+int mc2_all_gather_mm(const void *const *x_chunks, int world_size, int64_t m_local, int64_t k,
+                      const void *x2, int64_t n, int x2_is_nk, const void *bias, int dtype,
+                      int gather_output, void *out, void *gathered, void *stream);
+
+/*
+ * Workspace size (bytes) that mc2_alltoall_quant_mm needs for these sizes.
+ * Same argument meanings and validation as mc2_alltoall_quant_mm.
+ */
+int mc2_alltoall_quant_mm_workspace(int rank_size, int64_t bs_local, int64_t h, int64_t n,
+                                    int x1_quant_mode, int x1_dtype, size_t *bytes);
+
+/*
+ * AlltoAllQuantMatmul  ("aclnnAlltoAllQuantMatmul": 功能说明 / 计算公式,
+ * 函数原型, 约束说明).  The AlltoAll has already delivered the rank's
+ * rank_size received blocks, chunks[r] = commOut[r], each (bs_local, h).
+ *
+ *   permuted[t, r*h + j] = chunks[r][t, j]            (bs_local, rank_size*h)
+ *   x1_quant_mode 7 (per-token dynamic):
+ *     y = permuted * x1_scale (smooth, per column; absent = 1), in fp32
+ *     x1s[t] = max_j |y[t, j]| / 127;  q = clamp(rne(y / x1s[t]), -127, 127)
+ *     (an all-zero row gives x1s = 0, q = 0)
+ *   x1_quant_mode 3 (per-token, pre-quantised): q = permuted (int8),
+ *     x1s = x1_scale (input)
+ *   acc = q @ x2, exact int32
+ *   out = bf16_rne(((float(acc) * x1s[t]) * x2_scale[j]) + bias[j]), fp32 ops in
+ *         that order
+ *
+ *   chunks          host array of rank_size device pointers, each (bs_local, h):
+ *                   dtype x1_dtype (MC2_BF16 / MC2_F16 for mode 7, MC2_I8 for mode 3)
+ *   rank_size       2, 4 or 8
+ *   bs_local        BS / rank_size, 1 <= BS <= INT32_MAX
+ *   h               1 <= rank_size*h <= 35000, rank_size*h % 16 == 0
+ *   x1_scale        mode 7: NULL or the smooth scale (rank_size*h) of x1_dtype;
+ *                   mode 3: required per-token scale (bs_local) fp32
+ *   x2              int8 (rank_size*h, n), contiguous
+ *   x2_scale        fp32 (n), per channel (x2_quant_mode must be 2)
+ *   bias            (n), required; bias_dtype MC2_F32 or MC2_BF16
+ *   n               1 <= n <= INT32_MAX (this kernel: n % 16 == 0)
+ *   out             bf16 (bs_local, n)
+ *   q_out           NULL or int8 (bs_local, rank_size*h): the quantised activations (mode 7)
+ *   x1_scale_out    NULL or fp32 (bs_local): the per-token scales (mode 7)
+ *   acc_out         NULL or int32 (bs_local, n): the exact accumulators (debug)
+ *   workspace       device scratch of at least the bytes the query returns
+ *
+ * Returns MC2_OK or a negative mc2_status; nothing is launched on error.
+ */
+int mc2_alltoall_quant_mm(const void *const *chunks, int rank_size, int64_t bs_local, int64_t h,
+                          int x1_dtype, const void *x1_scale, const int8_t *x2, const float *x2_scale,
+                          const void *bias, int bias_dtype, int x1_quant_mode, int x2_quant_mode,
+                          int64_t n, void *out, int8_t *q_out, float *x1_scale_out, int32_t *acc_out,
+                          void *workspace, size_t workspace_bytes, void *stream);
+
+/* Name of a status code (static string). */
+const char *mc2_status_str(int status);
+
+/* Description of the last failure on this thread (static per-thread buffer). */
+const char *mc2_last_error(void);
+
+/*
+ * Device-side status of the kernels launched so far on the current device:
+ * synchronises the device, returns MC2_OK or MC2_ERR_TIMEOUT if a bounded wait
+ * inside a kernel gave up (the kernel then skipped the rest of its tile loop),
+ * and clears the flag.
+ */
+int mc2_device_status(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MC2_GB300_H */

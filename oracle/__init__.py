@@ -195,6 +195,29 @@ def int8_mm(a: torch.Tensor, x2: torch.Tensor) -> torch.Tensor:
     return acc
 
 
+def int8_mm_fp64(a: torch.Tensor, x2: torch.Tensor, col_block: int = 1024) -> torch.Tensor:
+    """The same exact int8 matmul through an fp64 library matmul.
+
+    Every product of two int8 values is an integer of magnitude <= 127*127 and
+    every partial sum over k <= 35000 terms is an integer below 2^30, far inside
+    the 2^53 range where fp64 represents integers exactly, so the result is
+    exact whatever order the library sums in.  Used for large row sets.
+    """
+    ac = _c(a)
+    bc = _c(x2)
+    k = ac.shape[1]
+    if k * 127 * 127 >= 2 ** 53:
+        raise ValueError("k too large for an exact fp64 sum")
+    ad = ac.double()
+    out = torch.empty((ac.shape[0], bc.shape[1]), dtype=torch.int32)
+    for j0 in range(0, bc.shape[1], col_block):
+        blk = ad @ bc[:, j0:j0 + col_block].double()
+        if blk.abs().max().item() > 2 ** 31 - 1:
+            raise RuntimeError("oracle int8_mm: a result does not fit in int32")
+        out[:, j0:j0 + col_block] = blk.to(torch.int32)
+    return out
+
+
 def dequant(acc: torch.Tensor, x1_scale: torch.Tensor, x2_scale: torch.Tensor,
             bias: Optional[torch.Tensor]) -> torch.Tensor:
     """bf16(((float(acc) * x1s[t]) * x2s[n]) + bias[n]) in fp32, one op at a time."""
@@ -232,6 +255,17 @@ def alltoall_quant_mm(chunks: Sequence[torch.Tensor], x2: torch.Tensor, x2_scale
         raise ValueError("quant_mode must be 3 or 7")
     r, nr = _rows_arg(rows)
     nrows = nr if r is not None else bs_local
+    if nrows * R * h * n > (1 << 31):
+        # large: the same steps, with the exact fp64 library matmul for the int8 product
+        P = permute(cs, rows=r)
+        if quant_mode == 7:
+            q, sc = quant_pertoken_dynamic(P, s_in)
+        else:
+            q = P
+            sc = s_in if r is None else s_in[r]
+        acc = int8_mm_fp64(q, x2c)
+        out = dequant(acc, sc, x2_scale, bias)
+        return {"out": out, "q": q, "x1_scale": sc.clone(), "acc": acc}
     out = torch.empty((nrows, n), dtype=torch.int16)
     q = torch.empty((nrows, R * h), dtype=torch.int8)
     sc = torch.empty((nrows,), dtype=torch.float32)

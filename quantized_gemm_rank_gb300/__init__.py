@@ -1,0 +1,192 @@
+"""GB300 (sm_103a) MC2 fused linears: Python binding of the C ABI in
+``include/mc2_gb300.h``.
+
+Argument marshalling only: every step of both operations runs in the CUDA
+library ``libmc2_gb300.so`` (built in-tree by :mod:`.build`).  PyTorch
+provides device memory and streams.  There is no CPU fallback: if the library
+cannot be built or loaded, importing the functions raises.
+
+  mc2_all_gather_mm        out = concat_m(x_chunks) @ x2 (+ bias), plus gathered
+  mc2_alltoall_quant_mm    out = (Quant(permute(chunks)) @ x2) * x1s * x2s + bias
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import torch
+
+from . import build as _build
+
+MC2_OK = 0
+MC2_ERR_NULL = -1
+MC2_ERR_SHAPE = -2
+MC2_ERR_DTYPE = -3
+MC2_ERR_UNSUPPORTED = -4
+MC2_ERR_WORKSPACE = -5
+MC2_ERR_CUDA = -6
+MC2_ERR_TIMEOUT = -7
+
+MC2_F16, MC2_BF16, MC2_F32, MC2_I8 = 1, 2, 3, 4
+QUANT_PERCHANNEL = 2
+QUANT_PERTOKEN = 3
+QUANT_PERTOKEN_DYNAMIC = 7
+
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_INT = ctypes.c_int
+_lib = None
+
+
+class Mc2Error(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{status_str(status)}: {message}")
+        self.status = status
+        self.message = message
+
+
+def lib() -> ctypes.CDLL:
+    """Load (building first if the sources changed) the CUDA library."""
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        L = ctypes.CDLL(path)
+        L.mc2_all_gather_mm.argtypes = [_P, _INT, _I64, _I64, _P, _I64, _INT, _P, _INT, _INT, _P, _P, _P]
+        L.mc2_all_gather_mm.restype = _INT
+        L.mc2_alltoall_quant_mm_workspace.argtypes = [_INT, _I64, _I64, _I64, _INT, _INT,
+                                                      ctypes.POINTER(ctypes.c_size_t)]
+        L.mc2_alltoall_quant_mm_workspace.restype = _INT
+        L.mc2_alltoall_quant_mm.argtypes = [_P, _INT, _I64, _I64, _INT, _P, _P, _P, _P, _INT, _INT, _INT, _I64,
+                                            _P, _P, _P, _P, _P, ctypes.c_size_t, _P]
+        L.mc2_alltoall_quant_mm.restype = _INT
+        L.mc2_status_str.argtypes = [_INT]
+        L.mc2_status_str.restype = ctypes.c_char_p
+        L.mc2_last_error.argtypes = []
+        L.mc2_last_error.restype = ctypes.c_char_p
+        L.mc2_device_status.argtypes = []
+        L.mc2_device_status.restype = _INT
+        _lib = L
+    return _lib
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def status_str(status: int) -> str:
+    return lib().mc2_status_str(status).decode()
+
+
+def last_error() -> str:
+    return lib().mc2_last_error().decode()
+
+
+def _check(status: int):
+    if status != MC2_OK:
+        raise Mc2Error(status, last_error())
+
+
+def _dtype_code(dt: torch.dtype) -> int:
+    return {torch.float16: MC2_F16, torch.bfloat16: MC2_BF16, torch.float32: MC2_F32, torch.int8: MC2_I8}[dt]
+
+
+def _dev(t: torch.Tensor, what: str) -> int:
+    if not t.is_cuda:
+        raise ValueError(f"{what} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{what} must be contiguous")
+    return t.data_ptr()
+
+
+def _opt(t: Optional[torch.Tensor], what: str) -> Optional[int]:
+    return None if t is None else _dev(t, what)
+
+
+def _stream(stream) -> Optional[int]:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _ptrs(ts: Sequence[torch.Tensor], what: str):
+    return (ctypes.c_void_p * len(ts))(*[_dev(t, f"{what}[{i}]") for i, t in enumerate(ts)])
+
+
+def mc2_all_gather_mm(x_chunks: Sequence[torch.Tensor], x2: torch.Tensor, *, x2_is_nk: bool = False,
+                      bias: Optional[torch.Tensor] = None, gather_output: bool = True,
+                      out: Optional[torch.Tensor] = None, gathered: Optional[torch.Tensor] = None,
+                      stream=None):
+    """AllGatherMatmul on the rank chunks already resident on this GPU.
+
+    x_chunks: world_size tensors (m_local, k); x2 (k, n), or w (n, k) with
+    ``x2_is_nk``.  Returns (out (m, n), gathered (m, k) or None).
+    """
+    R = len(x_chunks)
+    m_local, k = x_chunks[0].shape
+    n = x2.shape[0] if x2_is_nk else x2.shape[1]
+    dt = x_chunks[0].dtype
+    if out is None:
+        out = torch.empty((R * m_local, n), dtype=dt, device=x_chunks[0].device)
+    if gather_output and gathered is None:
+        gathered = torch.empty((R * m_local, k), dtype=dt, device=x_chunks[0].device)
+    ptrs = _ptrs(x_chunks, "x_chunks")
+    st = lib().mc2_all_gather_mm(ptrs, R, m_local, k, _dev(x2, "x2"), n, int(x2_is_nk), _opt(bias, "bias"),
+                                 _dtype_code(dt), int(gather_output), _dev(out, "out"),
+                                 _opt(gathered, "gathered") if gather_output else None, _stream(stream))
+    _check(st)
+    return out, (gathered if gather_output else None)
+
+
+def mc2_alltoall_quant_mm_workspace(rank_size: int, bs_local: int, h: int, n: int, x1_quant_mode: int,
+                                    x1_dtype: torch.dtype) -> int:
+    nbytes = ctypes.c_size_t(0)
+    _check(lib().mc2_alltoall_quant_mm_workspace(rank_size, bs_local, h, n, x1_quant_mode, _dtype_code(x1_dtype),
+                                                 ctypes.byref(nbytes)))
+    return int(nbytes.value)
+
+
+def mc2_alltoall_quant_mm(chunks: Sequence[torch.Tensor], x2: torch.Tensor, x2_scale: torch.Tensor,
+                          bias: torch.Tensor, *, x1_quant_mode: int, x1_scale: Optional[torch.Tensor] = None,
+                          x2_quant_mode: int = QUANT_PERCHANNEL, out: Optional[torch.Tensor] = None,
+                          q_out: Optional[torch.Tensor] = None, x1_scale_out: Optional[torch.Tensor] = None,
+                          acc_out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                          stream=None) -> dict:
+    """AlltoAllQuantMatmul on the received chunks already resident on this GPU.
+
+    chunks: rank_size tensors (bs_local, h) (bf16/fp16 for mode 7, int8 for
+    mode 3); x2 int8 (rank_size*h, n); x2_scale fp32 (n); bias fp32/bf16 (n).
+    Returns dict(out, q, x1_scale, acc) with the optional outputs that were given.
+    """
+    R = len(chunks)
+    bs_local, h = chunks[0].shape
+    n = x2.shape[1]
+    dev = chunks[0].device
+    x1_dtype = chunks[0].dtype
+    if out is None:
+        out = torch.empty((bs_local, n), dtype=torch.bfloat16, device=dev)
+    need = mc2_alltoall_quant_mm_workspace(R, bs_local, h, n, x1_quant_mode, x1_dtype)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    ptrs = _ptrs(chunks, "chunks")
+    st = lib().mc2_alltoall_quant_mm(ptrs, R, bs_local, h, _dtype_code(x1_dtype), _opt(x1_scale, "x1_scale"),
+                                     _dev(x2, "x2"), _dev(x2_scale, "x2_scale"), _dev(bias, "bias"),
+                                     _dtype_code(bias.dtype), x1_quant_mode, x2_quant_mode, n, _dev(out, "out"),
+                                     _opt(q_out, "q_out"), _opt(x1_scale_out, "x1_scale_out"),
+                                     _opt(acc_out, "acc_out"), _dev(workspace, "workspace"),
+                                     workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st)
+    return {"out": out, "q": q_out, "x1_scale": x1_scale_out, "acc": acc_out}
+
+
+def mc2_device_status() -> int:
+    """Synchronise and return (and clear) the kernels' bounded-wait status."""
+    return int(lib().mc2_device_status())
+
+
+__all__ = [
+    "Mc2Error", "lib", "library_path", "status_str", "last_error", "mc2_all_gather_mm",
+    "mc2_alltoall_quant_mm_workspace", "mc2_alltoall_quant_mm", "mc2_device_status",
+    "MC2_OK", "MC2_ERR_NULL", "MC2_ERR_SHAPE", "MC2_ERR_DTYPE", "MC2_ERR_UNSUPPORTED", "MC2_ERR_WORKSPACE",
+    "MC2_ERR_CUDA", "MC2_ERR_TIMEOUT", "MC2_F16", "MC2_BF16", "MC2_F32", "MC2_I8",
+    "QUANT_PERCHANNEL", "QUANT_PERTOKEN", "QUANT_PERTOKEN_DYNAMIC",
+]

@@ -1,0 +1,32 @@
+// internal.h -- declarations shared by the library's translation units
+// (not part of the public C ABI).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace mc2 {
+
+struct ChunkPtrs {
+    const void *p[8];
+};
+
+struct GemmParams;
+
+// GEMM launch: kind selects the instantiation.
+enum GemmKind : int { GEMM_F16 = 0, GEMM_BF16 = 1, GEMM_INT_AS_F16 = 2 };
+cudaError_t launch_gemm(GemmKind kind, const GemmParams &p, int num_sms, cudaStream_t stream);
+int gemm_smem_bytes();
+int read_and_clear_gemm_status(int *status);
+
+cudaError_t launch_quant_pertoken(const ChunkPtrs &chunks, int rank_size, int64_t bs_local, int h, bool bf16,
+                                  const void *smooth, __half *qh, int8_t *q_out, float *scale_out, int num_sms,
+                                  cudaStream_t stream);
+cudaError_t launch_widen_i8(const int8_t *src, __half *dst, int64_t count, int num_sms, cudaStream_t stream);
+cudaError_t launch_permute_widen_i8(const ChunkPtrs &chunks, int rank_size, int64_t bs_local, int h, __half *dst,
+                                    int8_t *q_out, int num_sms, cudaStream_t stream);
+
+}  // namespace mc2

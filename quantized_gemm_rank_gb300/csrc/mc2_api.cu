@@ -1,0 +1,327 @@
+// mc2_api.cu -- the C ABI declared in include/mc2_gb300.h: argument
+// validation (constraints of "torch_npu.npu_all_gather_base_mm" 约束说明 and
+// "aclnnAlltoAllQuantMatmul" 约束说明, plus this kernel's alignment needs),
+// TMA tensor-map encoding, workspace carving and stream-ordered launches.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "gemm_tcgen05.cuh"
+#include "internal.h"
+#include "mc2_gb300.h"
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+int fail(int status, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+    va_end(ap);
+    return status;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ------------------------------------------------------------------ driver entry point
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+// 2-D map over a row-major (outer, inner) matrix with 16-bit elements and a
+// 128-byte swizzle; out-of-range box elements read as zero.
+bool make_map16(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, uint32_t box_inner,
+                uint32_t box_outer) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {inner * 2};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+struct DeviceInfo {
+    int device = -1;
+    int num_sms = 0;
+};
+
+int current_device(DeviceInfo *info) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(MC2_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    static int sms_cache[64] = {0};
+    int sms = dev < 64 ? sms_cache[dev] : 0;
+    if (sms == 0) {
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return fail(MC2_ERR_CUDA, "cudaDeviceGetAttribute: %s", cudaGetErrorString(e));
+        int major = 0, minor = 0;
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        if (major != 10 || minor != 3)
+            return fail(MC2_ERR_UNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a only", dev,
+                        major, minor);
+        if (dev < 64) sms_cache[dev] = sms;
+    }
+    info->device = dev;
+    info->num_sms = sms;
+    return MC2_OK;
+}
+
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per bounded device-side wait
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+struct A2AWorkspace {
+    size_t x2h = 0, ah = 0, scale = 0, total = 0;
+};
+
+A2AWorkspace a2a_layout(int rank_size, int64_t bs_local, int64_t h, int64_t n) {
+    A2AWorkspace w;
+    const size_t K = static_cast<size_t>(rank_size) * static_cast<size_t>(h);
+    w.x2h = 0;
+    w.ah = align_up(w.x2h + K * static_cast<size_t>(n) * 2, 256);
+    w.scale = align_up(w.ah + static_cast<size_t>(bs_local) * K * 2, 256);
+    w.total = align_up(w.scale + static_cast<size_t>(bs_local) * 4, 256);
+    return w;
+}
+
+int validate_a2a(int rank_size, int64_t bs_local, int64_t h, int64_t n, int x1_quant_mode, int x1_dtype) {
+    if (rank_size != 2 && rank_size != 4 && rank_size != 8)
+        return fail(MC2_ERR_SHAPE, "rank_size must be 2, 4 or 8 (got %d)", rank_size);
+    if (bs_local < 1 || h < 1 || n < 1)
+        return fail(MC2_ERR_SHAPE, "empty tensors are not supported (bs_local=%lld h=%lld n=%lld)",
+                    (long long)bs_local, (long long)h, (long long)n);
+    if (bs_local * rank_size > INT32_MAX) return fail(MC2_ERR_SHAPE, "BS = rank_size*bs_local exceeds INT32_MAX");
+    if (n > INT32_MAX) return fail(MC2_ERR_SHAPE, "N exceeds INT32_MAX");
+    const int64_t K = static_cast<int64_t>(rank_size) * h;
+    if (K > 35000) return fail(MC2_ERR_SHAPE, "rank_size*H = %lld is outside [1, 35000]", (long long)K);
+    if (K % 16 != 0) return fail(MC2_ERR_SHAPE, "rank_size*H = %lld is not a multiple of 16", (long long)K);
+    if (x1_quant_mode == MC2_QUANT_PERTOKEN_DYNAMIC) {
+        if (x1_dtype != MC2_BF16 && x1_dtype != MC2_F16)
+            return fail(MC2_ERR_DTYPE, "x1QuantMode 7 needs bf16 or fp16 chunks (got dtype %d)", x1_dtype);
+    } else if (x1_quant_mode == MC2_QUANT_PERTOKEN) {
+        if (x1_dtype != MC2_I8) return fail(MC2_ERR_DTYPE, "x1QuantMode 3 needs int8 chunks (got dtype %d)", x1_dtype);
+    } else {
+        return fail(MC2_ERR_DTYPE, "x1QuantMode must be 3 (pertoken) or 7 (pertoken dynamic), got %d", x1_quant_mode);
+    }
+    if (n % 16 != 0) return fail(MC2_ERR_UNSUPPORTED, "this kernel needs N %% 16 == 0 (got %lld)", (long long)n);
+    return MC2_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *mc2_status_str(int status) {
+    switch (status) {
+        case MC2_OK: return "MC2_OK";
+        case MC2_ERR_NULL: return "MC2_ERR_NULL";
+        case MC2_ERR_SHAPE: return "MC2_ERR_SHAPE";
+        case MC2_ERR_DTYPE: return "MC2_ERR_DTYPE";
+        case MC2_ERR_UNSUPPORTED: return "MC2_ERR_UNSUPPORTED";
+        case MC2_ERR_WORKSPACE: return "MC2_ERR_WORKSPACE";
+        case MC2_ERR_CUDA: return "MC2_ERR_CUDA";
+        case MC2_ERR_TIMEOUT: return "MC2_ERR_TIMEOUT";
+    }
+    return "MC2_ERR_UNKNOWN";
+}
+
+const char *mc2_last_error(void) { return g_last_error; }
+
+int mc2_device_status(void) {
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return fail(MC2_ERR_CUDA, "cudaDeviceSynchronize: %s", cudaGetErrorString(e));
+    int st = 0;
+    if (mc2::read_and_clear_gemm_status(&st) != 0) return fail(MC2_ERR_CUDA, "reading the device status word failed");
+    if (st != 0) return fail(MC2_ERR_TIMEOUT, "a bounded wait inside the GEMM kernel gave up");
+    return MC2_OK;
+}
+
+int mc2_all_gather_mm(const void *const *x_chunks, int world_size, int64_t m_local, int64_t k, const void *x2,
+                      int64_t n, int x2_is_nk, const void *bias, int dtype, int gather_output, void *out,
+                      void *gathered, void *stream) {
+    g_last_error[0] = '\0';
+    if (!x_chunks) return fail(MC2_ERR_NULL, "x_chunks is NULL");
+    if (!x2) return fail(MC2_ERR_NULL, "x2 is NULL");
+    if (!out) return fail(MC2_ERR_NULL, "out is NULL");
+    if (world_size != 2 && world_size != 4 && world_size != 8)
+        return fail(MC2_ERR_SHAPE, "world_size must be 2, 4 or 8 (got %d)", world_size);
+    for (int r = 0; r < world_size; ++r)
+        if (!x_chunks[r]) return fail(MC2_ERR_NULL, "x_chunks[%d] is NULL", r);
+    if (dtype != MC2_F16 && dtype != MC2_BF16)
+        return fail(MC2_ERR_DTYPE, "dtype must be MC2_F16 or MC2_BF16 (got %d)", dtype);
+    if (m_local < 1 || n < 1)
+        return fail(MC2_ERR_SHAPE, "empty tensors are not supported (m_local=%lld n=%lld)", (long long)m_local,
+                    (long long)n);
+    if (k < 256 || k >= 65535) return fail(MC2_ERR_SHAPE, "k must be in [256, 65535) (got %lld)", (long long)k);
+    if (gather_output && !gathered) return fail(MC2_ERR_NULL, "gather_output is set but gathered is NULL");
+    if (!gather_output && gathered) return fail(MC2_ERR_SHAPE, "gathered must be NULL when gather_output is 0");
+    const int64_t m = m_local * world_size;
+    if (m > INT32_MAX || n > INT32_MAX) return fail(MC2_ERR_SHAPE, "m or n exceeds INT32_MAX");
+    if (m_local % 8 != 0)
+        return fail(MC2_ERR_UNSUPPORTED, "this kernel needs m_local %% 8 == 0 (got %lld)", (long long)m_local);
+    if (k % 8 != 0 || n % 8 != 0)
+        return fail(MC2_ERR_UNSUPPORTED, "this kernel needs k %% 8 == 0 and n %% 8 == 0 (k=%lld n=%lld)",
+                    (long long)k, (long long)n);
+    for (int r = 0; r < world_size; ++r)
+        if (!aligned16(x_chunks[r])) return fail(MC2_ERR_UNSUPPORTED, "x_chunks[%d] is not 16-byte aligned", r);
+    if (!aligned16(x2) || !aligned16(out) || (bias && !aligned16(bias)) || (gathered && !aligned16(gathered)))
+        return fail(MC2_ERR_UNSUPPORTED, "x2, out, bias and gathered must be 16-byte aligned");
+
+    DeviceInfo dev;
+    if (int st = current_device(&dev)) return st;
+
+    mc2::GemmParams p;
+    memset(&p, 0, sizeof(p));
+    // A: one map per rank's chunk, box rows = the largest power of two dividing
+    // both m_local and the 128-row tile, so that no box crosses a chunk.
+    int box_rows = mc2::kBM;
+    while (m_local % box_rows != 0) box_rows >>= 1;
+    for (int r = 0; r < world_size; ++r)
+        if (!make_map16(&p.a_maps[r], x_chunks[r], k, m_local, mc2::kBK, box_rows))
+            return fail(MC2_ERR_CUDA, "cuTensorMapEncodeTiled failed for x_chunks[%d]", r);
+    p.num_a_maps = world_size;
+    p.a_mode = mc2::A_MCONCAT;
+    p.a_box_rows = box_rows;
+    p.m_local = static_cast<int>(m_local);
+    if (x2_is_nk) {
+        if (!make_map16(&p.b_map, x2, k, n, mc2::kBK, mc2::kBN))
+            return fail(MC2_ERR_CUDA, "cuTensorMapEncodeTiled failed for x2 (n, k)");
+        p.b_mn_major = 0;
+    } else {
+        if (!make_map16(&p.b_map, x2, n, k, 64, mc2::kBK))
+            return fail(MC2_ERR_CUDA, "cuTensorMapEncodeTiled failed for x2 (k, n)");
+        p.b_mn_major = 1;
+    }
+    if (gather_output) {
+        if (!make_map16(&p.g_map, gathered, k, m, mc2::kBK, mc2::kBM))
+            return fail(MC2_ERR_CUDA, "cuTensorMapEncodeTiled failed for gathered");
+        p.gather = 1;
+    }
+    p.m = static_cast<int>(m);
+    p.n = static_cast<int>(n);
+    p.k = static_cast<int>(k);
+    p.kblock_tiles = 1;
+    p.out = out;
+    p.bias16 = bias;
+    p.wait_limit_ns = kWaitLimitNs;
+    cudaError_t e = mc2::launch_gemm(dtype == MC2_BF16 ? mc2::GEMM_BF16 : mc2::GEMM_F16, p, dev.num_sms,
+                                     static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(MC2_ERR_CUDA, "GEMM launch: %s", cudaGetErrorString(e));
+    return MC2_OK;
+}
+
+int mc2_alltoall_quant_mm_workspace(int rank_size, int64_t bs_local, int64_t h, int64_t n, int x1_quant_mode,
+                                    int x1_dtype, size_t *bytes) {
+    g_last_error[0] = '\0';
+    if (!bytes) return fail(MC2_ERR_NULL, "bytes is NULL");
+    if (int st = validate_a2a(rank_size, bs_local, h, n, x1_quant_mode, x1_dtype)) return st;
+    *bytes = a2a_layout(rank_size, bs_local, h, n).total;
+    return MC2_OK;
+}
+
+int mc2_alltoall_quant_mm(const void *const *chunks, int rank_size, int64_t bs_local, int64_t h, int x1_dtype,
+                          const void *x1_scale, const int8_t *x2, const float *x2_scale, const void *bias,
+                          int bias_dtype, int x1_quant_mode, int x2_quant_mode, int64_t n, void *out,
+                          int8_t *q_out, float *x1_scale_out, int32_t *acc_out, void *workspace,
+                          size_t workspace_bytes, void *stream) {
+    g_last_error[0] = '\0';
+    if (!chunks) return fail(MC2_ERR_NULL, "chunks is NULL");
+    if (!x2) return fail(MC2_ERR_NULL, "x2 is NULL");
+    if (!x2_scale) return fail(MC2_ERR_NULL, "x2_scale is NULL");
+    if (!out) return fail(MC2_ERR_NULL, "output is NULL");
+    if (!bias) return fail(MC2_ERR_NULL, "bias is NULL (biasOptional may not be NULL on this op)");
+    if (int st = validate_a2a(rank_size, bs_local, h, n, x1_quant_mode, x1_dtype)) return st;
+    for (int r = 0; r < rank_size; ++r)
+        if (!chunks[r]) return fail(MC2_ERR_NULL, "chunks[%d] is NULL", r);
+    if (x2_quant_mode != MC2_QUANT_PERCHANNEL)
+        return fail(MC2_ERR_DTYPE, "x2QuantMode must be 2 (perchannel), got %d", x2_quant_mode);
+    if (bias_dtype != MC2_F32 && bias_dtype != MC2_BF16)
+        return fail(MC2_ERR_DTYPE, "bias dtype must be MC2_F32 or MC2_BF16 (got %d)", bias_dtype);
+    if (x1_quant_mode == MC2_QUANT_PERTOKEN && !x1_scale)
+        return fail(MC2_ERR_NULL, "x1QuantMode 3 needs the per-token x1 scale");
+    for (int r = 0; r < rank_size; ++r)
+        if (!aligned16(chunks[r])) return fail(MC2_ERR_UNSUPPORTED, "chunks[%d] is not 16-byte aligned", r);
+    if (!aligned16(x2) || !aligned16(out) || !aligned16(x2_scale) || !aligned16(bias) ||
+        (x1_scale && !aligned16(x1_scale)) || (q_out && !aligned16(q_out)) || (acc_out && !aligned16(acc_out)) ||
+        (x1_scale_out && !aligned16(x1_scale_out)))
+        return fail(MC2_ERR_UNSUPPORTED, "all tensors must be 16-byte aligned");
+    const A2AWorkspace ws = a2a_layout(rank_size, bs_local, h, n);
+    if (!workspace || workspace_bytes < ws.total)
+        return fail(MC2_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", ws.total,
+                    workspace ? workspace_bytes : (size_t)0);
+    if (!aligned16(workspace)) return fail(MC2_ERR_UNSUPPORTED, "workspace must be 16-byte aligned");
+
+    DeviceInfo dev;
+    if (int st = current_device(&dev)) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t *wsb = static_cast<uint8_t *>(workspace);
+    __half *x2h = reinterpret_cast<__half *>(wsb + ws.x2h);
+    __half *ah = reinterpret_cast<__half *>(wsb + ws.ah);
+    float *scale = x1_scale_out ? x1_scale_out : reinterpret_cast<float *>(wsb + ws.scale);
+    const int64_t K = static_cast<int64_t>(rank_size) * h;
+    mc2::ChunkPtrs cp;
+    memset(&cp, 0, sizeof(cp));
+    for (int r = 0; r < rank_size; ++r) cp.p[r] = chunks[r];
+
+    cudaError_t e;
+    if (x1_quant_mode == MC2_QUANT_PERTOKEN_DYNAMIC) {
+        e = mc2::launch_quant_pertoken(cp, rank_size, bs_local, static_cast<int>(h), x1_dtype == MC2_BF16, x1_scale,
+                                       ah, q_out, scale, dev.num_sms, s);
+    } else {
+        e = mc2::launch_permute_widen_i8(cp, rank_size, bs_local, static_cast<int>(h), ah, q_out, dev.num_sms, s);
+        if (e == cudaSuccess && x1_scale_out)
+            e = cudaMemcpyAsync(x1_scale_out, x1_scale, static_cast<size_t>(bs_local) * 4, cudaMemcpyDeviceToDevice, s);
+        scale = const_cast<float *>(static_cast<const float *>(x1_scale));
+    }
+    if (e != cudaSuccess) return fail(MC2_ERR_CUDA, "prologue launch: %s", cudaGetErrorString(e));
+    e = mc2::launch_widen_i8(x2, x2h, K * n, dev.num_sms, s);
+    if (e != cudaSuccess) return fail(MC2_ERR_CUDA, "x2 widening launch: %s", cudaGetErrorString(e));
+
+    mc2::GemmParams p;
+    memset(&p, 0, sizeof(p));
+    if (!make_map16(&p.a_maps[0], ah, K, bs_local, mc2::kBK, mc2::kBM))
+        return fail(MC2_ERR_CUDA, "cuTensorMapEncodeTiled failed for the quantised activations");
+    if (!make_map16(&p.b_map, x2h, n, K, 64, mc2::kBK))
+        return fail(MC2_ERR_CUDA, "cuTensorMapEncodeTiled failed for x2");
+    p.num_a_maps = 1;
+    p.a_mode = mc2::A_SINGLE;
+    p.b_mn_major = 1;
+    p.m = static_cast<int>(bs_local);
+    p.n = static_cast<int>(n);
+    p.k = static_cast<int>(K);
+    p.kblock_tiles = 1024 / mc2::kBK;
+    p.out = out;
+    p.x1_scale = scale;
+    p.x2_scale = x2_scale;
+    p.bias_q = bias;
+    p.bias_q_bf16 = bias_dtype == MC2_BF16;
+    p.acc_out = acc_out;
+    p.wait_limit_ns = kWaitLimitNs;
+    e = mc2::launch_gemm(mc2::GEMM_INT_AS_F16, p, dev.num_sms, s);
+    if (e != cudaSuccess) return fail(MC2_ERR_CUDA, "GEMM launch: %s", cudaGetErrorString(e));
+    return MC2_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,237 @@
+// quant_kernels.cu -- the memory-bound steps of AlltoAllQuantMatmul
+// ("aclnnAlltoAllQuantMatmul", 功能说明 / 计算公式):
+//   * the per-token dynamic quant prologue of the dynamic-quant scenario,
+//     reading the rank's received chunks through the permute(1,0,2) index
+//     (permuted[t, r*h + j] = chunk_r[t, j]) without materialising the
+//     permuted bf16/fp16 matrix;
+//   * the exact int8 -> fp16 widening of the int8 operands that the tensor
+//     cores consume (sm_103a has no integer tcgen05 MMA).
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <cstdint>
+
+#include "internal.h"
+
+namespace mc2 {
+
+namespace {
+
+template <bool kBF16>
+__device__ __forceinline__ float to_f32(uint16_t v) {
+    if constexpr (kBF16) {
+        return __uint_as_float(static_cast<uint32_t>(v) << 16);
+    } else {
+        return __half2float(__ushort_as_half(v));
+    }
+}
+
+__device__ __forceinline__ float block_max(float v, float *red) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+        v = lane < static_cast<int>(blockDim.x >> 5) ? red[lane] : 0.0f;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+        if (lane == 0) red[0] = v;
+    }
+    __syncthreads();
+    const float r = red[0];
+    __syncthreads();
+    return r;
+}
+
+// q = clamp(rne(y / scale), -127, 127); a zero scale (all-zero row) gives 0.
+__device__ __forceinline__ int quant1(float y, float scale) {
+    if (scale == 0.0f) return 0;
+    const int q = __float2int_rn(__fdiv_rn(y, scale));
+    return max(-127, min(127, q));
+}
+
+// One CTA per permuted row t.  Pass 1: y = x * smooth (fp32), row absmax.
+// scale = absmax / 127 (IEEE division).  Pass 2 (row re-read from L1/L2):
+// q, written as exact fp16 (GEMM operand) and optionally as int8.
+template <bool kBF16>
+__global__ void __launch_bounds__(256) quant_pertoken_kernel(ChunkPtrs chunks, int h, int64_t bs_local, int rank_size,
+                                                             const uint16_t *__restrict__ smooth,
+                                                             __half *__restrict__ qh, int8_t *__restrict__ q_out,
+                                                             float *__restrict__ scale_out) {
+    __shared__ float red[32];
+    const int K = rank_size * h;
+    const bool vec = (h % 8) == 0;
+    for (int64_t t = blockIdx.x; t < bs_local; t += gridDim.x) {
+        float amax = 0.0f;
+        if (vec) {
+            for (int v = threadIdx.x; v < K / 8; v += blockDim.x) {
+                const int c = v * 8;
+                const int r = c / h;
+                const int j = c - r * h;
+                const uint4 xv = __ldg(reinterpret_cast<const uint4 *>(
+                    static_cast<const uint16_t *>(chunks.p[r]) + t * h + j));
+                uint4 sv = make_uint4(0, 0, 0, 0);
+                if (smooth) sv = __ldg(reinterpret_cast<const uint4 *>(smooth + c));
+                const uint16_t *xe = reinterpret_cast<const uint16_t *>(&xv);
+                const uint16_t *se = reinterpret_cast<const uint16_t *>(&sv);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float y = smooth ? __fmul_rn(to_f32<kBF16>(xe[e]), to_f32<kBF16>(se[e]))
+                                           : to_f32<kBF16>(xe[e]);
+                    amax = fmaxf(amax, fabsf(y));
+                }
+            }
+        } else {
+            for (int c = threadIdx.x; c < K; c += blockDim.x) {
+                const int r = c / h;
+                const int j = c - r * h;
+                const float x = to_f32<kBF16>(static_cast<const uint16_t *>(chunks.p[r])[t * h + j]);
+                const float y = smooth ? __fmul_rn(x, to_f32<kBF16>(smooth[c])) : x;
+                amax = fmaxf(amax, fabsf(y));
+            }
+        }
+        amax = block_max(amax, red);
+        const float scale = __fdiv_rn(amax, 127.0f);
+        if (threadIdx.x == 0) scale_out[t] = scale;
+        __half *qrow = qh + t * K;
+        int8_t *orow = q_out ? q_out + t * K : nullptr;
+        if (vec) {
+            for (int v = threadIdx.x; v < K / 8; v += blockDim.x) {
+                const int c = v * 8;
+                const int r = c / h;
+                const int j = c - r * h;
+                const uint4 xv = __ldg(reinterpret_cast<const uint4 *>(
+                    static_cast<const uint16_t *>(chunks.p[r]) + t * h + j));
+                uint4 sv = make_uint4(0, 0, 0, 0);
+                if (smooth) sv = __ldg(reinterpret_cast<const uint4 *>(smooth + c));
+                const uint16_t *xe = reinterpret_cast<const uint16_t *>(&xv);
+                const uint16_t *se = reinterpret_cast<const uint16_t *>(&sv);
+                uint4 hv;
+                uint16_t *he = reinterpret_cast<uint16_t *>(&hv);
+                uint2 iv;
+                int8_t *ie = reinterpret_cast<int8_t *>(&iv);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float y = smooth ? __fmul_rn(to_f32<kBF16>(xe[e]), to_f32<kBF16>(se[e]))
+                                           : to_f32<kBF16>(xe[e]);
+                    const int q = quant1(y, scale);
+                    he[e] = __half_as_ushort(__int2half_rn(q));
+                    ie[e] = static_cast<int8_t>(q);
+                }
+                *reinterpret_cast<uint4 *>(qrow + c) = hv;
+                if (orow) *reinterpret_cast<uint2 *>(orow + c) = iv;
+            }
+        } else {
+            for (int c = threadIdx.x; c < K; c += blockDim.x) {
+                const int r = c / h;
+                const int j = c - r * h;
+                const float x = to_f32<kBF16>(static_cast<const uint16_t *>(chunks.p[r])[t * h + j]);
+                const float y = smooth ? __fmul_rn(x, to_f32<kBF16>(smooth[c])) : x;
+                const int q = quant1(y, scale);
+                qrow[c] = __int2half_rn(q);
+                if (orow) orow[c] = static_cast<int8_t>(q);
+            }
+        }
+    }
+}
+
+// int8 -> fp16, exact, 16 elements per thread-iteration.
+__global__ void __launch_bounds__(256) widen_i8_kernel(const int8_t *__restrict__ src, __half *__restrict__ dst,
+                                                       int64_t count) {
+    const int64_t nvec = count / 16;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < nvec; i += stride) {
+        const int4 v = __ldg(reinterpret_cast<const int4 *>(src) + i);
+        const int8_t *e = reinterpret_cast<const int8_t *>(&v);
+        uint4 o[2];
+        uint16_t *oe = reinterpret_cast<uint16_t *>(o);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) oe[j] = __half_as_ushort(__int2half_rn(e[j]));
+        reinterpret_cast<uint4 *>(dst)[2 * i] = o[0];
+        reinterpret_cast<uint4 *>(dst)[2 * i + 1] = o[1];
+    }
+    for (int64_t i = nvec * 16 + static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < count; i += stride)
+        dst[i] = __int2half_rn(src[i]);
+}
+
+// Permuted int8 chunks -> fp16 GEMM operand (and optionally the int8
+// permuted matrix): dst[t, r*h + j] = chunk_r[t, j].
+__global__ void __launch_bounds__(256) permute_widen_i8_kernel(ChunkPtrs chunks, int h, int64_t bs_local,
+                                                               int rank_size, __half *__restrict__ dst,
+                                                               int8_t *__restrict__ q_out) {
+    const int K = rank_size * h;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    if (h % 16 == 0) {
+        const int vpr = K / 16;
+        const int64_t total = bs_local * vpr;
+        for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += stride) {
+            const int64_t t = i / vpr;
+            const int c = static_cast<int>(i - t * vpr) * 16;
+            const int r = c / h;
+            const int j = c - r * h;
+            const int4 v = __ldg(reinterpret_cast<const int4 *>(static_cast<const int8_t *>(chunks.p[r]) + t * h + j));
+            const int8_t *e = reinterpret_cast<const int8_t *>(&v);
+            uint4 o[2];
+            uint16_t *oe = reinterpret_cast<uint16_t *>(o);
+#pragma unroll
+            for (int q = 0; q < 16; ++q) oe[q] = __half_as_ushort(__int2half_rn(e[q]));
+            uint4 *d = reinterpret_cast<uint4 *>(dst + t * K + c);
+            d[0] = o[0];
+            d[1] = o[1];
+            if (q_out) *reinterpret_cast<int4 *>(q_out + t * K + c) = v;
+        }
+    } else {
+        const int64_t total = bs_local * K;
+        for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += stride) {
+            const int64_t t = i / K;
+            const int c = static_cast<int>(i - t * K);
+            const int r = c / h;
+            const int j = c - r * h;
+            const int8_t v = static_cast<const int8_t *>(chunks.p[r])[t * h + j];
+            dst[i] = __int2half_rn(v);
+            if (q_out) q_out[i] = v;
+        }
+    }
+}
+
+int grid_for(int64_t work_items, int threads, int num_sms) {
+    int64_t g = (work_items + threads - 1) / threads;
+    const int64_t cap = static_cast<int64_t>(num_sms) * 16;
+    if (g > cap) g = cap;
+    if (g < 1) g = 1;
+    return static_cast<int>(g);
+}
+
+}  // namespace
+
+cudaError_t launch_quant_pertoken(const ChunkPtrs &chunks, int rank_size, int64_t bs_local, int h, bool bf16,
+                                  const void *smooth, __half *qh, int8_t *q_out, float *scale_out, int num_sms,
+                                  cudaStream_t stream) {
+    const int64_t rows_cap = static_cast<int64_t>(num_sms) * 64;
+    const int grid = static_cast<int>(bs_local < rows_cap ? bs_local : rows_cap);
+    if (bf16)
+        quant_pertoken_kernel<true><<<grid, 256, 0, stream>>>(chunks, h, bs_local, rank_size,
+                                                              static_cast<const uint16_t *>(smooth), qh, q_out,
+                                                              scale_out);
+    else
+        quant_pertoken_kernel<false><<<grid, 256, 0, stream>>>(chunks, h, bs_local, rank_size,
+                                                               static_cast<const uint16_t *>(smooth), qh, q_out,
+                                                               scale_out);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_widen_i8(const int8_t *src, __half *dst, int64_t count, int num_sms, cudaStream_t stream) {
+    widen_i8_kernel<<<grid_for(count / 16 + 1, 256, num_sms), 256, 0, stream>>>(src, dst, count);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_permute_widen_i8(const ChunkPtrs &chunks, int rank_size, int64_t bs_local, int h, __half *dst,
+                                    int8_t *q_out, int num_sms, cudaStream_t stream) {
+    const int64_t items = bs_local * static_cast<int64_t>(rank_size) * h / ((h % 16 == 0) ? 16 : 1);
+    permute_widen_i8_kernel<<<grid_for(items, 256, num_sms), 256, 0, stream>>>(chunks, h, bs_local, rank_size, dst,
+                                                                              q_out);
+    return cudaGetLastError();
+}
+
+}  // namespace mc2

@@ -1,0 +1,162 @@
+"""The C-ABI boundary without a GPU: the library loads, exports every function
+that include/*.h declares, and rejects each violated constraint with the right
+status before touching CUDA.
+
+Constraints come from "torch_npu.npu_all_gather_base_mm" (参数说明/约束说明:
+world_size 2/4/8, k in [256, 65535), 2-D fp16/bf16 operands of one dtype) and
+"aclnnAlltoAllQuantMatmul" (约束说明: rankSize 2/4/8, BS and N <= INT32_MAX, no
+empty tensors, non-null x1/x2/x2Scale/output/bias, x1QuantMode 3 or 7,
+x2QuantMode 2, rankSize*H a multiple of 16 in [1, 35000]).
+"""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+import torch
+
+import quantized_gemm_rank_gb300 as mc2
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+FAKE = 0x10000  # a 16-byte-aligned non-null address; validation must never dereference it
+
+
+def declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names |= set(re.findall(r"\b(mc2_\w+)\s*\(", text))
+    return sorted(names)
+
+
+def test_library_exports_every_declared_symbol():
+    L = mc2.lib()
+    names = declared_functions()
+    assert "mc2_all_gather_mm" in names and "mc2_alltoall_quant_mm" in names
+    for name in names:
+        assert hasattr(L, name), name
+
+
+def test_status_strings():
+    assert mc2.status_str(0) == "MC2_OK"
+    assert mc2.status_str(mc2.MC2_ERR_TIMEOUT) == "MC2_ERR_TIMEOUT"
+    assert mc2.status_str(-99) == "MC2_ERR_UNKNOWN"
+
+
+def ag_call(world_size=2, m_local=16, k=256, n=64, x2_is_nk=0, bias=None, dtype=mc2.MC2_BF16, gather=1,
+            chunks=None, x2=FAKE, out=FAKE, gathered=FAKE):
+    if chunks is None:
+        chunks = [FAKE] * max(world_size, 1)
+    arr = (ctypes.c_void_p * len(chunks))(*chunks)
+    return mc2.lib().mc2_all_gather_mm(arr, world_size, m_local, k, x2, n, x2_is_nk, bias, dtype, gather, out,
+                                       gathered if gather else None, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(world_size=3), mc2.MC2_ERR_SHAPE),
+    (dict(world_size=1), mc2.MC2_ERR_SHAPE),
+    (dict(world_size=16), mc2.MC2_ERR_SHAPE),
+    (dict(k=255), mc2.MC2_ERR_SHAPE),
+    (dict(k=65535), mc2.MC2_ERR_SHAPE),
+    (dict(m_local=0), mc2.MC2_ERR_SHAPE),
+    (dict(n=0), mc2.MC2_ERR_SHAPE),
+    (dict(dtype=mc2.MC2_F32), mc2.MC2_ERR_DTYPE),
+    (dict(dtype=mc2.MC2_I8), mc2.MC2_ERR_DTYPE),
+    (dict(x2=None), mc2.MC2_ERR_NULL),
+    (dict(out=None), mc2.MC2_ERR_NULL),
+    (dict(chunks=[FAKE, None]), mc2.MC2_ERR_NULL),
+    (dict(gathered=None), mc2.MC2_ERR_NULL),
+    (dict(m_local=12), mc2.MC2_ERR_UNSUPPORTED),
+    (dict(k=260), mc2.MC2_ERR_UNSUPPORTED),
+    (dict(n=60), mc2.MC2_ERR_UNSUPPORTED),
+    (dict(x2=FAKE + 8), mc2.MC2_ERR_UNSUPPORTED),
+    (dict(chunks=[FAKE, FAKE + 2]), mc2.MC2_ERR_UNSUPPORTED),
+])
+def test_all_gather_rejects(kw, status):
+    assert ag_call(**kw) == status
+    assert mc2.last_error() != ""
+
+
+def test_all_gather_k_bounds_accepted_by_validation():
+    # k = 256 and k = 65528 (< 65535, multiple of 8) pass validation; without a GPU the
+    # call then fails at the first CUDA call, never earlier.
+    if torch.cuda.is_available():
+        pytest.skip("would launch on a real device with fake pointers")
+    for k in (256, 65528):
+        assert ag_call(k=k) == mc2.MC2_ERR_CUDA, mc2.last_error()
+
+
+def test_all_gather_gather_flag_consistency():
+    arr = (ctypes.c_void_p * 2)(FAKE, FAKE)
+    st = mc2.lib().mc2_all_gather_mm(arr, 2, 16, 256, FAKE, 64, 0, None, mc2.MC2_BF16, 0, FAKE, FAKE, None)
+    assert st == mc2.MC2_ERR_SHAPE
+
+
+def a2a_call(rank_size=2, bs_local=16, h=64, x1_dtype=mc2.MC2_BF16, x1_scale=None, x2=FAKE, x2_scale=FAKE,
+             bias=FAKE, bias_dtype=mc2.MC2_F32, mode=7, mode2=2, n=64, out=FAKE, ws=FAKE, ws_bytes=1 << 40,
+             chunks=None):
+    if chunks is None:
+        chunks = [FAKE] * max(rank_size, 1)
+    arr = (ctypes.c_void_p * len(chunks))(*chunks)
+    return mc2.lib().mc2_alltoall_quant_mm(arr, rank_size, bs_local, h, x1_dtype, x1_scale, x2, x2_scale, bias,
+                                           bias_dtype, mode, mode2, n, out, None, None, None, ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(rank_size=3), mc2.MC2_ERR_SHAPE),
+    (dict(rank_size=16), mc2.MC2_ERR_SHAPE),
+    (dict(bs_local=0), mc2.MC2_ERR_SHAPE),
+    (dict(h=0), mc2.MC2_ERR_SHAPE),
+    (dict(n=0), mc2.MC2_ERR_SHAPE),
+    (dict(bs_local=2 ** 30, rank_size=2), mc2.MC2_ERR_SHAPE),          # BS = 2^31 > INT32_MAX
+    (dict(n=2 ** 31), mc2.MC2_ERR_SHAPE),
+    (dict(rank_size=8, h=4376), mc2.MC2_ERR_SHAPE),                     # R*H = 35008 > 35000
+    (dict(rank_size=2, h=12), mc2.MC2_ERR_SHAPE),                       # R*H = 24, not % 16
+    (dict(mode=1), mc2.MC2_ERR_DTYPE),
+    (dict(mode=0), mc2.MC2_ERR_DTYPE),
+    (dict(mode2=1), mc2.MC2_ERR_DTYPE),
+    (dict(mode=7, x1_dtype=mc2.MC2_I8), mc2.MC2_ERR_DTYPE),
+    (dict(mode=3, x1_dtype=mc2.MC2_BF16, x1_scale=FAKE), mc2.MC2_ERR_DTYPE),
+    (dict(bias_dtype=mc2.MC2_I8), mc2.MC2_ERR_DTYPE),
+    (dict(mode=3, x1_dtype=mc2.MC2_I8, x1_scale=None), mc2.MC2_ERR_NULL),
+    (dict(x2=None), mc2.MC2_ERR_NULL),
+    (dict(x2_scale=None), mc2.MC2_ERR_NULL),
+    (dict(bias=None), mc2.MC2_ERR_NULL),
+    (dict(out=None), mc2.MC2_ERR_NULL),
+    (dict(chunks=[FAKE, None]), mc2.MC2_ERR_NULL),
+    (dict(ws=None), mc2.MC2_ERR_WORKSPACE),
+    (dict(ws_bytes=16), mc2.MC2_ERR_WORKSPACE),
+    (dict(n=40), mc2.MC2_ERR_UNSUPPORTED),
+    (dict(out=FAKE + 4), mc2.MC2_ERR_UNSUPPORTED),
+])
+def test_alltoall_rejects(kw, status):
+    assert a2a_call(**kw) == status, mc2.last_error()
+    assert mc2.last_error() != ""
+
+
+def test_alltoall_boundary_values_accepted_by_validation():
+    if torch.cuda.is_available():
+        pytest.skip("would launch on a real device with fake pointers")
+    # R*H = 35000 is allowed by the page but is not a multiple of 16 -> shape error;
+    # R*H = 34992 (largest multiple of 16 <= 35000) passes validation
+    assert a2a_call(rank_size=8, h=4375) == mc2.MC2_ERR_SHAPE
+    assert a2a_call(rank_size=8, h=4374) == mc2.MC2_ERR_CUDA, mc2.last_error()
+    assert a2a_call(rank_size=2, h=8) == mc2.MC2_ERR_CUDA, mc2.last_error()  # R*H = 16
+
+
+def test_workspace_query():
+    nbytes = mc2.mc2_alltoall_quant_mm_workspace(8, 4096, 1024, 4096, 7, torch.bfloat16)
+    assert nbytes >= 8192 * 4096 * 2 + 4096 * 8192 * 2 + 4096 * 4
+    with pytest.raises(mc2.Mc2Error) as ei:
+        mc2.mc2_alltoall_quant_mm_workspace(3, 4096, 1024, 4096, 7, torch.bfloat16)
+    assert ei.value.status == mc2.MC2_ERR_SHAPE
+
+
+def test_binding_refuses_cpu_tensors():
+    x = [torch.zeros(16, 256, dtype=torch.bfloat16)] * 2
+    with pytest.raises(ValueError):
+        mc2.mc2_all_gather_mm(x, torch.zeros(256, 64, dtype=torch.bfloat16),
+                              out=torch.zeros(32, 64, dtype=torch.bfloat16),
+                              gathered=torch.zeros(32, 256, dtype=torch.bfloat16))

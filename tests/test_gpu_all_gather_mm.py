@@ -1,0 +1,94 @@
+"""GPU parity of mc2_all_gather_mm (C ABI) against the CPU oracle.
+
+"torch_npu.npu_all_gather_base_mm": out = AllGather_m(input) @ x2 and the
+gathered input as the second output.  Cases span several 128 x 256 x 64 tiles
+with ragged m / n / k tails, chunk boundaries inside an m-tile, both x2 layouts,
+bias, both dtypes, and the full-size workloads on sampled rows.
+"""
+import pytest
+import torch
+
+import mc2_inputs
+import oracle
+import quantized_gemm_rank_gb300 as mc2
+from parity import assert_bits_equal, assert_close_16
+
+pytestmark = pytest.mark.gpu
+
+
+def run_gpu(inp, shape):
+    dev = torch.device("cuda")
+    chunks = [c.to(dev) for c in inp["chunks"]]
+    x2 = inp["x2"].to(dev)
+    bias = None if inp["bias"] is None else inp["bias"].to(dev)
+    out, gathered = mc2.mc2_all_gather_mm(chunks, x2, x2_is_nk=shape.x2_is_nk, bias=bias,
+                                          gather_output=shape.gather_output)
+    torch.cuda.synchronize()
+    assert mc2.mc2_device_status() == mc2.MC2_OK
+    return out.cpu(), (None if gathered is None else gathered.cpu())
+
+
+CASES = {
+    # name: (AGShape, note)
+    "ragged-bf16-kn": mc2_inputs.AGShape(world_size=4, m_local=72, k=328, n=520),
+    "ragged-fp16-nk-bias": mc2_inputs.AGShape(world_size=2, m_local=136, k=392, n=264, dtype=torch.float16,
+                                              x2_is_nk=True, bias=True),
+    "bf16-nk-bias-8ranks": mc2_inputs.AGShape(world_size=8, m_local=40, k=512, n=776, x2_is_nk=True, bias=True),
+    "fp16-kn-nogather": mc2_inputs.AGShape(world_size=2, m_local=256, k=256, n=512, dtype=torch.float16,
+                                           gather_output=False),
+    "bf16-kn-bias-tile-aligned": mc2_inputs.AGShape(world_size=2, m_local=256, k=1024, n=512, bias=True),
+    "ag-tiny": mc2_inputs.WORKLOADS["ag-tiny"],
+}
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_all_gather_mm_parity(name):
+    shape = CASES[name]
+    inp = mc2_inputs.ag_inputs(shape, seed=7)
+    out, gathered = run_gpu(inp, shape)
+    ref, ref_g = oracle.all_gather_mm(inp["chunks"], inp["x2"], x2_is_nk=shape.x2_is_nk, bias=inp["bias"],
+                                      gather_output=shape.gather_output)
+    assert_close_16(out, ref, f"{name}: out")
+    if shape.gather_output:
+        assert_bits_equal(gathered, ref_g, f"{name}: gathered")
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+@pytest.mark.parametrize("x2_is_nk", [False, True])
+def test_integer_valued_inputs_bit_exact(dtype, x2_is_nk):
+    """Small-integer operands: fp32 accumulation is exact, so the GPU must equal
+    the oracle bit for bit (any layout or indexing slip shows up here)."""
+    g = torch.Generator().manual_seed(5)
+    R, ml, k, n = 4, 40, 520, 264
+    chunks = [torch.randint(-4, 5, (ml, k), generator=g).to(dtype) for _ in range(R)]
+    x2 = torch.randint(-4, 5, (n, k) if x2_is_nk else (k, n), generator=g).to(dtype)
+    bias = torch.randint(-8, 9, (n,), generator=g).to(dtype)
+    dev = torch.device("cuda")
+    out, gathered = mc2.mc2_all_gather_mm([c.to(dev) for c in chunks], x2.to(dev), x2_is_nk=x2_is_nk,
+                                          bias=bias.to(dev))
+    ref, ref_g = oracle.all_gather_mm(chunks, x2, x2_is_nk=x2_is_nk, bias=bias)
+    assert_bits_equal(out, ref, "out")
+    assert_bits_equal(gathered, ref_g, "gathered")
+
+
+@pytest.mark.parametrize("name", ["ag-8x1024", "ag-4x4096"])
+def test_full_size_sampled_rows(name):
+    """The full-size workloads, in the launch configuration the benchmark times;
+    the oracle computes a seeded sample of rows that touches every chunk."""
+    shape = mc2_inputs.WORKLOADS[name]
+    inp = mc2_inputs.ag_inputs(shape, seed=0)
+    out, gathered = run_gpu(inp, shape)
+    rows = mc2_inputs.sample_rows(shape.m, 48, seed=1)
+    rows = torch.unique(torch.cat([rows, torch.tensor([0, shape.m_local - 1, shape.m_local, shape.m - 1])]))
+    ref, _ = oracle.all_gather_mm(inp["chunks"], inp["x2"], x2_is_nk=shape.x2_is_nk, bias=inp["bias"],
+                                  rows=rows, gather_output=False)
+    assert_close_16(out[rows], ref, f"{name}: out rows")
+    assert_bits_equal(gathered, torch.cat(inp["chunks"], 0), f"{name}: gathered")
+
+
+def test_repeat_calls_are_deterministic():
+    shape = CASES["ragged-bf16-kn"]
+    inp = mc2_inputs.ag_inputs(shape, seed=3)
+    a, _ = run_gpu(inp, shape)
+    b, _ = run_gpu(inp, shape)
+    assert_bits_equal(a, b, "repeat")

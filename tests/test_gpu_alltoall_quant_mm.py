@@ -1,0 +1,138 @@
+"""GPU parity of mc2_alltoall_quant_mm (C ABI) against the CPU oracle.
+
+"aclnnAlltoAllQuantMatmul" (计算公式): permute the received chunks, quantise per
+token (mode 7) or take the int8 chunks as they are (mode 3), int8 matmul with
+exact int32 accumulation, dequant by x1 scale x x2 scale, add bias, bf16 out.
+Every output is compared bit for bit: q, x1_scale, the int32 accumulators and
+out (the same fp32 operations in the same order on both sides).
+"""
+import pytest
+import torch
+
+import mc2_inputs
+import oracle
+import quantized_gemm_rank_gb300 as mc2
+from parity import assert_bits_equal
+
+pytestmark = pytest.mark.gpu
+
+
+def run_gpu(inp, shape, want_debug=True, bias_bf16=False):
+    dev = torch.device("cuda")
+    chunks = [c.to(dev) for c in inp["chunks"]]
+    x1s = None if inp["x1_scale"] is None else inp["x1_scale"].to(dev)
+    bias = inp["bias"].to(torch.bfloat16 if bias_bf16 else torch.float32).to(dev)
+    K = shape.rank_size * shape.h
+    q = torch.empty((shape.bs_local, K), dtype=torch.int8, device=dev) if want_debug else None
+    s = torch.empty((shape.bs_local,), dtype=torch.float32, device=dev) if want_debug else None
+    acc = torch.empty((shape.bs_local, shape.n), dtype=torch.int32, device=dev) if want_debug else None
+    res = mc2.mc2_alltoall_quant_mm(chunks, inp["x2"].to(dev), inp["x2_scale"].to(dev), bias,
+                                    x1_quant_mode=shape.quant_mode, x1_scale=x1s, q_out=q, x1_scale_out=s,
+                                    acc_out=acc)
+    torch.cuda.synchronize()
+    assert mc2.mc2_device_status() == mc2.MC2_OK
+    return {k: (None if v is None else v.cpu()) for k, v in res.items()}
+
+
+def run_oracle(inp, shape, rows=None, bias_bf16=False):
+    bias = inp["bias"]
+    if bias_bf16:
+        bias = bias.to(torch.bfloat16).float()
+    return oracle.alltoall_quant_mm(inp["chunks"], inp["x2"], inp["x2_scale"], bias,
+                                    quant_mode=shape.quant_mode, x1_scale=inp["x1_scale"], rows=rows)
+
+
+def compare(got, ref, name, rows=None):
+    sel = (lambda t: t) if rows is None else (lambda t: t[rows])
+    assert_bits_equal(sel(got["acc"]), ref["acc"], f"{name}: acc")
+    assert_bits_equal(sel(got["q"]), ref["q"], f"{name}: q")
+    assert_bits_equal(sel(got["x1_scale"]), ref["x1_scale"], f"{name}: x1_scale")
+    assert_bits_equal(sel(got["out"]), ref["out"], f"{name}: out")
+
+
+A2A = mc2_inputs.A2AShape
+CASES = {
+    "dyn-bf16-ragged": A2A(rank_size=4, bs_local=200, h=96, n=272, quant_mode=7),
+    "dyn-fp16-scalar-h": A2A(rank_size=8, bs_local=72, h=6, n=48, quant_mode=7, x1_dtype=torch.float16),
+    "dyn-bf16-nosmooth": A2A(rank_size=2, bs_local=130, h=256, n=528, quant_mode=7, smooth=False),
+    "dyn-bf16-2kblocks": A2A(rank_size=8, bs_local=136, h=320, n=256, quant_mode=7),
+    "full-int8-ragged": A2A(rank_size=8, bs_local=136, h=48, n=320, quant_mode=3),
+    "full-int8-scalar-h": A2A(rank_size=2, bs_local=40, h=24, n=32, quant_mode=3),
+    "full-int8-3kblocks": A2A(rank_size=4, bs_local=256, h=640, n=512, quant_mode=3),
+}
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_alltoall_quant_mm_parity(name):
+    shape = CASES[name]
+    inp = mc2_inputs.a2a_inputs(shape, seed=13)
+    got = run_gpu(inp, shape)
+    ref = run_oracle(inp, shape)
+    compare(got, ref, name)
+
+
+def test_bias_bf16_accepted():
+    shape = CASES["dyn-bf16-ragged"]
+    inp = mc2_inputs.a2a_inputs(shape, seed=4)
+    got = run_gpu(inp, shape, bias_bf16=True)
+    ref = run_oracle(inp, shape, bias_bf16=True)
+    compare(got, ref, "bias-bf16")
+
+
+def test_zero_and_outlier_rows():
+    shape = A2A(rank_size=4, bs_local=64, h=128, n=256, quant_mode=7)
+    inp = mc2_inputs.a2a_inputs(shape, seed=8)
+    for c in inp["chunks"]:
+        c[3].zero_()            # zero row: scale 0, q 0, out = bias
+        c[9, 5] = 3.0e4         # a single huge outlier in row 9 of every chunk
+    got = run_gpu(inp, shape)
+    ref = run_oracle(inp, shape)
+    compare(got, ref, "zero/outlier rows")
+    assert torch.all(got["q"][3] == 0) and got["x1_scale"][3].item() == 0.0
+
+
+@pytest.mark.parametrize("sign", [1, -1])
+def test_accumulator_bound_all_127(sign):
+    """All-127 operands: every 1024-long block reaches 1024*127*127 = 16516096
+    (just under 2^24) and the total 4096*16129 = 66064384 is far above it, so
+    the int32 result is exact only if each block is flushed exactly."""
+    shape = A2A(rank_size=8, bs_local=128, h=512, n=256, quant_mode=3)
+    inp = mc2_inputs.a2a_inputs(shape, seed=1)
+    inp["chunks"] = [torch.full_like(c, 127 * sign) for c in inp["chunks"]]
+    inp["x2"] = torch.full_like(inp["x2"], 127)
+    got = run_gpu(inp, shape)
+    ref = run_oracle(inp, shape)
+    assert torch.all(ref["acc"] == sign * 4096 * 16129)
+    compare(got, ref, "all-127")
+
+
+def test_full_size_dynamic_sampled_rows():
+    shape = mc2_inputs.WORKLOADS["a2a-dyn"]
+    inp = mc2_inputs.a2a_inputs(shape, seed=0)
+    got = run_gpu(inp, shape)
+    rows = mc2_inputs.sample_rows(shape.bs_local, 96, seed=1)
+    ref = run_oracle(inp, shape, rows=rows)
+    compare(got, ref, "a2a-dyn", rows=rows)
+    # the quantised activations and scales of every row (cheap on the CPU)
+    P = oracle.permute(inp["chunks"])
+    q, s = oracle.quant_pertoken_dynamic(P, inp["x1_scale"])
+    assert_bits_equal(got["q"], q, "a2a-dyn: all q")
+    assert_bits_equal(got["x1_scale"], s, "a2a-dyn: all scales")
+
+
+def test_full_size_full_quant_subset():
+    """The full-quant workload; the oracle checks a seeded 1024-row subset."""
+    shape = mc2_inputs.WORKLOADS["a2a-full"]
+    inp = mc2_inputs.a2a_inputs(shape, seed=0)
+    got = run_gpu(inp, shape)
+    rows = mc2_inputs.sample_rows(shape.bs_local, 1024, seed=1)
+    ref = run_oracle(inp, shape, rows=rows)
+    compare(got, ref, "a2a-full", rows=rows)
+
+
+def test_without_debug_outputs_matches():
+    shape = CASES["dyn-bf16-2kblocks"]
+    inp = mc2_inputs.a2a_inputs(shape, seed=2)
+    a = run_gpu(inp, shape, want_debug=True)
+    b = run_gpu(inp, shape, want_debug=False)
+    assert_bits_equal(a["out"], b["out"], "out with/without debug outputs")

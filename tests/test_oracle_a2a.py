@@ -198,3 +198,26 @@ def test_full_quant_mode_uses_input_scale():
     assert torch.equal(res["x1_scale"], inp["x1_scale"])
     ref = P.numpy().astype(np.int64) @ inp["x2"].numpy().astype(np.int64)
     assert np.array_equal(res["acc"].numpy().astype(np.int64), ref)
+
+
+def test_fp64_int8_mm_route_equals_integer_loop():
+    g = torch.Generator().manual_seed(31)
+    a = torch.randint(-127, 128, (20, 3000), generator=g, dtype=torch.int8)
+    b = torch.randint(-127, 128, (3000, 70), generator=g, dtype=torch.int8)
+    assert torch.equal(oracle.int8_mm_fp64(a, b, col_block=32), oracle.int8_mm(a, b))
+    full = torch.full((3, 35000), 127, dtype=torch.int8)
+    assert torch.all(oracle.int8_mm_fp64(full, torch.full((35000, 2), -127, dtype=torch.int8)) == -35000 * 16129)
+
+
+def test_large_composite_uses_same_steps():
+    # big enough to take the fp64 route; compare with the step-by-step C path
+    s = mc2_inputs.scaled(mc2_inputs.WORKLOADS["a2a-full"], bs_local=40, h=2048, n=4096)
+    inp = mc2_inputs.a2a_inputs(s, seed=3)
+    assert 40 * 8 * 2048 * 4096 > (1 << 31)
+    big = oracle.alltoall_quant_mm(inp["chunks"], inp["x2"], inp["x2_scale"], inp["bias"], quant_mode=3,
+                                   x1_scale=inp["x1_scale"])
+    P = oracle.permute(inp["chunks"])
+    acc = oracle.int8_mm(P, inp["x2"])
+    assert torch.equal(big["acc"], acc)
+    assert torch.equal(big["out"].view(torch.int16),
+                       oracle.dequant(acc, inp["x1_scale"], inp["x2_scale"], inp["bias"]).view(torch.int16))
