@@ -1,0 +1,461 @@
+#!/usr/bin/env python
+"""Benchmark of the MC2 fused-linear hot path on GB300.
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+  * mc2_all_gather_mm on "ag-8x1024": 8 rank chunks (1024, 4096) bf16, x2 (4096,
+    4096), gathered output on -> chunk addressing, gathered store, bf16 GEMM;
+  * mc2_alltoall_quant_mm on "a2a-dyn": 8 received chunks (4096, 1024) bf16 with
+    the smooth scale, per-token dynamic quant (mode 7), int8 GEMM with exact
+    int32 accumulation, per-token x per-channel dequant + bias, bf16 out.
+value = (2*m*n*k of both GEMMs) / device time per step, in TFLOP/s (bf16 FLOPs
+plus int8 OPs).  L2 (129 MB) is flushed between timed steps by writing a
+512 MiB buffer outside the timed events.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+With --gpus N > 1 (under torch.distributed.run) every rank runs its own replica
+of the step (the ops do not shard on one GPU; there is no data-path
+collective) and value is the sum over ranks divided by the slowest rank's time.
+--impl reference times the CPU oracle (the reference arm) on a bounded sample.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import mc2_inputs  # noqa: E402
+
+METRIC = "fused MC2 GEMM TFLOP/s (bf16) & TOP/s (int8) on 1 GB300, % of tensor peak"
+UNIT = "TFLOP/s"
+AG_NAME = "ag-8x1024"
+A2A_NAME = "a2a-dyn"
+WORKLOAD = f"{AG_NAME}+{A2A_NAME}"
+FLUSH_BYTES = 512 << 20
+
+# DRAM bytes (read + write) per launch of the bf16 all-gather GEMM on the
+# ag-8x1024 workload, from the ncu capture summarised in
+# profiles/gemm_bf16_ag-8x1024.md, and the hash of the kernel sources the
+# capture was taken with (the figure is reported only while they match).
+AG_GEMM_TRAFFIC = None
+AG_GEMM_TRAFFIC_SRC_HASH = None
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--no-extra", action="store_true", help="skip the per-workload table")
+    ap.add_argument("--profile", action="store_true",
+                    help="only the timed steps (no e2e, per-workload table or CPU baseline): for ncu")
+    return ap.parse_args()
+
+
+def kernel_src_hash() -> str:
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "quantized_gemm_rank_gb300", "csrc")
+    for name in sorted(os.listdir(d)):
+        with open(os.path.join(d, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"bf16": float(p["bf16_tflops"]), "bf16_sustained": float(p["bf16_tflops_sustained"]),
+                "hbm": float(p["hbm_gbs"]), "source": "measured"}
+    except Exception:
+        return {"bf16": 1900.0, "bf16_sustained": 1700.0, "hbm": 6800.0, "source": "fallback"}
+
+
+# ----------------------------------------------------------------------------- distributed
+def dist_setup(n_gpus):
+    if n_gpus <= 1 or "RANK" not in os.environ:
+        return 0, 1, 0
+    import torch.distributed as dist
+    rank = int(os.environ["RANK"])
+    world = int(os.environ["WORLD_SIZE"])
+    local = int(os.environ.get("LOCAL_RANK", rank))
+    torch.cuda.set_device(local)
+    dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.file = tempfile.NamedTemporaryFile(mode="w+", suffix=".csv", delete=False)
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.file, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [r.strip().split(",") for r in self.file.read().splitlines() if r.strip()]
+        os.unlink(self.file.name)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+                for nm, v in zip(names, r[5:9]):
+                    if v.strip().lower() == "active":
+                        reasons.add(nm)
+            except (ValueError, IndexError):
+                continue
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- workloads
+class Step:
+    """Device-resident inputs and outputs for one step of the hot path."""
+
+    def __init__(self, dev, ag_shape, a2a_shape, seed=0):
+        import quantized_gemm_rank_gb300 as mc2
+        self.mc2 = mc2
+        self.ag_s, self.a2a_s = ag_shape, a2a_shape
+        ag = mc2_inputs.ag_inputs(ag_shape, seed=seed)
+        a2 = mc2_inputs.a2a_inputs(a2a_shape, seed=seed)
+        self.host = {"ag": ag, "a2a": a2}
+        self.ag_chunks = [c.to(dev) for c in ag["chunks"]]
+        self.ag_x2 = ag["x2"].to(dev)
+        self.ag_bias = None if ag["bias"] is None else ag["bias"].to(dev)
+        m, n, k = ag_shape.m, ag_shape.n, ag_shape.k
+        self.ag_out = torch.empty((m, n), dtype=ag_shape.dtype, device=dev)
+        self.ag_gathered = torch.empty((m, k), dtype=ag_shape.dtype, device=dev) if ag_shape.gather_output else None
+        self.a_chunks = [c.to(dev) for c in a2["chunks"]]
+        self.a_x1s = None if a2["x1_scale"] is None else a2["x1_scale"].to(dev)
+        self.a_x2 = a2["x2"].to(dev)
+        self.a_x2s = a2["x2_scale"].to(dev)
+        self.a_bias = a2["bias"].to(dev)
+        self.a_out = torch.empty((a2a_shape.bs_local, a2a_shape.n), dtype=torch.bfloat16, device=dev)
+        ws = mc2.mc2_alltoall_quant_mm_workspace(a2a_shape.rank_size, a2a_shape.bs_local, a2a_shape.h, a2a_shape.n,
+                                                 a2a_shape.quant_mode, self.a_chunks[0].dtype)
+        self.ws = torch.empty(ws, dtype=torch.uint8, device=dev)
+
+    def run_ag(self):
+        self.mc2.mc2_all_gather_mm(self.ag_chunks, self.ag_x2, x2_is_nk=self.ag_s.x2_is_nk, bias=self.ag_bias,
+                                   gather_output=self.ag_s.gather_output, out=self.ag_out,
+                                   gathered=self.ag_gathered)
+
+    def run_a2a(self):
+        self.mc2.mc2_alltoall_quant_mm(self.a_chunks, self.a_x2, self.a_x2s, self.a_bias,
+                                       x1_quant_mode=self.a2a_s.quant_mode, x1_scale=self.a_x1s, out=self.a_out,
+                                       workspace=self.ws)
+
+    def run(self):
+        self.run_ag()
+        self.run_a2a()
+
+    launches_per_step = 4  # ag: GEMM; a2a (mode 7): quant prologue, x2 widening, GEMM
+
+    @property
+    def flops(self):
+        return self.ag_s.flops + self.a2a_s.ops
+
+
+def time_device(fn, steps, warmup, flush, stream):
+    """Per-step device times (ms) by CUDA events on `stream`, flushing L2 outside them."""
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(steps):
+        flush.zero_()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        b.synchronize()
+        times.append(a.elapsed_time(b))
+    return times
+
+
+def time_e2e(step: Step, steps, warmup, dev):
+    """Same step through the public calls with HOST inputs: pinned host -> device
+    copies of every input, both calls, device -> host copies of every output."""
+    ag, a2 = step.host["ag"], step.host["a2a"]
+    h_in = [c.pin_memory() for c in ag["chunks"]] + [ag["x2"].pin_memory()] + \
+           [c.pin_memory() for c in a2["chunks"]] + [a2["x2"].pin_memory(), a2["x2_scale"].pin_memory(),
+                                                     a2["bias"].pin_memory()]
+    if a2["x1_scale"] is not None:
+        h_in.append(a2["x1_scale"].pin_memory())
+    d_in = step.ag_chunks + [step.ag_x2] + step.a_chunks + [step.a_x2, step.a_x2s, step.a_bias]
+    if step.a_x1s is not None:
+        d_in.append(step.a_x1s)
+    d_out = [step.ag_out] + ([step.ag_gathered] if step.ag_gathered is not None else []) + [step.a_out]
+    h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in d_out]
+    h2d = sum(t.numel() * t.element_size() for t in h_in)
+    d2h = sum(t.numel() * t.element_size() for t in h_out)
+
+    def one():
+        for d, h in zip(d_in, h_in):
+            d.copy_(h, non_blocking=True)
+        step.run()
+        for h, d in zip(h_out, d_out):
+            h.copy_(d, non_blocking=True)
+
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        one()
+    b.record(stream)
+    b.synchronize()
+    return a.elapsed_time(b) / steps, h2d, d2h
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+def oracle_sample(rows_ag: int, rows_a2a: int, ag_s, a2a_s, host):
+    """Oracle on a bounded row sample of the step's workload; returns (seconds, flops)."""
+    import oracle
+    ra = mc2_inputs.sample_rows(ag_s.m, rows_ag, seed=11)
+    rb = mc2_inputs.sample_rows(a2a_s.bs_local, rows_a2a, seed=12)
+    t0 = time.perf_counter()
+    oracle.all_gather_mm(host["ag"]["chunks"], host["ag"]["x2"], x2_is_nk=ag_s.x2_is_nk, bias=host["ag"]["bias"],
+                         rows=ra, gather_output=False)
+    oracle.alltoall_quant_mm(host["a2a"]["chunks"], host["a2a"]["x2"], host["a2a"]["x2_scale"],
+                             host["a2a"]["bias"], quant_mode=a2a_s.quant_mode, x1_scale=host["a2a"]["x1_scale"],
+                             rows=rb)
+    dt = time.perf_counter() - t0
+    flops = 2.0 * len(ra) * ag_s.n * ag_s.k + 2.0 * len(rb) * a2a_s.n * a2a_s.k
+    return dt, flops
+
+
+def oracle_baseline(ag_s, a2a_s, host, target_s=10.0, max_reps=3):
+    """Time the oracle as it stands on whole steps of the workload (every output
+    row of both ops), repeated until ~target_s seconds of CPU work."""
+    import oracle
+    t_tot, fl_tot, reps = 0.0, 0.0, 0
+    while reps < max_reps and t_tot < target_s:
+        dt, fl = oracle_sample(ag_s.m, a2a_s.bs_local, ag_s, a2a_s, host)
+        t_tot += dt
+        fl_tot += fl
+        reps += 1
+    return {"value": fl_tot / t_tot / 1e12, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{reps} whole step(s) of {WORKLOAD} (all {ag_s.m} + {a2a_s.bs_local} output rows), "
+                      f"{t_tot:.1f} s"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    ag_s, a2a_s = mc2_inputs.WORKLOADS[AG_NAME], mc2_inputs.WORKLOADS[A2A_NAME]
+    host = {"ag": mc2_inputs.ag_inputs(ag_s, seed=0), "a2a": mc2_inputs.a2a_inputs(a2a_s, seed=0)}
+    import oracle
+    rows = 64
+    for _ in range(args.warmup):
+        oracle_sample(rows, rows, ag_s, a2a_s, host)
+    t0 = time.perf_counter()
+    tot_fl = 0.0
+    for _ in range(args.steps):
+        _, fl = oracle_sample(rows, rows, ag_s, a2a_s, host)
+        tot_fl += fl
+    dt = time.perf_counter() - t0
+    value = tot_fl / dt / 1e12
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64+int64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": WORKLOAD, "step": f"oracle on {rows} seeded rows of each op's output",
+                       "parallelism": "host cores"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+                             "sample": f"{rows} rows of each op per step"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------- main
+def extra_table(dev, flush, stream, steps):
+    """Per-workload device times of each call alone (all five workloads)."""
+    import quantized_gemm_rank_gb300 as mc2
+    res = {}
+    for name, s in mc2_inputs.WORKLOADS.items():
+        if name in (AG_NAME, A2A_NAME):
+            continue
+        if isinstance(s, mc2_inputs.AGShape):
+            inp = mc2_inputs.ag_inputs(s, seed=0)
+            ch = [c.to(dev) for c in inp["chunks"]]
+            x2 = inp["x2"].to(dev)
+            b = None if inp["bias"] is None else inp["bias"].to(dev)
+            out = torch.empty((s.m, s.n), dtype=s.dtype, device=dev)
+            g = torch.empty((s.m, s.k), dtype=s.dtype, device=dev)
+            fn = lambda: mc2.mc2_all_gather_mm(ch, x2, x2_is_nk=s.x2_is_nk, bias=b, out=out, gathered=g)  # noqa
+            fl = s.flops
+        else:
+            inp = mc2_inputs.a2a_inputs(s, seed=0)
+            ch = [c.to(dev) for c in inp["chunks"]]
+            x1s = None if inp["x1_scale"] is None else inp["x1_scale"].to(dev)
+            x2, x2s, b = inp["x2"].to(dev), inp["x2_scale"].to(dev), inp["bias"].to(dev)
+            out = torch.empty((s.bs_local, s.n), dtype=torch.bfloat16, device=dev)
+            ws = torch.empty(mc2.mc2_alltoall_quant_mm_workspace(s.rank_size, s.bs_local, s.h, s.n, s.quant_mode,
+                                                                 ch[0].dtype), dtype=torch.uint8, device=dev)
+            fn = lambda: mc2.mc2_alltoall_quant_mm(ch, x2, x2s, b, x1_quant_mode=s.quant_mode,  # noqa
+                                                   x1_scale=x1s, out=out, workspace=ws)
+            fl = s.ops
+        t = statistics.median(time_device(fn, steps, 3, flush, stream))
+        res[name] = {"us": round(t * 1e3, 2), "tflops": round(fl / (t * 1e-3) / 1e12, 1)}
+        del inp, ch
+        torch.cuda.empty_cache()
+    return res
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    if args.warmup < 3:
+        args.warmup = 3
+    rank, world, local = dist_setup(args.gpus)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    peaks = load_peaks()
+
+    ag_s, a2a_s = mc2_inputs.WORKLOADS[AG_NAME], mc2_inputs.WORKLOADS[A2A_NAME]
+    step = Step(dev, ag_s, a2a_s, seed=rank)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    # ---- timed region: K steps, barrier + synchronize on both sides
+    sampler = ClockSampler(local)
+    for _ in range(args.warmup):
+        step.run()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    sampler.start()
+    wall0 = time.perf_counter()
+    step_ms, ag_ms = [], []
+    for _ in range(args.steps):
+        flush.zero_()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e2 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        step.run_ag()
+        e1.record(stream)
+        step.run_a2a()
+        e2.record(stream)
+        e2.synchronize()
+        step_ms.append(e0.elapsed_time(e2))
+        ag_ms.append(e0.elapsed_time(e1))
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    clocks = sampler.stop()
+
+    ms = sum(step_ms) / len(step_ms)
+    ms = max_over_ranks(ms, world)
+    value = world * step.flops / (ms * 1e-3) / 1e12
+    ag_mean = sum(ag_ms) / len(ag_ms)
+    ag_tflops = ag_s.flops / (ag_mean * 1e-3) / 1e12
+
+    # ---- end to end through the public calls with host buffers
+    if args.profile:
+        e2e_ms, h2d, d2h = float("nan"), 0, 0
+    else:
+        e2e_ms, h2d, d2h = time_e2e(step, max(3, args.steps // 3), 2, dev)
+        e2e_ms = max_over_ranks(e2e_ms, world)
+    e2e_value = world * step.flops / (e2e_ms * 1e-3) / 1e12
+
+    mc2 = step.mc2
+    assert mc2.mc2_device_status() == mc2.MC2_OK, "a bounded device wait gave up"
+
+    extra = None if (args.no_extra or args.profile or rank != 0) else extra_table(dev, flush, stream, 10)
+    cpu = oracle_baseline(ag_s, a2a_s, step.host) if (rank == 0 and world == 1 and not args.profile) else None
+
+    traffic = AG_GEMM_TRAFFIC if (AG_GEMM_TRAFFIC is not None and AG_GEMM_TRAFFIC_SRC_HASH == kernel_src_hash()) \
+        else None
+    roof = {"kernel": "mc2_gemm_kernel<bf16> (all-gather GEMM, ag-8x1024)", "bound": "tensor",
+            "achieved": round(ag_tflops, 1), "peak": peaks["bf16"], "unit": "TFLOP/s",
+            "frac": round(ag_tflops / peaks["bf16"], 4), "traffic": traffic,
+            "peak_kind": f"bf16 dense burst, {peaks['source']}",
+            "algorithmic_flops_per_launch": ag_s.flops}
+    line = {"metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16+int8", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "all_gather_mm": "8 x (1024, 4096) bf16 @ (4096, 4096), gathered",
+                       "alltoall_quant_mm": "8 x (4096, 1024) bf16 -> (4096, 8192) @ int8 (8192, 4096), mode 7",
+                       "l2": "flushed between timed steps (512 MiB write outside the events)",
+                       "parallelism": f"replicas x{world}", "wall_s": round(wall, 3)},
+            "per_op": {AG_NAME: {"ms": round(ag_mean, 4), "tflops": round(ag_tflops, 1)},
+                       A2A_NAME: {"ms": round(ms - ag_mean, 4),
+                                  "tops": round(a2a_s.ops / ((ms - ag_mean) * 1e-3) / 1e12, 1)}},
+            "roofline": roof,
+            "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": Step.launches_per_step * args.steps,
+            "clocks": clocks}
+    if extra is not None:
+        line["per_workload"] = extra
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -8,32 +8,72 @@ __device__ int g_gemm_status = 0;
 
 namespace {
 
-template <bool kBF16, bool kIntPath>
+template <int kG, bool kBF16, bool kIntPath>
 cudaError_t launch_one(const GemmParams &p_in, int num_sms, cudaStream_t stream) {
-    auto kern = mc2_gemm_kernel<kBF16, kIntPath>;
+    using Cfg = TileCfg<kG>;
+    auto kern = mc2_gemm_kernel<kG, kBF16, kIntPath>;
     GemmParams p = p_in;
-    cudaError_t es = cudaGetSymbolAddress(reinterpret_cast<void **>(&p.status), g_gemm_status);
-    if (es != cudaSuccess) return es;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    cudaError_t e = cudaGetSymbolAddress(reinterpret_cast<void **>(&p.status), g_gemm_status);
     if (e != cudaSuccess) return e;
-    const int num_tiles = ((p.m + kBM - 1) / kBM) * ((p.n + kBN - 1) / kBN);
-    const int grid = num_tiles < num_sms ? num_tiles : num_sms;
-    kern<<<grid, kNumThreads, kSmemBytes, stream>>>(p);
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    const int num_tiles = ((p.m + Cfg::kTileM - 1) / Cfg::kTileM) * ((p.n + kBN - 1) / kBN);
+
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.blockDim = dim3(kNumThreads, 1, 1);
+    cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+    cfg.stream = stream;
+    if constexpr (kG == 2) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
+        if (e != cudaSuccess) return e;
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        // co-resident pairs on this device (cached per device)
+        static int cached[64] = {0};
+        int dev = 0;
+        cudaGetDevice(&dev);
+        int clusters = dev < 64 ? cached[dev] : 0;
+        if (clusters == 0) {
+            cfg.gridDim = dim3(2 * (num_sms / 2), 1, 1);
+            e = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
+            if (e != cudaSuccess || clusters < 1) clusters = num_sms / 2;
+            if (dev < 64) cached[dev] = clusters;
+        }
+        const int grid_clusters = num_tiles < clusters ? num_tiles : clusters;
+        cfg.gridDim = dim3(2 * grid_clusters, 1, 1);
+    } else {
+        cfg.gridDim = dim3(num_tiles < num_sms ? num_tiles : num_sms, 1, 1);
+    }
+    e = cudaLaunchKernelEx(&cfg, kern, p);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_gemm(GemmKind kind, const GemmParams &p, int num_sms, cudaStream_t stream) {
-    switch (kind) {
-        case GEMM_F16: return launch_one<false, false>(p, num_sms, stream);
-        case GEMM_BF16: return launch_one<true, false>(p, num_sms, stream);
-        case GEMM_INT_AS_F16: return launch_one<false, true>(p, num_sms, stream);
+int gemm_group_for(int m) { return m > kBM ? 2 : 1; }
+
+cudaError_t launch_gemm(GemmKind kind, int group, const GemmParams &p, int num_sms, cudaStream_t stream) {
+    if (group == 2) {
+        switch (kind) {
+            case GEMM_F16: return launch_one<2, false, false>(p, num_sms, stream);
+            case GEMM_BF16: return launch_one<2, true, false>(p, num_sms, stream);
+            case GEMM_INT_AS_F16: return launch_one<2, false, true>(p, num_sms, stream);
+        }
+    } else {
+        switch (kind) {
+            case GEMM_F16: return launch_one<1, false, false>(p, num_sms, stream);
+            case GEMM_BF16: return launch_one<1, true, false>(p, num_sms, stream);
+            case GEMM_INT_AS_F16: return launch_one<1, false, true>(p, num_sms, stream);
+        }
     }
     return cudaErrorInvalidValue;
 }
-
-int gemm_smem_bytes() { return static_cast<int>(kSmemBytes); }
 
 int read_and_clear_gemm_status(int *status) {
     int zero = 0;

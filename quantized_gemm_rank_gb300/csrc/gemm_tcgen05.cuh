@@ -12,16 +12,28 @@
 //     blocks of at most 1024 (1024 * 127 * 127 < 2^24) and each block's fp32
 //     sum is flushed into an int32 register total; the epilogue then applies
 //     the per-token x per-channel dequant and the bias in fp32 and rounds to bf16.
+//   The float path uses the same K blocks: each block starts from zero in
+//   TMEM and the block sums are added in fp32 registers with round-to-nearest,
+//   which keeps the tensor core's own accumulation error (it adds at the
+//   magnitude of the running sum) to the size of one block's partial sums.
 //
-// Tile 128 x 256 x 64 (M x N x K), 16-bit operands in 128-byte-swizzled
-// shared memory, 4-stage TMA ring, tcgen05.mma kind::f16 (M=128, N=256) into
-// two 256-column TMEM accumulators so the epilogue of one tile (or K block)
-// overlaps the MMAs of the next.
+// Two shapes of the same kernel (template parameter kG):
+//   kG = 1  one CTA per tile: tile 128 x 256 x 64, tcgen05.mma.cta_group::1
+//           M=128 N=256, 4-stage ring of 48 KiB stages.
+//   kG = 2  a CTA pair (cluster of 2) per tile: tile 256 x 256 x 64,
+//           tcgen05.mma.cta_group::2 M=256 N=256 issued by the leader CTA;
+//           each CTA loads its own 128 rows of A and 128 rows of B (half the
+//           B traffic per CTA of kG = 1), 6-stage ring of 32 KiB stages.
+// 16-bit operands live in 128-byte-swizzled shared memory; accumulators are
+// two 256-column fp32 TMEM buffers per CTA so the epilogue of one K block (or
+// tile) overlaps the MMAs of the next.
 //
-// Warp roles (384 threads):
+// Warp roles (384 threads per CTA):
 //   warp 0      TMA producer (one lane)
-//   warp 1      TMEM allocator and MMA issuer (one lane)
-//   warp 2      gathered-output TMA store (one lane; AllGather with gather only)
+//   warp 1      TMEM allocator; MMA issuer (one lane; the leader CTA for kG = 2)
+//   warp 2      gathered-output TMA store (one lane; AllGather with gather only).
+//               For kG = 2 the peer CTA's A tile completes a barrier of its
+//               own and this warp relays the arrival to the leader's barrier.
 //   warp 3      idle
 //   warps 4-11  epilogue: warp w reads TMEM lanes 32*(w%4)..+31 (its rows) and
 //               half (w-4)/4 of the 256 accumulator columns.
@@ -30,23 +42,31 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <type_traits>
+
 #include "sm103_ptx.cuh"
 
 namespace mc2 {
 
-constexpr int kBM = 128;
-constexpr int kBN = 256;
+constexpr int kBM = 128;  // rows of A per CTA
+constexpr int kBN = 256;  // columns of the accumulator (MMA N)
 constexpr int kBK = 64;
-constexpr int kStages = 4;
 constexpr int kMaxAMaps = 8;
 constexpr int kNumEpiWarps = 8;
 constexpr int kNumThreads = 128 + kNumEpiWarps * 32;
 constexpr uint32_t kATileBytes = kBM * kBK * 2;  // 16 KiB
-constexpr uint32_t kBTileBytes = kBN * kBK * 2;  // 32 KiB
-constexpr uint32_t kStageBytes = kATileBytes + kBTileBytes;
 constexpr uint32_t kTmemCols = 512;              // two 256-column fp32 accumulators
-constexpr uint32_t kSmemBytes = kStages * kStageBytes + 1024 + 1024;
 constexpr int kGroupM = 8;                       // m-tiles per raster group (L2 reuse of B)
+
+template <int kG>
+struct TileCfg {
+    static constexpr int kTileM = kBM * kG;               // rows per tile
+    static constexpr int kBRows = kBN / kG;               // rows of B (N) per CTA
+    static constexpr uint32_t kBTileBytes = kBRows * kBK * 2;
+    static constexpr uint32_t kStageBytes = kATileBytes + kBTileBytes;
+    static constexpr int kStages = kG == 1 ? 4 : 6;
+    static constexpr uint32_t kSmemBytes = kStages * kStageBytes + 1024 + 1024;
+};
 
 enum AMode : int { A_SINGLE = 0, A_MCONCAT = 1, A_KINTERLEAVE = 2 };
 
@@ -84,10 +104,13 @@ __device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int 
     nb = r / gsz;
 }
 
+template <bool kCluster>
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, const GemmParams &p,
                                               volatile int *abort_flag) {
     if (*abort_flag) return false;
-    if (ptx::mbar_wait(bar, parity, p.wait_limit_ns)) return true;
+    const bool ok = kCluster ? ptx::mbar_wait_cluster(bar, parity, p.wait_limit_ns)
+                             : ptx::mbar_wait(bar, parity, p.wait_limit_ns);
+    if (ok) return true;
     *abort_flag = 1;
     if (p.status) atomicExch(p.status, -7);
     return false;
@@ -128,44 +151,53 @@ __device__ __forceinline__ void store_row32_16(void *out, int n, int row, int co
     }
 }
 
-template <bool kBF16, bool kIntPath>
+template <int kG, bool kBF16, bool kIntPath>
 __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_constant__ GemmParams p) {
+    using Cfg = TileCfg<kG>;
+    constexpr bool kPair = kG == 2;
+    constexpr int S = Cfg::kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kStages * kStageBytes);
-    uint64_t *full_bar = bars;
-    uint64_t *empty_bar = bars + kStages;
-    uint64_t *tfull_bar = bars + 2 * kStages;
-    uint64_t *tempty_bar = bars + 2 * kStages + 2;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * kStages + 4);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S * Cfg::kStageBytes);
+    uint64_t *full_bar = bars;            // A/B landed (leader: whole pair; peer: its own A when relaying)
+    uint64_t *empty_bar = bars + S;       // stage free in this CTA
+    uint64_t *tfull_bar = bars + 2 * S;   // accumulator buffer ready
+    uint64_t *tempty_bar = bars + 2 * S + 2;  // accumulator buffer drained (leader's counts both CTAs)
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * S + 4);
     __shared__ int abort_flag_s;
     volatile int *abort_flag = &abort_flag_s;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int num_m = (p.m + kBM - 1) / kBM;
+    const uint32_t cr = kPair ? ptx::cluster_ctarank() : 0u;  // rank inside the pair
+    const bool leader = cr == 0;
+    const bool relay = kPair && p.gather;  // peer A lands on the peer's own barrier, relayed by warp 2
+    const int num_m = (p.m + Cfg::kTileM - 1) / Cfg::kTileM;
     const int num_n = (p.n + kBN - 1) / kBN;
     const int num_tiles = num_m * num_n;
     const int num_k = (p.k + kBK - 1) / kBK;
+    const int cluster_id = blockIdx.x / kG;
+    const int num_clusters = gridDim.x / kG;
 
     if (threadIdx.x == 0) {
         abort_flag_s = 0;
-        for (int s = 0; s < kStages; ++s) {
-            ptx::mbar_init(ptx::smem_u32(&full_bar[s]), 1);
+        for (int s = 0; s < S; ++s) {
+            ptx::mbar_init(ptx::smem_u32(&full_bar[s]), (kPair && leader && relay) ? 2 : 1);
             ptx::mbar_init(ptx::smem_u32(&empty_bar[s]), p.gather ? 2 : 1);
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(ptx::smem_u32(&tfull_bar[b]), 1);
-            ptx::mbar_init(ptx::smem_u32(&tempty_bar[b]), kNumEpiWarps);
+            ptx::mbar_init(ptx::smem_u32(&tempty_bar[b]), kNumEpiWarps * kG);
         }
         ptx::fence_mbar_init();
     }
     if (warp == 1) {
-        ptx::tmem_alloc(ptx::smem_u32(tmem_slot), kTmemCols);
-        ptx::tmem_relinquish();
+        ptx::tmem_alloc<kG>(ptx::smem_u32(tmem_slot), kTmemCols);
+        ptx::tmem_relinquish<kG>();
     }
     ptx::tc_fence_before();
     __syncthreads();
+    if constexpr (kPair) ptx::cluster_sync();
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
@@ -173,118 +205,142 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
         // ------------------------------------------------------------ TMA producer
         for (int i = 0; i < p.num_a_maps; ++i) ptx::prefetch_tmap(&p.a_maps[i]);
         ptx::prefetch_tmap(&p.b_map);
+        // bytes that complete the leader's full barrier per stage
+        uint32_t leader_bytes = Cfg::kStageBytes;
+        if (kPair) leader_bytes += Cfg::kBTileBytes + (relay ? 0u : kATileBytes);
         int stage = 0;
         uint32_t phase = 0;
-        uint32_t armed_phase[kStages];
-        bool armed[kStages];
-#pragma unroll
-        for (int s = 0; s < kStages; ++s) armed[s] = false, armed_phase[s] = 0;
+        int iters = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        for (int tile = cluster_id; tile < num_tiles && ok; tile += num_clusters) {
             int mb, nb;
             tile_coords(tile, num_m, num_n, mb, nb);
-            const int m0 = mb * kBM, n0 = nb * kBN;
+            const int m0 = mb * Cfg::kTileM + kBM * static_cast<int>(cr);
+            const int n0 = nb * kBN + Cfg::kBRows * static_cast<int>(cr);
             for (int kt = 0; kt < num_k; ++kt) {
-                if (!wait_or_abort(ptx::smem_u32(&empty_bar[stage]), phase ^ 1u, p, abort_flag)) {
+                if (!wait_or_abort<kPair>(ptx::smem_u32(&empty_bar[stage]), phase ^ 1u, p, abort_flag)) {
                     ok = false;
                     break;
                 }
-                const uint32_t fb = ptx::smem_u32(&full_bar[stage]);
-                const uint32_t sA = ptx::smem_u32(smem + stage * kStageBytes);
+                const uint32_t local_full = ptx::smem_u32(&full_bar[stage]);
+                const uint32_t sA = ptx::smem_u32(smem + stage * Cfg::kStageBytes);
                 const uint32_t sB = sA + kATileBytes;
-                ptx::mbar_arrive_expect_tx(fb, kStageBytes);
-                armed[stage] = true;
-                armed_phase[stage] = phase;
+                uint32_t a_bar = local_full, b_bar = local_full;
+                if (leader) {
+                    ptx::mbar_arrive_expect_tx(local_full, leader_bytes);
+                } else {
+                    const uint32_t leader_full = ptx::mapa(local_full, 0);
+                    b_bar = leader_full;
+                    if (relay)
+                        ptx::mbar_arrive_expect_tx(local_full, kATileBytes);
+                    else
+                        a_bar = leader_full;
+                }
                 const int k0 = kt * kBK;
+                auto load = [&](uint32_t dst, const CUtensorMap *m, int c0, int c1, uint32_t bar) {
+                    if constexpr (kPair)
+                        ptx::tma_load_2d_pair(dst, m, c0, c1, bar);
+                    else
+                        ptx::tma_load_2d(dst, m, c0, c1, bar);
+                };
                 if (p.a_mode == A_MCONCAT) {
                     const int nbox = kBM / p.a_box_rows;
                     for (int j = 0; j < nbox; ++j) {
                         const int i0 = m0 + j * p.a_box_rows;
                         const int c = min(i0 / p.m_local, p.num_a_maps - 1);
                         const int li = i0 - c * p.m_local;
-                        ptx::tma_load_2d(sA + j * p.a_box_rows * 128, &p.a_maps[c], k0, li, fb);
+                        load(sA + j * p.a_box_rows * 128, &p.a_maps[c], k0, li, a_bar);
                     }
                 } else if (p.a_mode == A_KINTERLEAVE) {
                     const int c = k0 / p.k_local;
-                    ptx::tma_load_2d(sA, &p.a_maps[c], k0 - c * p.k_local, m0, fb);
+                    load(sA, &p.a_maps[c], k0 - c * p.k_local, m0, a_bar);
                 } else {
-                    ptx::tma_load_2d(sA, &p.a_maps[0], k0, m0, fb);
+                    load(sA, &p.a_maps[0], k0, m0, a_bar);
                 }
                 if (p.b_mn_major) {
 #pragma unroll
-                    for (int j = 0; j < kBN / 64; ++j) ptx::tma_load_2d(sB + j * (kBK * 128), &p.b_map, n0 + 64 * j, k0, fb);
+                    for (int j = 0; j < Cfg::kBRows / 64; ++j)
+                        load(sB + j * (kBK * 128), &p.b_map, n0 + 64 * j, k0, b_bar);
                 } else {
-                    ptx::tma_load_2d(sB, &p.b_map, k0, n0, fb);
+                    load(sB, &p.b_map, k0, n0, b_bar);
                 }
-                if (++stage == kStages) stage = 0, phase ^= 1u;
+                ++iters;
+                if (++stage == S) stage = 0, phase ^= 1u;
             }
         }
         if (!ok) {
-            // let copies already in flight land before the CTA can exit
-            for (int s = 0; s < kStages; ++s)
-                if (armed[s]) (void)ptx::mbar_wait(ptx::smem_u32(&full_bar[s]), armed_phase[s], p.wait_limit_ns);
+            // let the copies already in flight land before the CTA can exit
+            const bool armed_local = !kPair || leader || relay;
+            for (int back = 1; back <= S && back <= iters && armed_local; ++back) {
+                const int i = iters - back;
+                (void)ptx::mbar_wait(ptx::smem_u32(&full_bar[i % S]), static_cast<uint32_t>((i / S) & 1),
+                                     p.wait_limit_ns);
+            }
+            ptx::nanosleep(20000);
         }
-    } else if (warp == 1 && lane == 0) {
+    } else if (warp == 1 && lane == 0 && leader) {
         // ------------------------------------------------------------ MMA issuer
-        const uint32_t idesc = ptx::idesc_f16(kBF16 && !kIntPath, p.b_mn_major != 0, kBM, kBN);
+        const uint32_t idesc = ptx::idesc_f16(kBF16 && !kIntPath, p.b_mn_major != 0, Cfg::kTileM, kBN);
         int stage = 0;
         uint32_t phase = 0;
         uint32_t acc_iter = 0;
         bool ok = true;
         uint32_t d_tmem = tmem_base;
-        for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        for (int tile = cluster_id; tile < num_tiles && ok; tile += num_clusters) {
             for (int kt = 0; kt < num_k; ++kt) {
-                const int kin = kIntPath ? (kt % p.kblock_tiles) : kt;  // k-tile index inside the block
+                const int kin = kt % p.kblock_tiles;  // k-tile index inside the current K block
                 if (kin == 0) {
                     const uint32_t b = acc_iter & 1u;
-                    if (!wait_or_abort(ptx::smem_u32(&tempty_bar[b]), ((acc_iter >> 1) & 1u) ^ 1u, p, abort_flag)) {
+                    if (!wait_or_abort<kPair>(ptx::smem_u32(&tempty_bar[b]), ((acc_iter >> 1) & 1u) ^ 1u, p,
+                                              abort_flag)) {
                         ok = false;
                         break;
                     }
                     ptx::tc_fence_after();
                     d_tmem = tmem_base + b * kBN;
                 }
-                if (!wait_or_abort(ptx::smem_u32(&full_bar[stage]), phase, p, abort_flag)) {
+                if (!wait_or_abort<kPair>(ptx::smem_u32(&full_bar[stage]), phase, p, abort_flag)) {
                     ok = false;
                     break;
                 }
                 ptx::tc_fence_after();
-                const uint32_t sA = ptx::smem_u32(smem + stage * kStageBytes);
+                const uint32_t sA = ptx::smem_u32(smem + stage * Cfg::kStageBytes);
                 const uint32_t sB = sA + kATileBytes;
 #pragma unroll
                 for (int kk = 0; kk < kBK / 16; ++kk) {
                     const uint64_t ad = ptx::smem_desc_sw128(sA + kk * 32, 16, 1024);
                     const uint64_t bd = p.b_mn_major ? ptx::smem_desc_sw128(sB + kk * 2048, kBK * 128, 1024)
                                                      : ptx::smem_desc_sw128(sB + kk * 32, 16, 1024);
-                    ptx::mma_f16_ss(d_tmem, ad, bd, idesc, (kin > 0 || kk > 0) ? 1u : 0u);
+                    ptx::mma_f16_ss<kG>(d_tmem, ad, bd, idesc, (kin > 0 || kk > 0) ? 1u : 0u);
                 }
-                ptx::mma_commit(ptx::smem_u32(&empty_bar[stage]));
-                if (++stage == kStages) stage = 0, phase ^= 1u;
-                const bool block_end = kIntPath ? (kin == p.kblock_tiles - 1 || kt == num_k - 1) : (kt == num_k - 1);
-                if (block_end) {
-                    ptx::mma_commit(ptx::smem_u32(&tfull_bar[acc_iter & 1u]));
+                ptx::mma_commit<kG>(ptx::smem_u32(&empty_bar[stage]));
+                if (++stage == S) stage = 0, phase ^= 1u;
+                if (kin == p.kblock_tiles - 1 || kt == num_k - 1) {
+                    ptx::mma_commit<kG>(ptx::smem_u32(&tfull_bar[acc_iter & 1u]));
                     ++acc_iter;
                 }
             }
         }
     } else if (warp == 2 && lane == 0 && p.gather) {
-        // ------------------------------------------------------------ gathered store
+        // ------------------------------------------------------------ gathered store (+ relay)
         ptx::prefetch_tmap(&p.g_map);
         int stage = 0;
         uint32_t phase = 0;
-        int pending_stage = -1;  // stage whose store may still be reading smem
-        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+        int pending_stage = -1;  // stage whose store may still be reading shared memory
+        for (int tile = cluster_id; tile < num_tiles; tile += num_clusters) {
             int mb, nb;
             tile_coords(tile, num_m, num_n, mb, nb);
+            const int m0 = mb * Cfg::kTileM + kBM * static_cast<int>(cr);
             bool ok = true;
             for (int kt = 0; kt < num_k; ++kt) {
-                if (!wait_or_abort(ptx::smem_u32(&full_bar[stage]), phase, p, abort_flag)) {
+                if (!wait_or_abort<kPair>(ptx::smem_u32(&full_bar[stage]), phase, p, abort_flag)) {
                     ok = false;
                     break;
                 }
+                if (kPair && !leader) ptx::mbar_arrive_remote(ptx::mapa(ptx::smem_u32(&full_bar[stage]), 0));
                 if (nb == 0) {
-                    const uint32_t sA = ptx::smem_u32(smem + stage * kStageBytes);
-                    ptx::tma_store_2d(&p.g_map, kt * kBK, mb * kBM, sA);
+                    const uint32_t sA = ptx::smem_u32(smem + stage * Cfg::kStageBytes);
+                    ptx::tma_store_2d(&p.g_map, kt * kBK, m0, sA);
                     ptx::bulk_commit_group();
                     // release the previous stage once its store has finished reading
                     ptx::bulk_wait_group_read<1>();
@@ -298,7 +354,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
                     }
                     ptx::mbar_arrive(ptx::smem_u32(&empty_bar[stage]));
                 }
-                if (++stage == kStages) stage = 0, phase ^= 1u;
+                if (++stage == S) stage = 0, phase ^= 1u;
             }
             if (!ok) break;
         }
@@ -311,73 +367,78 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
         const int half = (warp - 4) >> 2;     // which 128 of the 256 columns
         const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
         uint32_t acc_iter = 0;
-        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+        for (int tile = cluster_id; tile < num_tiles; tile += num_clusters) {
             int mb, nb;
             tile_coords(tile, num_m, num_n, mb, nb);
-            const int row = mb * kBM + 32 * q + lane;
+            const int row = mb * Cfg::kTileM + kBM * static_cast<int>(cr) + 32 * q + lane;
             const int colh = nb * kBN + half * 128;
             bool ok = true;
-            if constexpr (!kIntPath) {
+            // Sum of the K blocks: exact int32 (integer path) or fp32 with
+            // round-to-nearest adds (float path); one TMEM drain per block.
+            using acc_t = typename std::conditional<kIntPath, int32_t, float>::type;
+            acc_t sum[128];
+#pragma unroll
+            for (int i = 0; i < 128; ++i) sum[i] = acc_t(0);
+            const int nkb = (num_k + p.kblock_tiles - 1) / p.kblock_tiles;
+            for (int kb = 0; kb < nkb; ++kb) {
                 const uint32_t b = acc_iter & 1u;
-                if (!wait_or_abort(ptx::smem_u32(&tfull_bar[b]), (acc_iter >> 1) & 1u, p, abort_flag)) break;
+                if (!wait_or_abort<kPair>(ptx::smem_u32(&tfull_bar[b]), (acc_iter >> 1) & 1u, p, abort_flag)) {
+                    ok = false;
+                    break;
+                }
                 ptx::tc_fence_after();
-#pragma unroll 1
+#pragma unroll
                 for (int c = 0; c < 4; ++c) {
-                    const int col0 = colh + c * 32;
-                    if (col0 >= p.n) break;
-                    uint32_t r[32];
-                    ptx::tmem_ld_32x32b_x32(tmem_base + lane_addr + b * kBN + half * 128 + c * 32, r);
-                    ptx::tmem_ld_wait();
-                    float v[32];
+                    if (colh + c * 32 < p.n) {
+                        uint32_t r[32];
+                        ptx::tmem_ld_32x32b_x32(tmem_base + lane_addr + b * kBN + half * 128 + c * 32, r);
+                        ptx::tmem_ld_wait();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-                    if (p.bias16 != nullptr) {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            if (col0 + i < p.n) v[i] = __fadd_rn(v[i], load16<kBF16>(p.bias16, col0 + i));
+                        for (int i = 0; i < 32; ++i) {
+                            if constexpr (kIntPath)
+                                sum[c * 32 + i] += __float2int_rn(__uint_as_float(r[i]));
+                            else
+                                sum[c * 32 + i] = __fadd_rn(sum[c * 32 + i], __uint_as_float(r[i]));
+                        }
                     }
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) pk[i] = pack2<kBF16>(v[2 * i], v[2 * i + 1]);
-                    if (row < p.m) store_row32_16(p.out, p.n, row, col0, pk);
                 }
                 ptx::tc_fence_before();
                 __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&tempty_bar[b]));
-                ++acc_iter;
-            } else {
-                int32_t sum[128];
-#pragma unroll
-                for (int i = 0; i < 128; ++i) sum[i] = 0;
-                const int nkb = (num_k + p.kblock_tiles - 1) / p.kblock_tiles;
-                for (int kb = 0; kb < nkb; ++kb) {
-                    const uint32_t b = acc_iter & 1u;
-                    if (!wait_or_abort(ptx::smem_u32(&tfull_bar[b]), (acc_iter >> 1) & 1u, p, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    ptx::tc_fence_after();
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        if (colh + c * 32 < p.n) {
-                            uint32_t r[32];
-                            ptx::tmem_ld_32x32b_x32(tmem_base + lane_addr + b * kBN + half * 128 + c * 32, r);
-                            ptx::tmem_ld_wait();
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) sum[c * 32 + i] += __float2int_rn(__uint_as_float(r[i]));
-                        }
-                    }
-                    ptx::tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&tempty_bar[b]));
-                    ++acc_iter;
+                if (lane == 0) {
+                    if constexpr (kPair)
+                        ptx::mbar_arrive_remote(ptx::mapa(ptx::smem_u32(&tempty_bar[b]), 0));
+                    else
+                        ptx::mbar_arrive(ptx::smem_u32(&tempty_bar[b]));
                 }
-                if (!ok) break;
-                const float s1 = row < p.m ? p.x1_scale[row] : 0.0f;
+                ++acc_iter;
+            }
+            if (!ok) break;
+            if (row >= p.m) continue;
+            if constexpr (!kIntPath) {
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     const int col0 = colh + c * 32;
-                    if (col0 < p.n && row < p.m) {
+                    if (col0 < p.n) {
+                        float v[32];
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = sum[c * 32 + i];
+                        if (p.bias16 != nullptr) {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i)
+                                v[i] = __fadd_rn(v[i], load16<kBF16>(p.bias16, min(col0 + i, p.n - 1)));
+                        }
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) pk[i] = pack2<kBF16>(v[2 * i], v[2 * i + 1]);
+                        store_row32_16(p.out, p.n, row, col0, pk);
+                    }
+                }
+            } else {
+                const float s1 = p.x1_scale[row];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int col0 = colh + c * 32;
+                    if (col0 < p.n) {
                         uint32_t pk[16];
 #pragma unroll
                         for (int i = 0; i < 32; i += 2) {
@@ -404,8 +465,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
 #pragma unroll
                                 for (int j = 0; j < 8; ++j)
                                     reinterpret_cast<int4 *>(dst)[j] =
-                                        make_int4(sum[c * 32 + 4 * j], sum[c * 32 + 4 * j + 1], sum[c * 32 + 4 * j + 2],
-                                                  sum[c * 32 + 4 * j + 3]);
+                                        make_int4(sum[c * 32 + 4 * j], sum[c * 32 + 4 * j + 1],
+                                                  sum[c * 32 + 4 * j + 2], sum[c * 32 + 4 * j + 3]);
                             } else {
 #pragma unroll
                                 for (int i = 0; i < 32; ++i)
@@ -415,14 +476,14 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
                     }
                 }
             }
-            if (!ok) break;
         }
     }
 
     __syncthreads();
+    if constexpr (kPair) ptx::cluster_sync();
     if (warp == 1) {
         ptx::tc_fence_after();
-        ptx::tmem_dealloc(tmem_base, kTmemCols);
+        ptx::tmem_dealloc<kG>(tmem_base, kTmemCols);
     }
 }
 

@@ -18,8 +18,9 @@ struct GemmParams;
 
 // GEMM launch: kind selects the instantiation.
 enum GemmKind : int { GEMM_F16 = 0, GEMM_BF16 = 1, GEMM_INT_AS_F16 = 2 };
-cudaError_t launch_gemm(GemmKind kind, const GemmParams &p, int num_sms, cudaStream_t stream);
-int gemm_smem_bytes();
+// group: 1 = one CTA per 128 x 256 tile, 2 = a CTA pair per 256 x 256 tile.
+int gemm_group_for(int m);
+cudaError_t launch_gemm(GemmKind kind, int group, const GemmParams &p, int num_sms, cudaStream_t stream);
 int read_and_clear_gemm_status(int *status);
 
 cudaError_t launch_quant_pertoken(const ChunkPtrs &chunks, int rank_size, int64_t bs_local, int h, bool bf16,

@@ -205,8 +205,9 @@ int mc2_all_gather_mm(const void *const *x_chunks, int world_size, int64_t m_loc
     p.a_mode = mc2::A_MCONCAT;
     p.a_box_rows = box_rows;
     p.m_local = static_cast<int>(m_local);
+    const int group = mc2::gemm_group_for(static_cast<int>(m));
     if (x2_is_nk) {
-        if (!make_map16(&p.b_map, x2, k, n, mc2::kBK, mc2::kBN))
+        if (!make_map16(&p.b_map, x2, k, n, mc2::kBK, mc2::kBN / group))
             return fail(MC2_ERR_CUDA, "cuTensorMapEncodeTiled failed for x2 (n, k)");
         p.b_mn_major = 0;
     } else {
@@ -222,11 +223,11 @@ int mc2_all_gather_mm(const void *const *x_chunks, int world_size, int64_t m_loc
     p.m = static_cast<int>(m);
     p.n = static_cast<int>(n);
     p.k = static_cast<int>(k);
-    p.kblock_tiles = 1;
+    p.kblock_tiles = 1024 / mc2::kBK;
     p.out = out;
     p.bias16 = bias;
     p.wait_limit_ns = kWaitLimitNs;
-    cudaError_t e = mc2::launch_gemm(dtype == MC2_BF16 ? mc2::GEMM_BF16 : mc2::GEMM_F16, p, dev.num_sms,
+    cudaError_t e = mc2::launch_gemm(dtype == MC2_BF16 ? mc2::GEMM_BF16 : mc2::GEMM_F16, group, p, dev.num_sms,
                                      static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail(MC2_ERR_CUDA, "GEMM launch: %s", cudaGetErrorString(e));
     return MC2_OK;
@@ -319,7 +320,7 @@ int mc2_alltoall_quant_mm(const void *const *chunks, int rank_size, int64_t bs_l
     p.bias_q_bf16 = bias_dtype == MC2_BF16;
     p.acc_out = acc_out;
     p.wait_limit_ns = kWaitLimitNs;
-    e = mc2::launch_gemm(mc2::GEMM_INT_AS_F16, p, dev.num_sms, s);
+    e = mc2::launch_gemm(mc2::GEMM_INT_AS_F16, mc2::gemm_group_for(static_cast<int>(bs_local)), p, dev.num_sms, s);
     if (e != cudaSuccess) return fail(MC2_ERR_CUDA, "GEMM launch: %s", cudaGetErrorString(e));
     return MC2_OK;
 }

@@ -24,8 +24,12 @@ def assert_close_16(got: torch.Tensor, ref: torch.Tensor, what: str = "out"):
     small_err = torch.where(big, torch.zeros_like(err), err)
     worst_rel = rel.max().item() if rel.numel() else 0.0
     worst_abs = small_err.max().item() if small_err.numel() else 0.0
-    assert worst_rel <= REL_TOL and worst_abs <= ABS_TOL, \
-        f"{what}: max rel err {worst_rel:.3e} (tol {REL_TOL}), max abs err on small values {worst_abs:.3e}"
+    if not (worst_rel <= REL_TOL and worst_abs <= ABS_TOL):
+        idx = tuple(int(i) for i in (rel == rel.max()).nonzero()[0])
+        nbad = int(((rel > REL_TOL) | (small_err > ABS_TOL)).sum())
+        raise AssertionError(
+            f"{what}: max rel err {worst_rel:.3e} (tol {REL_TOL}), max abs err on small values {worst_abs:.3e}; "
+            f"{nbad} of {g.numel()} elements outside; worst at {idx}: got {g[idx].item():.6e} ref {r[idx].item():.6e}")
 
 
 def assert_bits_equal(got: torch.Tensor, ref: torch.Tensor, what: str):
