@@ -32,8 +32,10 @@
 //   warp 0      TMA producer (one lane)
 //   warp 1      TMEM allocator; MMA issuer (one lane; the leader CTA for kG = 2)
 //   warp 2      gathered-output TMA store (one lane; AllGather with gather only).
-//               For kG = 2 the peer CTA's A tile completes a barrier of its
-//               own and this warp relays the arrival to the leader's barrier.
+//               On n-tile-0 tiles the MMA commits each stage to a "consumed"
+//               barrier instead of "empty"; this warp then stores the A tile
+//               (already complete: the MMA read it) and frees the stage, so
+//               the store never delays the MMAs.
 //   warp 3      idle
 //   warps 4-11  epilogue: warp w reads TMEM lanes 32*(w%4)..+31 (its rows) and
 //               half (w-4)/4 of the 256 accumulator columns.
@@ -104,16 +106,32 @@ __device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int 
     nb = r / gsz;
 }
 
+// Slow path of a barrier wait: poll with a wall-clock limit and the CTA's
+// abort flag; on timeout raise both the flag and the device status word.
+template <bool kCluster>
+__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, uint64_t limit_ns, int *status,
+                                       volatile int *abort_flag) {
+    const uint64_t start = ptx::globaltimer_ns();
+    for (uint32_t it = 0;; ++it) {
+        if (kCluster ? ptx::mbar_try_wait_cluster(bar, parity) : ptx::mbar_try_wait(bar, parity)) return true;
+        if ((it & 63u) == 63u) {
+            if (*abort_flag) return false;
+            if (ptx::globaltimer_ns() - start > limit_ns) {
+                *abort_flag = 1;
+                if (status) atomicExch(status, -7);
+                return false;
+            }
+        }
+    }
+}
+
+// Wait for the phase of `bar` with parity `parity`: one try_wait on the fast
+// path, the bounded loop otherwise.
 template <bool kCluster>
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, const GemmParams &p,
                                               volatile int *abort_flag) {
-    if (*abort_flag) return false;
-    const bool ok = kCluster ? ptx::mbar_wait_cluster(bar, parity, p.wait_limit_ns)
-                             : ptx::mbar_wait(bar, parity, p.wait_limit_ns);
-    if (ok) return true;
-    *abort_flag = 1;
-    if (p.status) atomicExch(p.status, -7);
-    return false;
+    if (kCluster ? ptx::mbar_try_wait_cluster(bar, parity) : ptx::mbar_try_wait(bar, parity)) return true;
+    return wait_slow<kCluster>(bar, parity, p.wait_limit_ns, p.status, abort_flag);
 }
 
 template <bool kBF16>
@@ -159,11 +177,12 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S * Cfg::kStageBytes);
-    uint64_t *full_bar = bars;            // A/B landed (leader: whole pair; peer: its own A when relaying)
-    uint64_t *empty_bar = bars + S;       // stage free in this CTA
-    uint64_t *tfull_bar = bars + 2 * S;   // accumulator buffer ready
-    uint64_t *tempty_bar = bars + 2 * S + 2;  // accumulator buffer drained (leader's counts both CTAs)
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * S + 4);
+    uint64_t *full_bar = bars;                // A/B of the stage landed (the leader's counts both CTAs)
+    uint64_t *empty_bar = bars + S;           // stage free in this CTA
+    uint64_t *consumed_bar = bars + 2 * S;    // gathered tiles: the MMAs have read the stage
+    uint64_t *tfull_bar = bars + 3 * S;       // accumulator buffer ready
+    uint64_t *tempty_bar = bars + 3 * S + 2;  // accumulator buffer drained (the leader's counts both CTAs)
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 3 * S + 4);
     __shared__ int abort_flag_s;
     volatile int *abort_flag = &abort_flag_s;
 
@@ -171,7 +190,6 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
     const int lane = threadIdx.x & 31;
     const uint32_t cr = kPair ? ptx::cluster_ctarank() : 0u;  // rank inside the pair
     const bool leader = cr == 0;
-    const bool relay = kPair && p.gather;  // peer A lands on the peer's own barrier, relayed by warp 2
     const int num_m = (p.m + Cfg::kTileM - 1) / Cfg::kTileM;
     const int num_n = (p.n + kBN - 1) / kBN;
     const int num_tiles = num_m * num_n;
@@ -182,8 +200,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
     if (threadIdx.x == 0) {
         abort_flag_s = 0;
         for (int s = 0; s < S; ++s) {
-            ptx::mbar_init(ptx::smem_u32(&full_bar[s]), (kPair && leader && relay) ? 2 : 1);
-            ptx::mbar_init(ptx::smem_u32(&empty_bar[s]), p.gather ? 2 : 1);
+            ptx::mbar_init(ptx::smem_u32(&full_bar[s]), 1);
+            ptx::mbar_init(ptx::smem_u32(&empty_bar[s]), 1);
+            ptx::mbar_init(ptx::smem_u32(&consumed_bar[s]), 1);
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(ptx::smem_u32(&tfull_bar[b]), 1);
@@ -205,9 +224,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
         // ------------------------------------------------------------ TMA producer
         for (int i = 0; i < p.num_a_maps; ++i) ptx::prefetch_tmap(&p.a_maps[i]);
         ptx::prefetch_tmap(&p.b_map);
-        // bytes that complete the leader's full barrier per stage
-        uint32_t leader_bytes = Cfg::kStageBytes;
-        if (kPair) leader_bytes += Cfg::kBTileBytes + (relay ? 0u : kATileBytes);
+        // bytes that complete the leader's full barrier per stage (both CTAs' tiles)
+        constexpr uint32_t leader_bytes = Cfg::kStageBytes * kG;
         int stage = 0;
         uint32_t phase = 0;
         int iters = 0;
@@ -217,6 +235,18 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
             tile_coords(tile, num_m, num_n, mb, nb);
             const int m0 = mb * Cfg::kTileM + kBM * static_cast<int>(cr);
             const int n0 = nb * kBN + Cfg::kBRows * static_cast<int>(cr);
+            // first A box of this tile: chunk and row inside it (rows past m stay in the
+            // last chunk, out of its range, and read as zeros)
+            int a_chunk0 = 0, a_row0 = m0, a_nbox = 1;
+            if (p.a_mode == A_MCONCAT) {
+                a_chunk0 = m0 / p.m_local;
+                a_row0 = m0 - a_chunk0 * p.m_local;
+                if (a_chunk0 > p.num_a_maps - 1) {
+                    a_row0 += (a_chunk0 - (p.num_a_maps - 1)) * p.m_local;
+                    a_chunk0 = p.num_a_maps - 1;
+                }
+                a_nbox = kBM / p.a_box_rows;
+            }
             for (int kt = 0; kt < num_k; ++kt) {
                 if (!wait_or_abort<kPair>(ptx::smem_u32(&empty_bar[stage]), phase ^ 1u, p, abort_flag)) {
                     ok = false;
@@ -229,12 +259,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
                 if (leader) {
                     ptx::mbar_arrive_expect_tx(local_full, leader_bytes);
                 } else {
-                    const uint32_t leader_full = ptx::mapa(local_full, 0);
-                    b_bar = leader_full;
-                    if (relay)
-                        ptx::mbar_arrive_expect_tx(local_full, kATileBytes);
-                    else
-                        a_bar = leader_full;
+                    a_bar = b_bar = ptx::mapa(local_full, 0);
                 }
                 const int k0 = kt * kBK;
                 auto load = [&](uint32_t dst, const CUtensorMap *m, int c0, int c1, uint32_t bar) {
@@ -244,12 +269,12 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
                         ptx::tma_load_2d(dst, m, c0, c1, bar);
                 };
                 if (p.a_mode == A_MCONCAT) {
-                    const int nbox = kBM / p.a_box_rows;
-                    for (int j = 0; j < nbox; ++j) {
-                        const int i0 = m0 + j * p.a_box_rows;
-                        const int c = min(i0 / p.m_local, p.num_a_maps - 1);
-                        const int li = i0 - c * p.m_local;
+                    // walk the tile's boxes through the chunks (box_rows divides m_local)
+                    int c = a_chunk0, li = a_row0;
+                    for (int j = 0; j < a_nbox; ++j) {
                         load(sA + j * p.a_box_rows * 128, &p.a_maps[c], k0, li, a_bar);
+                        li += p.a_box_rows;
+                        if (li >= p.m_local && c < p.num_a_maps - 1) li -= p.m_local, ++c;
                     }
                 } else if (p.a_mode == A_KINTERLEAVE) {
                     const int c = k0 / p.k_local;
@@ -270,7 +295,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
         }
         if (!ok) {
             // let the copies already in flight land before the CTA can exit
-            const bool armed_local = !kPair || leader || relay;
+            const bool armed_local = leader;
             for (int back = 1; back <= S && back <= iters && armed_local; ++back) {
                 const int i = iters - back;
                 (void)ptx::mbar_wait(ptx::smem_u32(&full_bar[i % S]), static_cast<uint32_t>((i / S) & 1),
@@ -281,14 +306,30 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
     } else if (warp == 1 && lane == 0 && leader) {
         // ------------------------------------------------------------ MMA issuer
         const uint32_t idesc = ptx::idesc_f16(kBF16 && !kIntPath, p.b_mn_major != 0, Cfg::kTileM, kBN);
+        // descriptors of stage 0, k-slice 0; later ones add to the address field
+        // (>> 4 units): +2 per 16-wide k-slice of A, +stage bytes per stage
+        const uint32_t s0 = ptx::smem_u32(smem);
+        const uint64_t a_desc0 = ptx::smem_desc_sw128(s0, 16, 1024);
+        const uint64_t b_desc0 = p.b_mn_major ? ptx::smem_desc_sw128(s0 + kATileBytes, kBK * 128, 1024)
+                                              : ptx::smem_desc_sw128(s0 + kATileBytes, 16, 1024);
+        const uint32_t b_kk = p.b_mn_major ? (2048u >> 4) : (32u >> 4);
+        constexpr uint32_t kStageStep = Cfg::kStageBytes >> 4;
+        const uint32_t full0 = ptx::smem_u32(&full_bar[0]);
+        const uint32_t empty0 = ptx::smem_u32(&empty_bar[0]);
+        const int kblock = p.kblock_tiles;
         int stage = 0;
-        uint32_t phase = 0;
+        uint32_t phase = 0, stage_off = 0;
         uint32_t acc_iter = 0;
         bool ok = true;
         uint32_t d_tmem = tmem_base;
+        const uint32_t consumed0 = ptx::smem_u32(&consumed_bar[0]);
         for (int tile = cluster_id; tile < num_tiles && ok; tile += num_clusters) {
+            int mb, nb;
+            tile_coords(tile, num_m, num_n, mb, nb);
+            // stages of gathered tiles go to the gathered-store warp before being freed
+            const uint32_t release0 = (p.gather && nb == 0) ? consumed0 : empty0;
+            int kin = 0;  // k-tile index inside the current K block
             for (int kt = 0; kt < num_k; ++kt) {
-                const int kin = kt % p.kblock_tiles;  // k-tile index inside the current K block
                 if (kin == 0) {
                     const uint32_t b = acc_iter & 1u;
                     if (!wait_or_abort<kPair>(ptx::smem_u32(&tempty_bar[b]), ((acc_iter >> 1) & 1u) ^ 1u, p,
@@ -299,67 +340,66 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
                     ptx::tc_fence_after();
                     d_tmem = tmem_base + b * kBN;
                 }
-                if (!wait_or_abort<kPair>(ptx::smem_u32(&full_bar[stage]), phase, p, abort_flag)) {
+                if (!wait_or_abort<kPair>(full0 + 8u * stage, phase, p, abort_flag)) {
                     ok = false;
                     break;
                 }
                 ptx::tc_fence_after();
-                const uint32_t sA = ptx::smem_u32(smem + stage * Cfg::kStageBytes);
-                const uint32_t sB = sA + kATileBytes;
-#pragma unroll
-                for (int kk = 0; kk < kBK / 16; ++kk) {
-                    const uint64_t ad = ptx::smem_desc_sw128(sA + kk * 32, 16, 1024);
-                    const uint64_t bd = p.b_mn_major ? ptx::smem_desc_sw128(sB + kk * 2048, kBK * 128, 1024)
-                                                     : ptx::smem_desc_sw128(sB + kk * 32, 16, 1024);
-                    ptx::mma_f16_ss<kG>(d_tmem, ad, bd, idesc, (kin > 0 || kk > 0) ? 1u : 0u);
+                const uint64_t ad = a_desc0 + stage_off;
+                const uint64_t bd = b_desc0 + stage_off;
+                ptx::mma_f16_ss<kG>(d_tmem, ad, bd, idesc, kin > 0 ? 1u : 0u);
+                ptx::mma_f16_ss<kG>(d_tmem, ad + 2, bd + b_kk, idesc, 1u);
+                ptx::mma_f16_ss<kG>(d_tmem, ad + 4, bd + 2 * b_kk, idesc, 1u);
+                ptx::mma_f16_ss<kG>(d_tmem, ad + 6, bd + 3 * b_kk, idesc, 1u);
+                ptx::mma_commit<kG>(release0 + 8u * stage);
+                if (++stage == S) {
+                    stage = 0;
+                    stage_off = 0;
+                    phase ^= 1u;
+                } else {
+                    stage_off += kStageStep;
                 }
-                ptx::mma_commit<kG>(ptx::smem_u32(&empty_bar[stage]));
-                if (++stage == S) stage = 0, phase ^= 1u;
-                if (kin == p.kblock_tiles - 1 || kt == num_k - 1) {
+                if (++kin == kblock || kt == num_k - 1) {
                     ptx::mma_commit<kG>(ptx::smem_u32(&tfull_bar[acc_iter & 1u]));
                     ++acc_iter;
+                    kin = 0;
                 }
             }
         }
     } else if (warp == 2 && lane == 0 && p.gather) {
-        // ------------------------------------------------------------ gathered store (+ relay)
+        // ------------------------------------------------------------ gathered store
         ptx::prefetch_tmap(&p.g_map);
         int stage = 0;
-        uint32_t phase = 0;
-        int pending_stage = -1;  // stage whose store may still be reading shared memory
-        for (int tile = cluster_id; tile < num_tiles; tile += num_clusters) {
+        uint32_t consumed_parity = 0;  // bit s: parity of the next consumed_bar[s] phase
+        int pending_stage = -1;        // stage whose store may still be reading shared memory
+        bool ok = true;
+        for (int tile = cluster_id; tile < num_tiles && ok; tile += num_clusters) {
             int mb, nb;
             tile_coords(tile, num_m, num_n, mb, nb);
+            if (nb != 0) {  // not a gathered tile: its stages are freed by the MMA directly
+                stage = (stage + num_k) % S;
+                continue;
+            }
             const int m0 = mb * Cfg::kTileM + kBM * static_cast<int>(cr);
-            bool ok = true;
             for (int kt = 0; kt < num_k; ++kt) {
-                if (!wait_or_abort<kPair>(ptx::smem_u32(&full_bar[stage]), phase, p, abort_flag)) {
+                if (!wait_or_abort<kPair>(ptx::smem_u32(&consumed_bar[stage]), (consumed_parity >> stage) & 1u, p,
+                                          abort_flag)) {
                     ok = false;
                     break;
                 }
-                if (kPair && !leader) ptx::mbar_arrive_remote(ptx::mapa(ptx::smem_u32(&full_bar[stage]), 0));
-                if (nb == 0) {
-                    const uint32_t sA = ptx::smem_u32(smem + stage * Cfg::kStageBytes);
-                    ptx::tma_store_2d(&p.g_map, kt * kBK, m0, sA);
-                    ptx::bulk_commit_group();
-                    // release the previous stage once its store has finished reading
-                    ptx::bulk_wait_group_read<1>();
-                    if (pending_stage >= 0) ptx::mbar_arrive(ptx::smem_u32(&empty_bar[pending_stage]));
-                    pending_stage = stage;
-                } else {
-                    if (pending_stage >= 0) {
-                        ptx::bulk_wait_group_read<0>();
-                        ptx::mbar_arrive(ptx::smem_u32(&empty_bar[pending_stage]));
-                        pending_stage = -1;
-                    }
-                    ptx::mbar_arrive(ptx::smem_u32(&empty_bar[stage]));
-                }
-                if (++stage == S) stage = 0, phase ^= 1u;
+                consumed_parity ^= 1u << stage;
+                ptx::tma_store_2d(&p.g_map, kt * kBK, m0, ptx::smem_u32(smem + stage * Cfg::kStageBytes));
+                ptx::bulk_commit_group();
+                // free the previous stage once its store has finished reading it
+                ptx::bulk_wait_group_read<1>();
+                if (pending_stage >= 0) ptx::mbar_arrive(ptx::smem_u32(&empty_bar[pending_stage]));
+                pending_stage = stage;
+                if (++stage == S) stage = 0;
             }
-            if (!ok) break;
+            ptx::bulk_wait_group_read<0>();
+            if (pending_stage >= 0) ptx::mbar_arrive(ptx::smem_u32(&empty_bar[pending_stage]));
+            pending_stage = -1;
         }
-        ptx::bulk_wait_group_read<0>();
-        if (pending_stage >= 0) ptx::mbar_arrive(ptx::smem_u32(&empty_bar[pending_stage]));
         ptx::bulk_wait_group<0>();
     } else if (warp >= 4) {
         // ------------------------------------------------------------ epilogue
