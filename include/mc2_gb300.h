@@ -12,8 +12,9 @@
  *     of device pointers.
  *   - Work is enqueued on `stream` (a cudaStream_t passed as void*; NULL is the
  *     legacy default stream) and the call returns without synchronising.  The
- *     library keeps no state between calls and never allocates device memory:
- *     scratch space is the caller's `workspace`.
+ *     library never allocates device memory: scratch space is the caller's
+ *     `workspace`.  The one exception is mc2_alltoall_quant_mm_no_alloc, which
+ *     uses a fixed scratch array built into the library (see there).
  *   - Arguments are validated before anything is launched.  A violated
  *     constraint returns a negative mc2_status and launches nothing;
  *     mc2_last_error() then describes which argument failed (thread-local).
@@ -134,6 +135,39 @@ int mc2_alltoall_quant_mm(const void *const *chunks, int rank_size, int64_t bs_l
                           const void *bias, int bias_dtype, int x1_quant_mode, int x2_quant_mode,
                           int64_t n, void *out, int8_t *q_out, float *x1_scale_out, int32_t *acc_out,
                           void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * AlltoAllQuantMatmul for callers that cannot allocate device memory.  The
+ * pages have no counterpart of this call: it is this library's own addition.
+ *
+ * mc2_alltoall_quant_mm needs a caller-provided workspace.  Some callers cannot
+ * provide one: a C or Fortran host program that links only this library and
+ * owns no device allocator, or a plugin inside a framework that owns all device
+ * memory and forbids its plugins to call cudaMalloc (it can synchronise the
+ * device and fragments the framework's pool).  This call takes the same
+ * arguments minus the workspace and computes the same result, using a scratch
+ * array built into the library instead.
+ *
+ *   - The scratch is MC2_NO_ALLOC_SCRATCH_BYTES (32 MiB).  Every GPU that
+ *     loads the library holds it until the process exits.
+ *   - Sizes whose workspace (as mc2_alltoall_quant_mm_workspace reports it)
+ *     exceeds that are refused with MC2_ERR_WORKSPACE before anything is
+ *     launched.
+ *   - The call never calls cudaMalloc, cudaFree or any allocating routine.
+ *   - The first call on each device looks up the scratch's device address,
+ *     with that device current; make that first call before any stream capture.
+ *   - All calls share the one scratch array, and it keeps whatever the last
+ *     call wrote (nothing in it needs to start at zero).  Calls whose work can
+ *     overlap on the GPU (other streams, other host threads) race on it and
+ *     must be serialised by the caller.
+ *   - Other arguments, outputs and errors are those of mc2_alltoall_quant_mm.
+ */
+#define MC2_NO_ALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+
+int mc2_alltoall_quant_mm_no_alloc(const void *const *chunks, int rank_size, int64_t bs_local, int64_t h,
+                                   int x1_dtype, const void *x1_scale, const int8_t *x2, const float *x2_scale,
+                                   const void *bias, int bias_dtype, int x1_quant_mode, int x2_quant_mode, int64_t n,
+                                   void *out, int8_t *q_out, float *x1_scale_out, int32_t *acc_out, void *stream);
 
 /* Name of a status code (static string). */
 const char *mc2_status_str(int status);

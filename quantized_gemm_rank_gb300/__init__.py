@@ -60,6 +60,9 @@ def lib() -> ctypes.CDLL:
         L.mc2_alltoall_quant_mm.argtypes = [_P, _INT, _I64, _I64, _INT, _P, _P, _P, _P, _INT, _INT, _INT, _I64,
                                             _P, _P, _P, _P, _P, ctypes.c_size_t, _P]
         L.mc2_alltoall_quant_mm.restype = _INT
+        L.mc2_alltoall_quant_mm_no_alloc.argtypes = [_P, _INT, _I64, _I64, _INT, _P, _P, _P, _P, _INT, _INT, _INT,
+                                                     _I64, _P, _P, _P, _P, _P]
+        L.mc2_alltoall_quant_mm_no_alloc.restype = _INT
         L.mc2_status_str.argtypes = [_INT]
         L.mc2_status_str.restype = ctypes.c_char_p
         L.mc2_last_error.argtypes = []
@@ -178,6 +181,36 @@ def mc2_alltoall_quant_mm(chunks: Sequence[torch.Tensor], x2: torch.Tensor, x2_s
     return {"out": out, "q": q_out, "x1_scale": x1_scale_out, "acc": acc_out}
 
 
+NO_ALLOC_SCRATCH_BYTES = 32 << 20
+
+
+def mc2_alltoall_quant_mm_no_alloc(chunks: Sequence[torch.Tensor], x2: torch.Tensor, x2_scale: torch.Tensor,
+                                   bias: torch.Tensor, *, x1_quant_mode: int, out: torch.Tensor,
+                                   x1_scale: Optional[torch.Tensor] = None, x2_quant_mode: int = QUANT_PERCHANNEL,
+                                   q_out: Optional[torch.Tensor] = None, x1_scale_out: Optional[torch.Tensor] = None,
+                                   acc_out: Optional[torch.Tensor] = None, stream=None) -> dict:
+    """The same computation as mc2_alltoall_quant_mm without a workspace.
+
+    For callers that cannot allocate device memory: the library's built-in
+    scratch (NO_ALLOC_SCRATCH_BYTES per GPU) is used instead, so problems whose
+    workspace would exceed it are refused.  ``out`` must be given (nothing is
+    allocated here).  Calls that may overlap on the GPU share that scratch and
+    must be serialised by the caller.
+    """
+    R = len(chunks)
+    bs_local, h = chunks[0].shape
+    n = x2.shape[1]
+    ptrs = _ptrs(chunks, "chunks")
+    st = lib().mc2_alltoall_quant_mm_no_alloc(ptrs, R, bs_local, h, _dtype_code(chunks[0].dtype),
+                                              _opt(x1_scale, "x1_scale"), _dev(x2, "x2"), _dev(x2_scale, "x2_scale"),
+                                              _dev(bias, "bias"), _dtype_code(bias.dtype), x1_quant_mode,
+                                              x2_quant_mode, n, _dev(out, "out"), _opt(q_out, "q_out"),
+                                              _opt(x1_scale_out, "x1_scale_out"), _opt(acc_out, "acc_out"),
+                                              _stream(stream))
+    _check(st)
+    return {"out": out, "q": q_out, "x1_scale": x1_scale_out, "acc": acc_out}
+
+
 def mc2_device_status() -> int:
     """Synchronise and return (and clear) the kernels' bounded-wait status."""
     return int(lib().mc2_device_status())
@@ -185,7 +218,8 @@ def mc2_device_status() -> int:
 
 __all__ = [
     "Mc2Error", "lib", "library_path", "status_str", "last_error", "mc2_all_gather_mm",
-    "mc2_alltoall_quant_mm_workspace", "mc2_alltoall_quant_mm", "mc2_device_status",
+    "mc2_alltoall_quant_mm_workspace", "mc2_alltoall_quant_mm", "mc2_alltoall_quant_mm_no_alloc",
+    "NO_ALLOC_SCRATCH_BYTES", "mc2_device_status",
     "MC2_OK", "MC2_ERR_NULL", "MC2_ERR_SHAPE", "MC2_ERR_DTYPE", "MC2_ERR_UNSUPPORTED", "MC2_ERR_WORKSPACE",
     "MC2_ERR_CUDA", "MC2_ERR_TIMEOUT", "MC2_F16", "MC2_BF16", "MC2_F32", "MC2_I8",
     "QUANT_PERCHANNEL", "QUANT_PERTOKEN", "QUANT_PERTOKEN_DYNAMIC",

@@ -23,6 +23,9 @@ int gemm_group_for(int m);
 cudaError_t launch_gemm(GemmKind kind, int group, const GemmParams &p, int num_sms, cudaStream_t stream);
 int read_and_clear_gemm_status(int *status);
 
+// Records `msg` as this thread's mc2_last_error() text and returns `status`.
+int record_error(int status, const char *msg);
+
 cudaError_t launch_quant_pertoken(const ChunkPtrs &chunks, int rank_size, int64_t bs_local, int h, bool bf16,
                                   const void *smooth, __half *qh, int8_t *q_out, float *scale_out, int num_sms,
                                   cudaStream_t stream);

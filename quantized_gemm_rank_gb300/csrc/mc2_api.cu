@@ -131,6 +131,10 @@ int validate_a2a(int rank_size, int64_t bs_local, int64_t h, int64_t n, int x1_q
 
 }  // namespace
 
+namespace mc2 {
+int record_error(int status, const char *msg) { return fail(status, "%s", msg); }
+}  // namespace mc2
+
 extern "C" {
 
 const char *mc2_status_str(int status) {
