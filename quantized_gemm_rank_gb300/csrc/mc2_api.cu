@@ -291,7 +291,12 @@ int mc2_alltoall_quant_mm(const void *const *chunks, int rank_size, int64_t bs_l
     for (int r = 0; r < rank_size; ++r) cp.p[r] = chunks[r];
 
     cudaError_t e;
-    if (x1_quant_mode == MC2_QUANT_PERTOKEN_DYNAMIC) {
+    bool x2_done = false;
+    if (x1_quant_mode == MC2_QUANT_PERTOKEN_DYNAMIC && mc2::a2a_prologue_fits(rank_size, bs_local, static_cast<int>(h))) {
+        e = mc2::launch_a2a_prologue(cp, rank_size, bs_local, static_cast<int>(h), x1_dtype == MC2_BF16, x1_scale, ah,
+                                     q_out, scale, x2, x2h, K * n, s);
+        x2_done = true;
+    } else if (x1_quant_mode == MC2_QUANT_PERTOKEN_DYNAMIC) {
         e = mc2::launch_quant_pertoken(cp, rank_size, bs_local, static_cast<int>(h), x1_dtype == MC2_BF16, x1_scale,
                                        ah, q_out, scale, dev.num_sms, s);
     } else {
@@ -301,7 +306,7 @@ int mc2_alltoall_quant_mm(const void *const *chunks, int rank_size, int64_t bs_l
         scale = const_cast<float *>(static_cast<const float *>(x1_scale));
     }
     if (e != cudaSuccess) return fail(MC2_ERR_CUDA, "prologue launch: %s", cudaGetErrorString(e));
-    e = mc2::launch_widen_i8(x2, x2h, K * n, dev.num_sms, s);
+    if (!x2_done) e = mc2::launch_widen_i8(x2, x2h, K * n, dev.num_sms, s);
     if (e != cudaSuccess) return fail(MC2_ERR_CUDA, "x2 widening launch: %s", cudaGetErrorString(e));
 
     mc2::GemmParams p;

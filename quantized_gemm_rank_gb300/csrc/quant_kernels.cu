@@ -55,7 +55,7 @@ __device__ __forceinline__ int quant1(float y, float scale) {
 // scale = absmax / 127 (IEEE division).  Pass 2 (row re-read from L1/L2):
 // q, written as exact fp16 (GEMM operand) and optionally as int8.
 template <bool kBF16>
-__global__ void __launch_bounds__(256) quant_pertoken_kernel(ChunkPtrs chunks, int h, int64_t bs_local, int rank_size,
+__global__ void __launch_bounds__(256) quant_pertoken_kernel(const __grid_constant__ ChunkPtrs chunks, int h, int64_t bs_local, int rank_size,
                                                              const uint16_t *__restrict__ smooth,
                                                              __half *__restrict__ qh, int8_t *__restrict__ q_out,
                                                              float *__restrict__ scale_out) {
@@ -136,6 +136,151 @@ __global__ void __launch_bounds__(256) quant_pertoken_kernel(ChunkPtrs chunks, i
     }
 }
 
+// ---------------------------------------------------------------------------
+// Fused prologue of the dynamic-quant scenario, for h % 8 == 0 and
+// rank_size*h <= 512*64: one launch whose CTAs take one of two roles,
+// interleaved so that both run side by side on every SM --
+//   * quant CTAs (one per permuted row): the row stays in registers (kV 16-byte
+//     vectors per thread, vector v of thread i = permuted columns
+//     (v*blockDim + i)*8 .. +7), so it is read from HBM once;
+//   * widen CTAs (every kWidenEvery-th CTA): a contiguous slice of x2, int8 ->
+//     fp16.
+// The quant role is instruction-bound and the widening memory-bound, which is
+// why they share the launch.
+//
+// Rounding without a division.  With rcp = 1/scale correctly rounded,
+// qa = fl(y * rcp) and the correctly rounded quotient z = fl(y / scale) are
+// both within a relative 2^-23 of y / scale, and |y / scale| < 127.5, so
+// |qa - z| < 2^-15.  k = fl(qa + M) - M with M = 1.5 * 2^23 is qa rounded to
+// the nearest integer, ties to even (every value in [2^23, 2^24) is an
+// integer and M is even), and d = qa - k is exact.  If |d| <= 0.5 - 2^-12,
+// z lies strictly between k - 1/2 and k + 1/2, so rne(z) = k; otherwise (rare,
+// and every exact tie) the IEEE division decides.  qa <= 127 * (1 + 3*2^-24)
+// keeps k inside [-127, 127], and the low byte of fl(qa + M) is k mod 256,
+// i.e. the int8 q.
+constexpr int kWidenEvery = 5;
+constexpr float kRoundMagic = 12582912.0f;  // 1.5 * 2^23
+
+template <bool kBF16>
+__device__ __forceinline__ float2 unpack2(uint32_t w) {
+    if constexpr (kBF16) {
+        return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+    } else {
+        return __half22float2(*reinterpret_cast<const __half2 *>(&w));
+    }
+}
+
+template <bool kBF16, int kV>
+__global__ void __launch_bounds__(512) a2a_prologue_kernel(const __grid_constant__ ChunkPtrs chunks, int h,
+                                                           int64_t bs_local, int rank_size,
+                                                           const uint16_t *__restrict__ smooth,
+                                                           __half *__restrict__ qh, int8_t *__restrict__ q_out,
+                                                           float *__restrict__ scale_out,
+                                                           const int8_t *__restrict__ x2,
+                                                           __half *__restrict__ x2h, int64_t x2_vecs,
+                                                           int64_t widen_ctas) {
+    const int64_t b = blockIdx.x;
+    if (b % kWidenEvery == kWidenEvery - 1) {
+        // ---- widen role: vectors [w * per, (w + 1) * per) of 16 int8 each
+        const int64_t w = b / kWidenEvery;
+        const int64_t per = (x2_vecs + widen_ctas - 1) / widen_ctas;
+        const int64_t end = min(x2_vecs, (w + 1) * per);
+        for (int64_t i = w * per + threadIdx.x; i < end; i += blockDim.x) {
+            const int4 v = __ldg(reinterpret_cast<const int4 *>(x2) + i);
+            const int8_t *e = reinterpret_cast<const int8_t *>(&v);
+            uint4 o[2];
+            __half2 *oh = reinterpret_cast<__half2 *>(o);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                oh[j] = __floats2half2_rn(static_cast<float>(e[2 * j]), static_cast<float>(e[2 * j + 1]));
+            reinterpret_cast<uint4 *>(x2h)[2 * i] = o[0];
+            reinterpret_cast<uint4 *>(x2h)[2 * i + 1] = o[1];
+        }
+        return;
+    }
+    // ---- quant role: permuted row t
+    const int64_t t = b - b / kWidenEvery;
+    if (t >= bs_local) return;
+    __shared__ float red[32];
+    const int K = rank_size * h;
+    const int nvec = K / 8;
+    uint4 xv[kV];
+#pragma unroll
+    for (int v = 0; v < kV; ++v) {
+        const int vi = v * blockDim.x + threadIdx.x;
+        xv[v] = make_uint4(0, 0, 0, 0);
+        if (vi < nvec) {
+            const int c = vi * 8;
+            const int r = c / h;
+            xv[v] = __ldg(reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(chunks.p[r]) + t * h +
+                                                          (c - r * h)));
+        }
+    }
+    // y = x * s (fp32, exact for 16-bit inputs); row absmax
+    float amax = 0.0f;
+#pragma unroll
+    for (int v = 0; v < kV; ++v) {
+        const int vi = v * blockDim.x + threadIdx.x;
+        const uint32_t *xw = reinterpret_cast<const uint32_t *>(&xv[v]);
+        uint4 sv = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);  // bf16 1.0
+        if (!kBF16) sv = make_uint4(0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u);  // fp16 1.0
+        if (smooth && vi < nvec) sv = __ldg(reinterpret_cast<const uint4 *>(smooth + vi * 8));
+        const uint32_t *sw = reinterpret_cast<const uint32_t *>(&sv);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 y = __fmul2_rn(unpack2<kBF16>(xw[e]), unpack2<kBF16>(sw[e]));
+            amax = fmaxf(amax, fmaxf(fabsf(y.x), fabsf(y.y)));
+        }
+    }
+    amax = block_max(amax, red);
+    const float scale = __fdiv_rn(amax, 127.0f);
+    const float rcp = scale == 0.0f ? 0.0f : __frcp_rn(scale);
+    const bool row_fast = rcp <= 3.0e38f;  // 1/scale finite (always, unless amax is subnormal)
+    if (threadIdx.x == 0) scale_out[t] = scale;
+    const float2 rcp2 = make_float2(rcp, rcp);
+    const float2 magic2 = make_float2(kRoundMagic, kRoundMagic);
+    const float2 nmagic2 = make_float2(-kRoundMagic, -kRoundMagic);
+#pragma unroll
+    for (int v = 0; v < kV; ++v) {
+        const int vi = v * blockDim.x + threadIdx.x;
+        if (vi >= nvec) continue;
+        const uint32_t *xw = reinterpret_cast<const uint32_t *>(&xv[v]);
+        uint4 sv = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+        if (!kBF16) sv = make_uint4(0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u);
+        if (smooth) sv = __ldg(reinterpret_cast<const uint4 *>(smooth + vi * 8));
+        const uint32_t *sw = reinterpret_cast<const uint32_t *>(&sv);
+        uint4 hv;
+        __half2 *hh = reinterpret_cast<__half2 *>(&hv);
+        uint32_t qb[8];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 y = __fmul2_rn(unpack2<kBF16>(xw[e]), unpack2<kBF16>(sw[e]));
+            const float2 qa = __fmul2_rn(y, rcp2);
+            const float2 tm = __fadd2_rn(qa, magic2);   // M + rne(qa)
+            const float2 k = __fadd2_rn(tm, nmagic2);   // rne(qa), exact
+            const float2 d = __fadd2_rn(qa, make_float2(-k.x, -k.y));
+            float2 kq = k;
+            uint32_t b0 = __float_as_uint(tm.x), b1 = __float_as_uint(tm.y);
+            if (!row_fast || fabsf(d.x) > 0.499755859375f || fabsf(d.y) > 0.499755859375f) {
+                const int q0 = quant1(y.x, scale), q1 = quant1(y.y, scale);
+                kq = make_float2(static_cast<float>(q0), static_cast<float>(q1));
+                b0 = static_cast<uint32_t>(q0);
+                b1 = static_cast<uint32_t>(q1);
+            }
+            hh[e] = __float22half2_rn(kq);
+            qb[2 * e] = b0;
+            qb[2 * e + 1] = b1;
+        }
+        *reinterpret_cast<uint4 *>(qh + t * K + vi * 8) = hv;
+        if (q_out) {
+            uint2 iv;
+            iv.x = __byte_perm(__byte_perm(qb[0], qb[1], 0x0040), __byte_perm(qb[2], qb[3], 0x0040), 0x5410);
+            iv.y = __byte_perm(__byte_perm(qb[4], qb[5], 0x0040), __byte_perm(qb[6], qb[7], 0x0040), 0x5410);
+            *reinterpret_cast<uint2 *>(q_out + t * K + vi * 8) = iv;
+        }
+    }
+}
+
 // int8 -> fp16, exact, 16 elements per thread-iteration.
 __global__ void __launch_bounds__(256) widen_i8_kernel(const int8_t *__restrict__ src, __half *__restrict__ dst,
                                                        int64_t count) {
@@ -157,7 +302,7 @@ __global__ void __launch_bounds__(256) widen_i8_kernel(const int8_t *__restrict_
 
 // Permuted int8 chunks -> fp16 GEMM operand (and optionally the int8
 // permuted matrix): dst[t, r*h + j] = chunk_r[t, j].
-__global__ void __launch_bounds__(256) permute_widen_i8_kernel(ChunkPtrs chunks, int h, int64_t bs_local,
+__global__ void __launch_bounds__(256) permute_widen_i8_kernel(const __grid_constant__ ChunkPtrs chunks, int h, int64_t bs_local,
                                                                int rank_size, __half *__restrict__ dst,
                                                                int8_t *__restrict__ q_out) {
     const int K = rank_size * h;
@@ -208,16 +353,40 @@ int grid_for(int64_t work_items, int threads, int num_sms) {
 cudaError_t launch_quant_pertoken(const ChunkPtrs &chunks, int rank_size, int64_t bs_local, int h, bool bf16,
                                   const void *smooth, __half *qh, int8_t *q_out, float *scale_out, int num_sms,
                                   cudaStream_t stream) {
+    const uint16_t *sm = static_cast<const uint16_t *>(smooth);
     const int64_t rows_cap = static_cast<int64_t>(num_sms) * 64;
     const int grid = static_cast<int>(bs_local < rows_cap ? bs_local : rows_cap);
     if (bf16)
-        quant_pertoken_kernel<true><<<grid, 256, 0, stream>>>(chunks, h, bs_local, rank_size,
-                                                              static_cast<const uint16_t *>(smooth), qh, q_out,
+        quant_pertoken_kernel<true><<<grid, 256, 0, stream>>>(chunks, h, bs_local, rank_size, sm, qh, q_out,
                                                               scale_out);
     else
-        quant_pertoken_kernel<false><<<grid, 256, 0, stream>>>(chunks, h, bs_local, rank_size,
-                                                               static_cast<const uint16_t *>(smooth), qh, q_out,
+        quant_pertoken_kernel<false><<<grid, 256, 0, stream>>>(chunks, h, bs_local, rank_size, sm, qh, q_out,
                                                                scale_out);
+    return cudaGetLastError();
+}
+
+bool a2a_prologue_fits(int rank_size, int64_t bs_local, int h) {
+    return h % 8 == 0 && static_cast<int64_t>(rank_size) * h <= 512 * 64 && bs_local <= (1ll << 30);
+}
+
+cudaError_t launch_a2a_prologue(const ChunkPtrs &chunks, int rank_size, int64_t bs_local, int h, bool bf16,
+                                const void *smooth, __half *qh, int8_t *q_out, float *scale_out, const int8_t *x2,
+                                __half *x2h, int64_t x2_count, cudaStream_t stream) {
+    constexpr int kV = 8;
+    const int K = rank_size * h;
+    int threads = 64;
+    while (threads * kV * 8 < K) threads *= 2;
+    // kWidenEvery - 1 quant CTAs for every widen CTA
+    const int64_t groups = (bs_local + kWidenEvery - 2) / (kWidenEvery - 1);
+    const int64_t grid = groups * kWidenEvery;
+    const int64_t widen_ctas = groups;
+    const uint16_t *sm = static_cast<const uint16_t *>(smooth);
+    if (bf16)
+        a2a_prologue_kernel<true, kV><<<static_cast<unsigned>(grid), threads, 0, stream>>>(
+            chunks, h, bs_local, rank_size, sm, qh, q_out, scale_out, x2, x2h, x2_count / 16, widen_ctas);
+    else
+        a2a_prologue_kernel<false, kV><<<static_cast<unsigned>(grid), threads, 0, stream>>>(
+            chunks, h, bs_local, rank_size, sm, qh, q_out, scale_out, x2, x2h, x2_count / 16, widen_ctas);
     return cudaGetLastError();
 }
 

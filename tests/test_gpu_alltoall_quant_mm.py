@@ -136,3 +136,38 @@ def test_without_debug_outputs_matches():
     a = run_gpu(inp, shape, want_debug=True)
     b = run_gpu(inp, shape, want_debug=False)
     assert_bits_equal(a["out"], b["out"], "out with/without debug outputs")
+
+
+def test_quant_ties_and_near_ties_on_gpu():
+    """Exact half-integer quotients (scale 1: every k + 0.5 for k in [-126, 125]),
+    values a few bf16 ulps around them, and the hand-derived golden rows: the GPU
+    must round each to the same integer as the oracle's IEEE division."""
+    import json
+    import os
+    R, h = 2, 256
+    K = R * h
+    rows = []
+    ties = [127.0] + [k + 0.5 for k in range(-126, 126)]
+    rows.append(ties + [0.0] * (K - len(ties)))
+    near = [127.0]
+    for k in range(-120, 120, 3):
+        for d in (-2 ** -6, 2 ** -6, -2 ** -5, 2 ** -5):
+            near.append(k + 0.5 + d)
+    rows.append(near[:K] + [0.0] * (K - len(near[:K])))
+    gold = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "quant_rows.json")))["cases"]
+    for c in gold:
+        if c["smooth"] is None:
+            rows.append(c["x"] + [0.0] * (K - len(c["x"])))
+    P = torch.tensor(rows, dtype=torch.bfloat16)
+    chunks = [P[:, r * h:(r + 1) * h].contiguous() for r in range(R)]
+    shape = A2A(rank_size=R, bs_local=P.shape[0], h=h, n=64, quant_mode=7, smooth=False)
+    g = torch.Generator().manual_seed(3)
+    inp = {"chunks": chunks, "x1_scale": None,
+           "x2": torch.randint(-127, 128, (K, 64), generator=g, dtype=torch.int8),
+           "x2_scale": torch.rand(64, generator=g) * 1e-2, "bias": torch.randn(64, generator=g)}
+    got = run_gpu(inp, shape)
+    ref = run_oracle(inp, shape)
+    compare(got, ref, "ties")
+    # the tie row: q = round-half-even of k + 0.5
+    want = [127] + [k if k % 2 == 0 else k + 1 for k in range(-126, 126)]
+    assert got["q"][0, :len(want)].tolist() == want
