@@ -199,7 +199,7 @@ class Step:
         self.run_ag()
         self.run_a2a()
 
-    launches_per_step = 4  # ag: GEMM; a2a (mode 7): quant prologue, x2 widening, GEMM
+    launches_per_step = 3  # ag: GEMM; a2a (mode 7): fused quant + x2-widening prologue, GEMM
 
     @property
     def flops(self):

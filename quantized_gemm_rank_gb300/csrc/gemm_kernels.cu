@@ -20,19 +20,22 @@ cudaError_t launch_one(const GemmParams &p_in, int num_sms, cudaStream_t stream)
     const int num_tiles = ((p.m + Cfg::kTileM - 1) / Cfg::kTileM) * ((p.n + kBN - 1) / kBN);
 
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     cfg.blockDim = dim3(kNumThreads, 1, 1);
     cfg.dynamicSmemBytes = Cfg::kSmemBytes;
     cfg.stream = stream;
+    // the kernel waits for the previous one (griddepcontrol.wait) before touching
+    // global memory, so its set-up may overlap that kernel's tail
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     if constexpr (kG == 2) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
-        if (e != cudaSuccess) return e;
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = 2;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.numAttrs = 2;
         // co-resident pairs on this device (cached per device)
         static int cached[64] = {0};
         int dev = 0;

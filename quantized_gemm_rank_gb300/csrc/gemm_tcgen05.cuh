@@ -219,6 +219,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
     if constexpr (kPair) ptx::cluster_sync();
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // The set-up above may overlap the previous kernel of the stream; nothing in
+    // global memory is touched before it has completed.
+    ptx::grid_dependency_wait();
 
     if (warp == 0 && lane == 0) {
         // ------------------------------------------------------------ TMA producer

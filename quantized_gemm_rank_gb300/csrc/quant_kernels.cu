@@ -12,6 +12,7 @@
 #include <cstdint>
 
 #include "internal.h"
+#include "sm103_ptx.cuh"
 
 namespace mc2 {
 
@@ -59,6 +60,7 @@ __global__ void __launch_bounds__(256) quant_pertoken_kernel(const __grid_consta
                                                              const uint16_t *__restrict__ smooth,
                                                              __half *__restrict__ qh, int8_t *__restrict__ q_out,
                                                              float *__restrict__ scale_out) {
+    ptx::allow_dependent_launch();
     __shared__ float red[32];
     const int K = rank_size * h;
     const bool vec = (h % 8) == 0;
@@ -143,8 +145,10 @@ __global__ void __launch_bounds__(256) quant_pertoken_kernel(const __grid_consta
 //   * quant CTAs (one per permuted row): the row stays in registers (kV 16-byte
 //     vectors per thread, vector v of thread i = permuted columns
 //     (v*blockDim + i)*8 .. +7), so it is read from HBM once;
-//   * widen CTAs (every kWidenEvery-th CTA): a contiguous slice of x2, int8 ->
-//     fp16.
+//   * widen CTAs: a contiguous slice of x2, int8 -> fp16; their number follows
+//     the size of x2 (about four 16-byte vectors per thread), and CTA b is a
+//     widen CTA when floor((b+1)W/G) > floor(bW/G) (W widen CTAs of G), which
+//     spreads the two roles evenly over the grid.
 // The quant role is instruction-bound and the widening memory-bound, which is
 // why they share the launch.
 //
@@ -158,7 +162,6 @@ __global__ void __launch_bounds__(256) quant_pertoken_kernel(const __grid_consta
 // and every exact tie) the IEEE division decides.  qa <= 127 * (1 + 3*2^-24)
 // keeps k inside [-127, 127], and the low byte of fl(qa + M) is k mod 256,
 // i.e. the int8 q.
-constexpr int kWidenEvery = 5;
 constexpr float kRoundMagic = 12582912.0f;  // 1.5 * 2^23
 
 template <bool kBF16>
@@ -179,10 +182,13 @@ __global__ void __launch_bounds__(512) a2a_prologue_kernel(const __grid_constant
                                                            const int8_t *__restrict__ x2,
                                                            __half *__restrict__ x2h, int64_t x2_vecs,
                                                            int64_t widen_ctas) {
+    ptx::allow_dependent_launch();
     const int64_t b = blockIdx.x;
-    if (b % kWidenEvery == kWidenEvery - 1) {
+    const int64_t G = gridDim.x;
+    const int64_t before = b * widen_ctas / G;  // widen CTAs among [0, b)
+    if ((b + 1) * widen_ctas / G > before) {
         // ---- widen role: vectors [w * per, (w + 1) * per) of 16 int8 each
-        const int64_t w = b / kWidenEvery;
+        const int64_t w = before;
         const int64_t per = (x2_vecs + widen_ctas - 1) / widen_ctas;
         const int64_t end = min(x2_vecs, (w + 1) * per);
         for (int64_t i = w * per + threadIdx.x; i < end; i += blockDim.x) {
@@ -199,7 +205,7 @@ __global__ void __launch_bounds__(512) a2a_prologue_kernel(const __grid_constant
         return;
     }
     // ---- quant role: permuted row t
-    const int64_t t = b - b / kWidenEvery;
+    const int64_t t = b - before;
     if (t >= bs_local) return;
     __shared__ float red[32];
     const int K = rank_size * h;
@@ -284,6 +290,7 @@ __global__ void __launch_bounds__(512) a2a_prologue_kernel(const __grid_constant
 // int8 -> fp16, exact, 16 elements per thread-iteration.
 __global__ void __launch_bounds__(256) widen_i8_kernel(const int8_t *__restrict__ src, __half *__restrict__ dst,
                                                        int64_t count) {
+    ptx::allow_dependent_launch();
     const int64_t nvec = count / 16;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < nvec; i += stride) {
@@ -305,6 +312,7 @@ __global__ void __launch_bounds__(256) widen_i8_kernel(const int8_t *__restrict_
 __global__ void __launch_bounds__(256) permute_widen_i8_kernel(const __grid_constant__ ChunkPtrs chunks, int h, int64_t bs_local,
                                                                int rank_size, __half *__restrict__ dst,
                                                                int8_t *__restrict__ q_out) {
+    ptx::allow_dependent_launch();
     const int K = rank_size * h;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     if (h % 16 == 0) {
@@ -376,17 +384,19 @@ cudaError_t launch_a2a_prologue(const ChunkPtrs &chunks, int rank_size, int64_t 
     const int K = rank_size * h;
     int threads = 64;
     while (threads * kV * 8 < K) threads *= 2;
-    // kWidenEvery - 1 quant CTAs for every widen CTA
-    const int64_t groups = (bs_local + kWidenEvery - 2) / (kWidenEvery - 1);
-    const int64_t grid = groups * kWidenEvery;
-    const int64_t widen_ctas = groups;
+    // one quant CTA per row; widen CTAs for ~4 vectors per thread
+    const int64_t x2_vecs = x2_count / 16;
+    int64_t widen_ctas = (x2_vecs + 4ll * threads - 1) / (4ll * threads);
+    if (widen_ctas < 1) widen_ctas = 1;
+    if (widen_ctas > (1ll << 30)) widen_ctas = 1ll << 30;
+    const int64_t grid = bs_local + widen_ctas;
     const uint16_t *sm = static_cast<const uint16_t *>(smooth);
     if (bf16)
         a2a_prologue_kernel<true, kV><<<static_cast<unsigned>(grid), threads, 0, stream>>>(
-            chunks, h, bs_local, rank_size, sm, qh, q_out, scale_out, x2, x2h, x2_count / 16, widen_ctas);
+            chunks, h, bs_local, rank_size, sm, qh, q_out, scale_out, x2, x2h, x2_vecs, widen_ctas);
     else
         a2a_prologue_kernel<false, kV><<<static_cast<unsigned>(grid), threads, 0, stream>>>(
-            chunks, h, bs_local, rank_size, sm, qh, q_out, scale_out, x2, x2h, x2_count / 16, widen_ctas);
+            chunks, h, bs_local, rank_size, sm, qh, q_out, scale_out, x2, x2h, x2_vecs, widen_ctas);
     return cudaGetLastError();
 }
 
