@@ -162,13 +162,14 @@ class ClockSampler:
 class Step:
     """Device-resident inputs and outputs for one step of the hot path."""
 
-    def __init__(self, dev, ag_shape, a2a_shape, seed=0):
+    def __init__(self, dev, ag_shape, a2a_shape, seed=0, host=None):
         import quantized_gemm_rank_gb300 as mc2
         self.mc2 = mc2
         self.ag_s, self.a2a_s = ag_shape, a2a_shape
-        ag = mc2_inputs.ag_inputs(ag_shape, seed=seed)
-        a2 = mc2_inputs.a2a_inputs(a2a_shape, seed=seed)
-        self.host = {"ag": ag, "a2a": a2}
+        if host is None:
+            host = {"ag": mc2_inputs.ag_inputs(ag_shape, seed=seed), "a2a": mc2_inputs.a2a_inputs(a2a_shape, seed=seed)}
+        ag, a2 = host["ag"], host["a2a"]
+        self.host = host
         self.ag_chunks = [c.to(dev) for c in ag["chunks"]]
         self.ag_x2 = ag["x2"].to(dev)
         self.ag_bias = None if ag["bias"] is None else ag["bias"].to(dev)
@@ -225,41 +226,64 @@ def time_device(fn, steps, warmup, flush, stream):
 
 
 def time_e2e(step: Step, steps, warmup, dev):
-    """Same step through the public calls with HOST inputs: pinned host -> device
-    copies of every input, both calls, device -> host copies of every output."""
+    """Same step through the public calls with HOST buffers: every step copies all
+    of its inputs from pinned host memory to the device and all of its outputs
+    back.  Two device buffer sets and three streams (upload, compute, download)
+    ordered by events let step i+1's upload and step i-1's download run while
+    step i computes, as a caller streaming batches would."""
     ag, a2 = step.host["ag"], step.host["a2a"]
     h_in = [c.pin_memory() for c in ag["chunks"]] + [ag["x2"].pin_memory()] + \
            [c.pin_memory() for c in a2["chunks"]] + [a2["x2"].pin_memory(), a2["x2_scale"].pin_memory(),
                                                      a2["bias"].pin_memory()]
     if a2["x1_scale"] is not None:
         h_in.append(a2["x1_scale"].pin_memory())
-    d_in = step.ag_chunks + [step.ag_x2] + step.a_chunks + [step.a_x2, step.a_x2s, step.a_bias]
-    if step.a_x1s is not None:
-        d_in.append(step.a_x1s)
-    d_out = [step.ag_out] + ([step.ag_gathered] if step.ag_gathered is not None else []) + [step.a_out]
-    h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in d_out]
+    sets = [step, Step(dev, step.ag_s, step.a2a_s, host=step.host)]
+
+    def dev_in(st):
+        d = st.ag_chunks + [st.ag_x2] + st.a_chunks + [st.a_x2, st.a_x2s, st.a_bias]
+        return d + ([st.a_x1s] if st.a_x1s is not None else [])
+
+    def dev_out(st):
+        return [st.ag_out] + ([st.ag_gathered] if st.ag_gathered is not None else []) + [st.a_out]
+
+    h_out = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in dev_out(st)] for st in sets]
     h2d = sum(t.numel() * t.element_size() for t in h_in)
-    d2h = sum(t.numel() * t.element_size() for t in h_out)
+    d2h = sum(t.numel() * t.element_size() for t in h_out[0])
+    up, comp, down = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    ev = [{k: torch.cuda.Event() for k in ("up", "comp", "down")} for _ in sets]
 
-    def one():
-        for d, h in zip(d_in, h_in):
-            d.copy_(h, non_blocking=True)
-        step.run()
-        for h, d in zip(h_out, d_out):
-            h.copy_(d, non_blocking=True)
+    def one(i):
+        b = i % 2
+        st, e = sets[b], ev[b]
+        up.wait_event(e["comp"])           # step i-2 has finished reading this set's inputs
+        with torch.cuda.stream(up):
+            for d, h in zip(dev_in(st), h_in):
+                d.copy_(h, non_blocking=True)
+        e["up"].record(up)
+        comp.wait_event(e["up"])
+        comp.wait_event(e["down"])         # step i-2's outputs of this set are on the host
+        with torch.cuda.stream(comp):
+            st.run()
+        e["comp"].record(comp)
+        down.wait_event(e["comp"])
+        with torch.cuda.stream(down):
+            for h, d in zip(h_out[b], dev_out(st)):
+                h.copy_(d, non_blocking=True)
+        e["down"].record(down)
 
-    stream = torch.cuda.current_stream()
-    for _ in range(warmup):
-        one()
+    for i in range(warmup):
+        one(i)
     torch.cuda.synchronize()
-    a = torch.cuda.Event(enable_timing=True)
-    b = torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(steps):
-        one()
-    b.record(stream)
-    b.synchronize()
-    return a.elapsed_time(b) / steps, h2d, d2h
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(up)
+    for i in range(steps):
+        one(i)
+    for s_ in (comp, down):
+        up.wait_stream(s_)
+    t1.record(up)
+    t1.synchronize()
+    return t0.elapsed_time(t1) / steps, h2d, d2h
 
 
 # ----------------------------------------------------------------------------- CPU oracle

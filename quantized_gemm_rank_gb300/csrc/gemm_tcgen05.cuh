@@ -241,6 +241,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
             // first A box of this tile: chunk and row inside it (rows past m stay in the
             // last chunk, out of its range, and read as zeros)
             int a_chunk0 = 0, a_row0 = m0, a_nbox = 1;
+            int kc = 0, kl = 0;  // A_KINTERLEAVE: chunk and column inside it of the current k-tile
             if (p.a_mode == A_MCONCAT) {
                 a_chunk0 = m0 / p.m_local;
                 a_row0 = m0 - a_chunk0 * p.m_local;
@@ -280,8 +281,10 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
                         if (li >= p.m_local && c < p.num_a_maps - 1) li -= p.m_local, ++c;
                     }
                 } else if (p.a_mode == A_KINTERLEAVE) {
-                    const int c = k0 / p.k_local;
-                    load(sA, &p.a_maps[c], k0 - c * p.k_local, m0, a_bar);
+                    // permuted column k0 = kc * k_local + kl lives in chunk kc (k_local % kBK == 0)
+                    load(sA, &p.a_maps[kc], kl, m0, a_bar);
+                    kl += kBK;
+                    if (kl >= p.k_local) kl = 0, ++kc;
                 } else {
                     load(sA, &p.a_maps[0], k0, m0, a_bar);
                 }

@@ -36,6 +36,10 @@ cudaError_t launch_a2a_prologue(const ChunkPtrs &chunks, int rank_size, int64_t 
                                 const void *smooth, __half *qh, int8_t *q_out, float *scale_out, const int8_t *x2,
                                 __half *x2h, int64_t x2_count, cudaStream_t stream);
 cudaError_t launch_widen_i8(const int8_t *src, __half *dst, int64_t count, int num_sms, cudaStream_t stream);
+// Widens each rank's int8 chunk to fp16 in its own layout at dst + r*bs_local*h
+// (h % 16 == 0); q_out (optional) receives the permuted int8 matrix.
+cudaError_t launch_widen_chunks_i8(const ChunkPtrs &chunks, int rank_size, int64_t bs_local, int h, __half *dst,
+                                   int8_t *q_out, int num_sms, cudaStream_t stream);
 cudaError_t launch_permute_widen_i8(const ChunkPtrs &chunks, int rank_size, int64_t bs_local, int h, __half *dst,
                                     int8_t *q_out, int num_sms, cudaStream_t stream);
 

@@ -290,6 +290,10 @@ int mc2_alltoall_quant_mm(const void *const *chunks, int rank_size, int64_t bs_l
     memset(&cp, 0, sizeof(cp));
     for (int r = 0; r < rank_size; ++r) cp.p[r] = chunks[r];
 
+    // Mode 3 with h % 64 == 0: each chunk is widened in place of its own and the
+    // GEMM reads the permuted matrix through one tensor map per chunk (a k-tile
+    // never straddles two chunks); otherwise the widening writes it permuted.
+    const bool a_by_chunk = x1_quant_mode == MC2_QUANT_PERTOKEN && h % mc2::kBK == 0;
     cudaError_t e;
     bool x2_done = false;
     if (x1_quant_mode == MC2_QUANT_PERTOKEN_DYNAMIC && mc2::a2a_prologue_fits(rank_size, bs_local, static_cast<int>(h))) {
@@ -300,7 +304,11 @@ int mc2_alltoall_quant_mm(const void *const *chunks, int rank_size, int64_t bs_l
         e = mc2::launch_quant_pertoken(cp, rank_size, bs_local, static_cast<int>(h), x1_dtype == MC2_BF16, x1_scale,
                                        ah, q_out, scale, dev.num_sms, s);
     } else {
-        e = mc2::launch_permute_widen_i8(cp, rank_size, bs_local, static_cast<int>(h), ah, q_out, dev.num_sms, s);
+        // mode 3: the scales are the caller's; the int8 chunks are widened
+        if (a_by_chunk)
+            e = mc2::launch_widen_chunks_i8(cp, rank_size, bs_local, static_cast<int>(h), ah, q_out, dev.num_sms, s);
+        else
+            e = mc2::launch_permute_widen_i8(cp, rank_size, bs_local, static_cast<int>(h), ah, q_out, dev.num_sms, s);
         if (e == cudaSuccess && x1_scale_out)
             e = cudaMemcpyAsync(x1_scale_out, x1_scale, static_cast<size_t>(bs_local) * 4, cudaMemcpyDeviceToDevice, s);
         scale = const_cast<float *>(static_cast<const float *>(x1_scale));
@@ -311,12 +319,18 @@ int mc2_alltoall_quant_mm(const void *const *chunks, int rank_size, int64_t bs_l
 
     mc2::GemmParams p;
     memset(&p, 0, sizeof(p));
-    if (!make_map16(&p.a_maps[0], ah, K, bs_local, mc2::kBK, mc2::kBM))
+    if (a_by_chunk) {
+        for (int r = 0; r < rank_size; ++r)
+            if (!make_map16(&p.a_maps[r], ah + static_cast<size_t>(r) * bs_local * h, h, bs_local, mc2::kBK, mc2::kBM))
+                return fail(MC2_ERR_CUDA, "cuTensorMapEncodeTiled failed for widened chunk %d", r);
+    } else if (!make_map16(&p.a_maps[0], ah, K, bs_local, mc2::kBK, mc2::kBM)) {
         return fail(MC2_ERR_CUDA, "cuTensorMapEncodeTiled failed for the quantised activations");
+    }
     if (!make_map16(&p.b_map, x2h, n, K, 64, mc2::kBK))
         return fail(MC2_ERR_CUDA, "cuTensorMapEncodeTiled failed for x2");
-    p.num_a_maps = 1;
-    p.a_mode = mc2::A_SINGLE;
+    p.num_a_maps = a_by_chunk ? rank_size : 1;
+    p.a_mode = a_by_chunk ? mc2::A_KINTERLEAVE : mc2::A_SINGLE;
+    p.k_local = static_cast<int>(h);
     p.b_mn_major = 1;
     p.m = static_cast<int>(bs_local);
     p.n = static_cast<int>(n);

@@ -307,6 +307,39 @@ __global__ void __launch_bounds__(256) widen_i8_kernel(const int8_t *__restrict_
         dst[i] = __int2half_rn(src[i]);
 }
 
+// Each rank's int8 chunk -> fp16 in its own layout (dst + r * bs_local * h), so
+// the GEMM reads the permuted matrix through per-chunk tensor maps instead of
+// a materialised permuted copy; q_out (optional) gets the permuted int8 matrix.
+// h % 16 == 0.
+__global__ void __launch_bounds__(256) widen_chunks_i8_kernel(const __grid_constant__ ChunkPtrs chunks, int h,
+                                                              int64_t bs_local, int rank_size,
+                                                              __half *__restrict__ dst, int8_t *__restrict__ q_out) {
+    ptx::allow_dependent_launch();
+    const int64_t per_chunk = bs_local * h / 16;  // 16-element vectors per chunk
+    const int64_t total = per_chunk * rank_size;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    const int vpr = h / 16;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += stride) {
+        const int r = static_cast<int>(i / per_chunk);
+        const int64_t li = i - r * per_chunk;
+        const int4 v = __ldg(reinterpret_cast<const int4 *>(chunks.p[r]) + li);
+        const int8_t *e = reinterpret_cast<const int8_t *>(&v);
+        uint4 o[2];
+        __half2 *oh = reinterpret_cast<__half2 *>(o);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            oh[j] = __floats2half2_rn(static_cast<float>(e[2 * j]), static_cast<float>(e[2 * j + 1]));
+        uint4 *d = reinterpret_cast<uint4 *>(dst) + 2 * i;
+        d[0] = o[0];
+        d[1] = o[1];
+        if (q_out) {
+            const int64_t t = li / vpr;
+            const int j = static_cast<int>(li - t * vpr) * 16;
+            *reinterpret_cast<int4 *>(q_out + t * (static_cast<int64_t>(rank_size) * h) + r * h + j) = v;
+        }
+    }
+}
+
 // Permuted int8 chunks -> fp16 GEMM operand (and optionally the int8
 // permuted matrix): dst[t, r*h + j] = chunk_r[t, j].
 __global__ void __launch_bounds__(256) permute_widen_i8_kernel(const __grid_constant__ ChunkPtrs chunks, int h, int64_t bs_local,
@@ -402,6 +435,14 @@ cudaError_t launch_a2a_prologue(const ChunkPtrs &chunks, int rank_size, int64_t 
 
 cudaError_t launch_widen_i8(const int8_t *src, __half *dst, int64_t count, int num_sms, cudaStream_t stream) {
     widen_i8_kernel<<<grid_for(count / 16 + 1, 256, num_sms), 256, 0, stream>>>(src, dst, count);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_widen_chunks_i8(const ChunkPtrs &chunks, int rank_size, int64_t bs_local, int h, __half *dst,
+                                   int8_t *q_out, int num_sms, cudaStream_t stream) {
+    const int64_t items = bs_local * static_cast<int64_t>(rank_size) * h / 16;
+    widen_chunks_i8_kernel<<<grid_for(items, 256, num_sms), 256, 0, stream>>>(chunks, h, bs_local, rank_size, dst,
+                                                                             q_out);
     return cudaGetLastError();
 }
 
