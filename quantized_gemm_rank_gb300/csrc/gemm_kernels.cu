@@ -8,6 +8,36 @@ __device__ int g_gemm_status = 0;
 
 namespace {
 
+// CTA pairs of this instantiation that fit on the device at once, from the
+// occupancy calculator (cached per device).
+template <bool kBF16, bool kIntPath>
+int concurrent_pairs(int num_sms) {
+    using Cfg = TileCfg<2>;
+    static int cached[64] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    int clusters = dev < 64 ? cached[dev] : 0;
+    if (clusters == 0) {
+        auto kern = mc2_gemm_kernel<2, kBF16, kIntPath>;
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        cfg.blockDim = dim3(kNumThreads, 1, 1);
+        cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+        cfg.gridDim = dim3(2 * (num_sms / 2), 1, 1);
+        if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess || clusters < 1)
+            clusters = num_sms / 2;
+        if (dev < 64) cached[dev] = clusters;
+    }
+    return clusters;
+}
+
 template <int kG, bool kBF16, bool kIntPath>
 cudaError_t launch_one(const GemmParams &p_in, int num_sms, cudaStream_t stream) {
     using Cfg = TileCfg<kG>;
@@ -36,21 +66,13 @@ cudaError_t launch_one(const GemmParams &p_in, int num_sms, cudaStream_t stream)
         attr[1].val.clusterDim.y = 1;
         attr[1].val.clusterDim.z = 1;
         cfg.numAttrs = 2;
-        // co-resident pairs on this device (cached per device)
-        static int cached[64] = {0};
-        int dev = 0;
-        cudaGetDevice(&dev);
-        int clusters = dev < 64 ? cached[dev] : 0;
-        if (clusters == 0) {
-            cfg.gridDim = dim3(2 * (num_sms / 2), 1, 1);
-            e = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
-            if (e != cudaSuccess || clusters < 1) clusters = num_sms / 2;
-            if (dev < 64) cached[dev] = clusters;
-        }
-        const int grid_clusters = num_tiles < clusters ? num_tiles : clusters;
+        const int clusters = concurrent_pairs<kBF16, kIntPath>(num_sms);
+        // with a stream-K tail every co-resident pair takes part
+        const int grid_clusters = (p.sk_tiles > 0 || num_tiles >= clusters) ? clusters : num_tiles;
         cfg.gridDim = dim3(2 * grid_clusters, 1, 1);
     } else {
-        cfg.gridDim = dim3(num_tiles < num_sms ? num_tiles : num_sms, 1, 1);
+        const int units = p.sk_tiles > 0 ? num_sms : (num_tiles < num_sms ? num_tiles : num_sms);
+        cfg.gridDim = dim3(units, 1, 1);
     }
     e = cudaLaunchKernelEx(&cfg, kern, p);
     if (e != cudaSuccess) return e;
@@ -60,6 +82,15 @@ cudaError_t launch_one(const GemmParams &p_in, int num_sms, cudaStream_t stream)
 }  // namespace
 
 int gemm_group_for(int m) { return m > kBM ? 2 : 1; }
+
+int gemm_units(GemmKind kind, int group, int num_sms) {
+    if (group == 1) return num_sms;
+    switch (kind) {
+        case GEMM_F16: return concurrent_pairs<false, false>(num_sms);
+        case GEMM_BF16: return concurrent_pairs<true, false>(num_sms);
+        default: return concurrent_pairs<false, true>(num_sms);
+    }
+}
 
 cudaError_t launch_gemm(GemmKind kind, int group, const GemmParams &p, int num_sms, cudaStream_t stream) {
     if (group == 2) {

@@ -92,8 +92,87 @@ struct GemmParams {
     const void *bias_q;             // integer path: (n) fp32 or bf16, or null
     int bias_q_bf16;
     int32_t *acc_out;               // integer path: optional (m, n)
+    int sk_tiles;                   // integer path: tiles of the stream-K tail (0: all data-parallel)
+    int32_t *sk_partials;           // stream-K partial sums: slot (unit * 2 + cta) of 128 x 256 int32
+    int *sk_flags;                  // stream-K: partial parts written, per (tile, cta); zero at launch
     int *status;                    // device word set to -7 when a bounded wait gives up
     uint64_t wait_limit_ns;
+};
+
+// ---------------------------------------------------------------------------
+// Work schedule of one cluster (identical in every role of every CTA of it).
+// Tiles [0, num_tiles - sk_tiles) are data-parallel: cluster c takes tiles
+// c, c + U, ... whole.  The K blocks of the last sk_tiles tiles are laid end to
+// end and cut into U equal ranges, one per cluster; a range shorter than a
+// tile covers at most two parts: the end of one tile and the start of the next.
+// A part that does not end at its tile's end is a WRITE part (its int32 sums
+// go to the cluster's partial slot); a part that ends there but starts inside
+// the tile is a FINISH part (it adds the WRITE parts of the earlier clusters);
+// WRITE parts are scheduled first, so a FINISH part never waits on a cluster
+// that is itself waiting.
+enum WorkKind : int { WORK_FULL = 0, WORK_WRITE = 1, WORK_FINISH = 2 };
+
+struct Work {
+    int tile, kb0, kb1, kind;
+};
+
+struct Schedule {
+    int c, U, nkb, dp_tiles, n_dp, n_sk;
+    long long total;  // K blocks in the stream-K region
+    Work sk[2];
+
+    __device__ __forceinline__ long long range_start(int u) const { return static_cast<long long>(u) * total / U; }
+
+    __device__ __forceinline__ void init(int cluster, int units, int num_tiles, int sk_tiles, int nkb_) {
+        c = cluster;
+        U = units;
+        nkb = nkb_;
+        dp_tiles = num_tiles - sk_tiles;
+        n_dp = c < dp_tiles ? (dp_tiles - c + U - 1) / U : 0;
+        total = static_cast<long long>(sk_tiles) * nkb;
+        n_sk = 0;
+        if (sk_tiles == 0) return;
+        const long long s0 = range_start(c), e0 = range_start(c + 1);
+        if (s0 == e0) return;
+        const int t0 = static_cast<int>(s0 / nkb);
+        const int kb0 = static_cast<int>(s0 - static_cast<long long>(t0) * nkb);
+        const int kb1 = static_cast<int>(min(static_cast<long long>(nkb), kb0 + (e0 - s0)));
+        Work a{dp_tiles + t0, kb0, kb1, kb1 < nkb ? WORK_WRITE : (kb0 > 0 ? WORK_FINISH : WORK_FULL)};
+        if (e0 > static_cast<long long>(t0 + 1) * nkb) {
+            // the range continues into the next tile: that start part is a WRITE part, done first
+            Work b{dp_tiles + t0 + 1, 0, static_cast<int>(e0 - static_cast<long long>(t0 + 1) * nkb), WORK_WRITE};
+            sk[0] = b;
+            sk[1] = a;
+            n_sk = 2;
+        } else {
+            sk[0] = a;
+            n_sk = 1;
+        }
+    }
+
+    __device__ __forceinline__ int count() const { return n_dp + n_sk; }
+
+    __device__ __forceinline__ Work get(int i) const {
+        if (i < n_dp) return Work{c + i * U, 0, nkb, WORK_FULL};
+        return sk[i - n_dp];
+    }
+
+    // Clusters u < c whose non-empty range reaches into `tile` (the WRITE parts a
+    // FINISH part of that tile adds), visited in descending u.
+    template <class F>
+    __device__ __forceinline__ int for_each_writer(int tile, F f) const {
+        const long long g0 = static_cast<long long>(tile - dp_tiles) * nkb;
+        int n = 0;
+        for (int u = c - 1; u >= 0; --u) {
+            const long long su = range_start(u), eu = range_start(u + 1);
+            if (eu <= g0) break;
+            if (su < eu) {
+                f(u);
+                ++n;
+            }
+        }
+        return n;
+    }
 };
 
 __device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int &mb, int &nb) {
@@ -196,6 +275,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
     const int num_k = (p.k + kBK - 1) / kBK;
     const int cluster_id = blockIdx.x / kG;
     const int num_clusters = gridDim.x / kG;
+    const int nkb = (num_k + p.kblock_tiles - 1) / p.kblock_tiles;  // K blocks per tile
+    Schedule sched;
+    sched.init(cluster_id, num_clusters, num_tiles, p.sk_tiles, nkb);
 
     if (threadIdx.x == 0) {
         abort_flag_s = 0;
@@ -233,15 +315,21 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
         uint32_t phase = 0;
         int iters = 0;
         bool ok = true;
-        for (int tile = cluster_id; tile < num_tiles && ok; tile += num_clusters) {
+        for (int wi = 0; wi < sched.count() && ok; ++wi) {
+            const Work w = sched.get(wi);
+            const int kt_begin = w.kb0 * p.kblock_tiles, kt_end = min(num_k, w.kb1 * p.kblock_tiles);
             int mb, nb;
-            tile_coords(tile, num_m, num_n, mb, nb);
+            tile_coords(w.tile, num_m, num_n, mb, nb);
             const int m0 = mb * Cfg::kTileM + kBM * static_cast<int>(cr);
             const int n0 = nb * kBN + Cfg::kBRows * static_cast<int>(cr);
             // first A box of this tile: chunk and row inside it (rows past m stay in the
             // last chunk, out of its range, and read as zeros)
             int a_chunk0 = 0, a_row0 = m0, a_nbox = 1;
             int kc = 0, kl = 0;  // A_KINTERLEAVE: chunk and column inside it of the current k-tile
+            if (p.a_mode == A_KINTERLEAVE) {
+                kc = kt_begin * kBK / p.k_local;
+                kl = kt_begin * kBK - kc * p.k_local;
+            }
             if (p.a_mode == A_MCONCAT) {
                 a_chunk0 = m0 / p.m_local;
                 a_row0 = m0 - a_chunk0 * p.m_local;
@@ -251,7 +339,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
                 }
                 a_nbox = kBM / p.a_box_rows;
             }
-            for (int kt = 0; kt < num_k; ++kt) {
+            for (int kt = kt_begin; kt < kt_end; ++kt) {
                 if (!wait_or_abort<kPair>(ptx::smem_u32(&empty_bar[stage]), phase ^ 1u, p, abort_flag)) {
                     ok = false;
                     break;
@@ -329,13 +417,15 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
         bool ok = true;
         uint32_t d_tmem = tmem_base;
         const uint32_t consumed0 = ptx::smem_u32(&consumed_bar[0]);
-        for (int tile = cluster_id; tile < num_tiles && ok; tile += num_clusters) {
+        for (int wi = 0; wi < sched.count() && ok; ++wi) {
+            const Work w = sched.get(wi);
+            const int kt_begin = w.kb0 * kblock, kt_end = min(num_k, w.kb1 * kblock);
             int mb, nb;
-            tile_coords(tile, num_m, num_n, mb, nb);
+            tile_coords(w.tile, num_m, num_n, mb, nb);
             // stages of gathered tiles go to the gathered-store warp before being freed
             const uint32_t release0 = (p.gather && nb == 0) ? consumed0 : empty0;
             int kin = 0;  // k-tile index inside the current K block
-            for (int kt = 0; kt < num_k; ++kt) {
+            for (int kt = kt_begin; kt < kt_end; ++kt) {
                 if (kin == 0) {
                     const uint32_t b = acc_iter & 1u;
                     if (!wait_or_abort<kPair>(ptx::smem_u32(&tempty_bar[b]), ((acc_iter >> 1) & 1u) ^ 1u, p,
@@ -365,7 +455,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
                 } else {
                     stage_off += kStageStep;
                 }
-                if (++kin == kblock || kt == num_k - 1) {
+                if (++kin == kblock || kt == kt_end - 1) {
                     ptx::mma_commit<kG>(ptx::smem_u32(&tfull_bar[acc_iter & 1u]));
                     ++acc_iter;
                     kin = 0;
@@ -379,15 +469,17 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
         uint32_t consumed_parity = 0;  // bit s: parity of the next consumed_bar[s] phase
         int pending_stage = -1;        // stage whose store may still be reading shared memory
         bool ok = true;
-        for (int tile = cluster_id; tile < num_tiles && ok; tile += num_clusters) {
+        for (int wi = 0; wi < sched.count() && ok; ++wi) {
+            const Work w = sched.get(wi);
+            const int kt_begin = w.kb0 * p.kblock_tiles, kt_end = min(num_k, w.kb1 * p.kblock_tiles);
             int mb, nb;
-            tile_coords(tile, num_m, num_n, mb, nb);
+            tile_coords(w.tile, num_m, num_n, mb, nb);
             if (nb != 0) {  // not a gathered tile: its stages are freed by the MMA directly
-                stage = (stage + num_k) % S;
+                stage = (stage + (kt_end - kt_begin)) % S;
                 continue;
             }
             const int m0 = mb * Cfg::kTileM + kBM * static_cast<int>(cr);
-            for (int kt = 0; kt < num_k; ++kt) {
+            for (int kt = kt_begin; kt < kt_end; ++kt) {
                 if (!wait_or_abort<kPair>(ptx::smem_u32(&consumed_bar[stage]), (consumed_parity >> stage) & 1u, p,
                                           abort_flag)) {
                     ok = false;
@@ -413,9 +505,10 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
         const int half = (warp - 4) >> 2;     // which 128 of the 256 columns
         const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
         uint32_t acc_iter = 0;
-        for (int tile = cluster_id; tile < num_tiles; tile += num_clusters) {
+        for (int wi = 0; wi < sched.count(); ++wi) {
+            const Work w = sched.get(wi);
             int mb, nb;
-            tile_coords(tile, num_m, num_n, mb, nb);
+            tile_coords(w.tile, num_m, num_n, mb, nb);
             const int row = mb * Cfg::kTileM + kBM * static_cast<int>(cr) + 32 * q + lane;
             const int colh = nb * kBN + half * 128;
             bool ok = true;
@@ -425,8 +518,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
             acc_t sum[128];
 #pragma unroll
             for (int i = 0; i < 128; ++i) sum[i] = acc_t(0);
-            const int nkb = (num_k + p.kblock_tiles - 1) / p.kblock_tiles;
-            for (int kb = 0; kb < nkb; ++kb) {
+            for (int kb = w.kb0; kb < w.kb1; ++kb) {
                 const uint32_t b = acc_iter & 1u;
                 if (!wait_or_abort<kPair>(ptx::smem_u32(&tfull_bar[b]), (acc_iter >> 1) & 1u, p, abort_flag)) {
                     ok = false;
@@ -459,6 +551,53 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
                 ++acc_iter;
             }
             if (!ok) break;
+            if constexpr (kIntPath) {
+                // stream-K: this thread's 128 sums of row (32q + lane) in slot (unit, cta)
+                const int r_in = 32 * q + lane;
+                if (w.kind == WORK_WRITE) {
+                    int32_t *slot = p.sk_partials + (static_cast<size_t>(cluster_id * 2 + cr) * kBM + r_in) * kBN +
+                                    half * 128;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        __stcg(reinterpret_cast<int4 *>(slot) + j,
+                               make_int4(sum[4 * j], sum[4 * j + 1], sum[4 * j + 2], sum[4 * j + 3]));
+                    __threadfence();
+                    __syncwarp();
+                    if (lane == 0) atomicAdd(&p.sk_flags[w.tile * 2 + cr], 1);
+                    continue;
+                }
+                if (w.kind == WORK_FINISH) {
+                    // wait until every epilogue warp of every earlier part has published
+                    const int need = kNumEpiWarps * sched.for_each_writer(w.tile, [](int) {});
+                    volatile int *flag = p.sk_flags + w.tile * 2 + cr;
+                    if (*flag < need) {
+                        const uint64_t start = ptx::globaltimer_ns();
+                        while (*flag < need) {
+                            if (*abort_flag || ptx::globaltimer_ns() - start > p.wait_limit_ns) {
+                                *abort_flag = 1;
+                                if (p.status) atomicExch(p.status, -7);
+                                ok = false;
+                                break;
+                            }
+                            ptx::nanosleep(64);
+                        }
+                    }
+                    if (!ok) break;
+                    __threadfence();
+                    sched.for_each_writer(w.tile, [&](int u) {
+                        const int32_t *slot = p.sk_partials + (static_cast<size_t>(u * 2 + cr) * kBM + r_in) * kBN +
+                                              half * 128;
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            const int4 v = __ldcg(reinterpret_cast<const int4 *>(slot) + j);
+                            sum[4 * j] += v.x;
+                            sum[4 * j + 1] += v.y;
+                            sum[4 * j + 2] += v.z;
+                            sum[4 * j + 3] += v.w;
+                        }
+                    });
+                }
+            }
             if (row >= p.m) continue;
             if constexpr (!kIntPath) {
 #pragma unroll

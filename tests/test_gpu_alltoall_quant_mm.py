@@ -171,3 +171,28 @@ def test_quant_ties_and_near_ties_on_gpu():
     # the tie row: q = round-half-even of k + 0.5
     want = [127] + [k if k % 2 == 0 else k + 1 for k in range(-126, 126)]
     assert got["q"][0, :len(want)].tolist() == want
+
+
+@pytest.mark.parametrize("n,mode", [(2560, 3), (4352, 7), (4352, 3)])
+def test_stream_k_tail_exact(n, mode):
+    """Shapes whose tile count is not a multiple of the co-resident CTA pairs,
+    so the leftover tiles are split by K blocks across pairs (stream-K) and
+    their int32 partial sums combined: every output element bit for bit."""
+    shape = A2A(rank_size=8, bs_local=2048, h=512, n=n, quant_mode=mode)   # 8 x (n/256) tiles, 4 K blocks each
+    inp = mc2_inputs.a2a_inputs(shape, seed=31)
+    got = run_gpu(inp, shape)
+    ref = run_oracle(inp, shape)
+    compare(got, ref, f"stream-K n={n} mode={mode}")
+
+
+def test_stream_k_all_127_bound():
+    """All-127 operands through the stream-K tail: exact int32 partials at the
+    accumulator bound (8192 * 16129 = 132128768)."""
+    shape = A2A(rank_size=8, bs_local=2048, h=1024, n=2560, quant_mode=3)
+    inp = mc2_inputs.a2a_inputs(shape, seed=2)
+    inp["chunks"] = [torch.full_like(c, -127) for c in inp["chunks"]]
+    inp["x2"] = torch.full_like(inp["x2"], 127)
+    got = run_gpu(inp, shape)
+    assert torch.all(got["acc"] == -8192 * 16129)
+    ref = run_oracle(inp, shape, rows=[0, 1, 1023, 2047])
+    compare(got, ref, "stream-K all-127", rows=[0, 1, 1023, 2047])
