@@ -167,8 +167,8 @@ def mc2_alltoall_quant_mm(chunks: Sequence[torch.Tensor], x2: torch.Tensor, x2_s
     x1_dtype = chunks[0].dtype
     if out is None:
         out = torch.empty((bs_local, n), dtype=torch.bfloat16, device=dev)
-    need = mc2_alltoall_quant_mm_workspace(R, bs_local, h, n, x1_quant_mode, x1_dtype)
     if workspace is None:
+        need = mc2_alltoall_quant_mm_workspace(R, bs_local, h, n, x1_quant_mode, x1_dtype)
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     ptrs = _ptrs(chunks, "chunks")
     st = lib().mc2_alltoall_quant_mm(ptrs, R, bs_local, h, _dtype_code(x1_dtype), _opt(x1_scale, "x1_scale"),

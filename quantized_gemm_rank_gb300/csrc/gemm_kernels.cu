@@ -43,10 +43,20 @@ cudaError_t launch_one(const GemmParams &p_in, int num_sms, cudaStream_t stream)
     using Cfg = TileCfg<kG>;
     auto kern = mc2_gemm_kernel<kG, kBF16, kIntPath>;
     GemmParams p = p_in;
-    cudaError_t e = cudaGetSymbolAddress(reinterpret_cast<void **>(&p.status), g_gemm_status);
+    // per device, once: the status word's address and the shared-memory opt-in
+    static int *status_addr[64] = {nullptr};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
-    if (e != cudaSuccess) return e;
+    if (dev >= 64 || status_addr[dev] == nullptr) {
+        e = cudaGetSymbolAddress(reinterpret_cast<void **>(&p.status), g_gemm_status);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        if (dev < 64) status_addr[dev] = p.status;
+    } else {
+        p.status = status_addr[dev];
+    }
     const int num_tiles = ((p.m + Cfg::kTileM - 1) / Cfg::kTileM) * ((p.n + kBN - 1) / kBN);
 
     cudaLaunchConfig_t cfg = {};

@@ -315,14 +315,14 @@ int mc2_alltoall_quant_mm(const void *const *chunks, int rank_size, int64_t bs_l
     const int units = mc2::gemm_units(mc2::GEMM_INT_AS_F16, group, dev.num_sms);
     int sk_tiles = 0;
     if (ws.nkb >= 2 && units <= ws.sk_slots && ws.num_tiles % units != 0) sk_tiles = ws.num_tiles % units;
+    // the stream-K counters are zeroed by the kernel that runs just before the GEMM
     int *sk_flags = reinterpret_cast<int *>(wsb + ws.sk_flags);
+    const int n_flags = sk_tiles > 0 ? ws.num_tiles * 2 : 0;
     cudaError_t e = cudaSuccess;
-    if (sk_tiles > 0) e = cudaMemsetAsync(sk_flags, 0, static_cast<size_t>(ws.num_tiles) * 2 * sizeof(int), s);
-    if (e != cudaSuccess) return fail(MC2_ERR_CUDA, "clearing the stream-K counters: %s", cudaGetErrorString(e));
     bool x2_done = false;
     if (x1_quant_mode == MC2_QUANT_PERTOKEN_DYNAMIC && mc2::a2a_prologue_fits(rank_size, bs_local, static_cast<int>(h))) {
         e = mc2::launch_a2a_prologue(cp, rank_size, bs_local, static_cast<int>(h), x1_dtype == MC2_BF16, x1_scale, ah,
-                                     q_out, scale, x2, x2h, K * n, s);
+                                     q_out, scale, x2, x2h, K * n, sk_flags, n_flags, s);
         x2_done = true;
     } else if (x1_quant_mode == MC2_QUANT_PERTOKEN_DYNAMIC) {
         e = mc2::launch_quant_pertoken(cp, rank_size, bs_local, static_cast<int>(h), x1_dtype == MC2_BF16, x1_scale,
@@ -338,7 +338,7 @@ int mc2_alltoall_quant_mm(const void *const *chunks, int rank_size, int64_t bs_l
         scale = const_cast<float *>(static_cast<const float *>(x1_scale));
     }
     if (e != cudaSuccess) return fail(MC2_ERR_CUDA, "prologue launch: %s", cudaGetErrorString(e));
-    if (!x2_done) e = mc2::launch_widen_i8(x2, x2h, K * n, dev.num_sms, s);
+    if (!x2_done) e = mc2::launch_widen_i8(x2, x2h, K * n, dev.num_sms, sk_flags, n_flags, s);
     if (e != cudaSuccess) return fail(MC2_ERR_CUDA, "x2 widening launch: %s", cudaGetErrorString(e));
 
     mc2::GemmParams p;

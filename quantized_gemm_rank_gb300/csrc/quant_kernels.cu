@@ -181,9 +181,13 @@ __global__ void __launch_bounds__(512) a2a_prologue_kernel(const __grid_constant
                                                            float *__restrict__ scale_out,
                                                            const int8_t *__restrict__ x2,
                                                            __half *__restrict__ x2h, int64_t x2_vecs,
-                                                           int64_t widen_ctas) {
+                                                           int64_t widen_ctas, int *__restrict__ zero_words,
+                                                           int n_zero) {
     ptx::allow_dependent_launch();
     const int64_t b = blockIdx.x;
+    // the GEMM's stream-K counters start at zero (it runs after this kernel)
+    if (b == gridDim.x - 1)
+        for (int i = threadIdx.x; i < n_zero; i += blockDim.x) zero_words[i] = 0;
     const int64_t G = gridDim.x;
     const int64_t before = b * widen_ctas / G;  // widen CTAs among [0, b)
     if ((b + 1) * widen_ctas / G > before) {
@@ -191,16 +195,27 @@ __global__ void __launch_bounds__(512) a2a_prologue_kernel(const __grid_constant
         const int64_t w = before;
         const int64_t per = (x2_vecs + widen_ctas - 1) / widen_ctas;
         const int64_t end = min(x2_vecs, (w + 1) * per);
-        for (int64_t i = w * per + threadIdx.x; i < end; i += blockDim.x) {
-            const int4 v = __ldg(reinterpret_cast<const int4 *>(x2) + i);
-            const int8_t *e = reinterpret_cast<const int8_t *>(&v);
-            uint4 o[2];
-            __half2 *oh = reinterpret_cast<__half2 *>(o);
+        // four loads in flight per thread before any conversion
+        for (int64_t i0 = w * per + threadIdx.x; i0 < end; i0 += 4 * blockDim.x) {
+            int4 v[4];
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-                oh[j] = __floats2half2_rn(static_cast<float>(e[2 * j]), static_cast<float>(e[2 * j + 1]));
-            reinterpret_cast<uint4 *>(x2h)[2 * i] = o[0];
-            reinterpret_cast<uint4 *>(x2h)[2 * i + 1] = o[1];
+            for (int u = 0; u < 4; ++u) {
+                const int64_t i = i0 + u * blockDim.x;
+                if (i < end) v[u] = __ldg(reinterpret_cast<const int4 *>(x2) + i);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int64_t i = i0 + u * blockDim.x;
+                if (i >= end) break;
+                const int8_t *e = reinterpret_cast<const int8_t *>(&v[u]);
+                uint4 o[2];
+                __half2 *oh = reinterpret_cast<__half2 *>(o);
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    oh[j] = __floats2half2_rn(static_cast<float>(e[2 * j]), static_cast<float>(e[2 * j + 1]));
+                reinterpret_cast<uint4 *>(x2h)[2 * i] = o[0];
+                reinterpret_cast<uint4 *>(x2h)[2 * i + 1] = o[1];
+            }
         }
         return;
     }
@@ -289,8 +304,11 @@ __global__ void __launch_bounds__(512) a2a_prologue_kernel(const __grid_constant
 
 // int8 -> fp16, exact, 16 elements per thread-iteration.
 __global__ void __launch_bounds__(256) widen_i8_kernel(const int8_t *__restrict__ src, __half *__restrict__ dst,
-                                                       int64_t count) {
+                                                       int64_t count, int *__restrict__ zero_words, int n_zero) {
     ptx::allow_dependent_launch();
+    // the GEMM's stream-K counters start at zero (it runs after this kernel)
+    if (blockIdx.x == 0)
+        for (int i = threadIdx.x; i < n_zero; i += blockDim.x) zero_words[i] = 0;
     const int64_t nvec = count / 16;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < nvec; i += stride) {
@@ -412,7 +430,7 @@ bool a2a_prologue_fits(int rank_size, int64_t bs_local, int h) {
 
 cudaError_t launch_a2a_prologue(const ChunkPtrs &chunks, int rank_size, int64_t bs_local, int h, bool bf16,
                                 const void *smooth, __half *qh, int8_t *q_out, float *scale_out, const int8_t *x2,
-                                __half *x2h, int64_t x2_count, cudaStream_t stream) {
+                                __half *x2h, int64_t x2_count, int *zero_words, int n_zero, cudaStream_t stream) {
     constexpr int kV = 8;
     const int K = rank_size * h;
     int threads = 64;
@@ -426,15 +444,18 @@ cudaError_t launch_a2a_prologue(const ChunkPtrs &chunks, int rank_size, int64_t 
     const uint16_t *sm = static_cast<const uint16_t *>(smooth);
     if (bf16)
         a2a_prologue_kernel<true, kV><<<static_cast<unsigned>(grid), threads, 0, stream>>>(
-            chunks, h, bs_local, rank_size, sm, qh, q_out, scale_out, x2, x2h, x2_vecs, widen_ctas);
+            chunks, h, bs_local, rank_size, sm, qh, q_out, scale_out, x2, x2h, x2_vecs, widen_ctas, zero_words,
+            n_zero);
     else
         a2a_prologue_kernel<false, kV><<<static_cast<unsigned>(grid), threads, 0, stream>>>(
-            chunks, h, bs_local, rank_size, sm, qh, q_out, scale_out, x2, x2h, x2_vecs, widen_ctas);
+            chunks, h, bs_local, rank_size, sm, qh, q_out, scale_out, x2, x2h, x2_vecs, widen_ctas, zero_words,
+            n_zero);
     return cudaGetLastError();
 }
 
-cudaError_t launch_widen_i8(const int8_t *src, __half *dst, int64_t count, int num_sms, cudaStream_t stream) {
-    widen_i8_kernel<<<grid_for(count / 16 + 1, 256, num_sms), 256, 0, stream>>>(src, dst, count);
+cudaError_t launch_widen_i8(const int8_t *src, __half *dst, int64_t count, int num_sms, int *zero_words, int n_zero,
+                            cudaStream_t stream) {
+    widen_i8_kernel<<<grid_for(count / 16 + 1, 256, num_sms), 256, 0, stream>>>(src, dst, count, zero_words, n_zero);
     return cudaGetLastError();
 }
 
