@@ -10,7 +10,9 @@ the IEEE layouts); this module only marshals torch CPU tensors into it.
 Pages followed (title -- section):
   * "torch_npu.npu_all_gather_base_mm" -- 功能说明, 接口原型, 输出说明, 约束说明
   * "aclnnAlltoAllQuantMatmul" -- 功能说明 / 计算公式 (dynamic- and full-quant)
-  * "hyper_parallel .../tensor_parallel/mc2.py" -- AllGatherMatmulFunction.forward
+  * "hyper_parallel .../tensor_parallel/mc2.py" -- module docstring (the
+    all_gather_matmul / matmul_reduce_scatter duals), AllGatherMatmulFunction
+    and MatmulReduceScatterFunction.forward
 
 Every function here is pinned by ``tests/test_oracle_*.py`` against closed
 forms, brute force and independent library routines.
@@ -65,6 +67,7 @@ def _load():
         lib.oracle_dequant.argtypes = [_P, _I64, _I64, _P, _P, _P, _P]
         lib.oracle_alltoall_quant_mm.argtypes = [_P, _INT, _I64, _I64, _INT, _INT, _P, _P, _P, _P,
                                                  _I64, _P, _I64, _P, _P, _P, _P]
+        lib.oracle_matmul_reduce_scatter.argtypes = [_P, _P, _INT, _I64, _I64, _I64, _INT, _P, _INT, _P, _I64, _P]
         lib.oracle_num_threads.restype = _INT
         _lib = lib
     return _lib
@@ -156,6 +159,25 @@ def all_gather_mm(chunks: Sequence[torch.Tensor], x2: torch.Tensor, *, x2_is_nk:
                                       int(x2_is_nk), _ptr(b), isb, _ptr(r), nr, out.data_ptr())
     _check(rc, "all_gather_mm")
     return out, (gather(cs) if gather_output else None)
+
+
+def matmul_reduce_scatter(x_chunks: Sequence[torch.Tensor], w_chunks: Sequence[torch.Tensor], *,
+                          w_is_nk: bool = True, bias: Optional[torch.Tensor] = None, rows=None) -> torch.Tensor:
+    """Y = ReduceScatter_m(sum_r X_r @ W_r^T): returns the (m, n) stack of the R
+    ranks' outputs (rank j = rows [j*m/R, (j+1)*m/R)), or only ``rows`` of it."""
+    xs = [_c(x) for x in x_chunks]
+    ws = [_c(w) for w in w_chunks]
+    dt = xs[0].dtype
+    isb = _is_bf16(dt)
+    m, k_local = xs[0].shape
+    n = ws[0].shape[0] if w_is_nk else ws[0].shape[1]
+    b = None if bias is None else _c(bias.to(dt))
+    r, nr = _rows_arg(rows)
+    out = torch.empty((nr if r is not None else m, n), dtype=dt)
+    rc = _load().oracle_matmul_reduce_scatter(_ptr_array(xs), _ptr_array(ws), len(xs), m, k_local, n,
+                                              int(w_is_nk), _ptr(b), isb, _ptr(r), nr, out.data_ptr())
+    _check(rc, "matmul_reduce_scatter")
+    return out
 
 
 # --------------------------------------------------------------------------- AlltoAllQuantMatmul

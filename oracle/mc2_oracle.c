@@ -386,3 +386,47 @@ int oracle_num_threads(void) {
     return 1;
 #endif
 }
+
+/* ------------------------------------------------------------------------ */
+/* [MC2] MatmulReduceScatter ("hyper_parallel .../mc2.py", module docstring:  */
+/*   matmul_reduce_scatter forward  Y = ReduceScatter_m(X @ W^T)), the dual    */
+/* of AllGatherMatmul.  Rank r holds X_r (m, k_local) and its weight shard     */
+/* W_r (n, k_local) (x2 = W_r^T, as MatmulReduceScatterFunction.forward        */
+/* passes w.t()).  The rank partials P_r = X_r @ W_r^T (m, n) are summed and   */
+/* the sum is scattered along m: rank j receives rows [j*m/R, (j+1)*m/R).     */
+/* Reading: the sum is exact (fp64 here) and rounded once to the output type; */
+/* bias (n), if given, is added before that rounding.                          */
+/* out is the (m, n) concatenation of the R ranks' outputs (rank j = block j). */
+/* ------------------------------------------------------------------------ */
+int oracle_matmul_reduce_scatter(const uint16_t *const *x_chunks, const uint16_t *const *w_chunks, int world_size,
+                                 int64_t m, int64_t k_local, int64_t n, int w_is_nk, const uint16_t *bias,
+                                 int is_bf16, const int64_t *rows, int64_t n_rows, uint16_t *out) {
+    if (!x_chunks || !w_chunks || !out || world_size < 1 || m < 1 || k_local < 1 || n < 1) return OR_ERR_ARG;
+    if (!rows) n_rows = m;
+    for (int64_t ii = 0; ii < n_rows; ++ii) {
+        int64_t i = rows ? rows[ii] : ii;
+        if (i < 0 || i >= m) return OR_ERR_ARG;
+    }
+    float *tab = (float *)malloc(65536 * sizeof(float));
+    if (!tab) return OR_ERR_NOMEM;
+    build_decode_table(is_bf16, tab);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t ii = 0; ii < n_rows; ++ii) {
+        int64_t i = rows ? rows[ii] : ii;
+        for (int64_t j = 0; j < n; ++j) {
+            double s = 0.0;
+            for (int r = 0; r < world_size; ++r) {        /* the reduction over ranks */
+                const uint16_t *xrow = x_chunks[r] + i * k_local;
+                for (int64_t kk = 0; kk < k_local; ++kk) {
+                    /* W_r^T[kk, j] = W_r[j, kk] (w_is_nk) or x2_r[kk, j] */
+                    uint16_t wv = w_is_nk ? w_chunks[r][j * k_local + kk] : w_chunks[r][kk * n + j];
+                    s += (double)tab[xrow[kk]] * (double)tab[wv];
+                }
+            }
+            if (bias) s += (double)tab[bias[j]];
+            out[ii * n + j] = oracle_encode16_rne(s, is_bf16);
+        }
+    }
+    free(tab);
+    return OR_OK;
+}
