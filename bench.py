@@ -349,7 +349,7 @@ def run_reference(args):
 
 # ----------------------------------------------------------------------------- main
 def extra_table(dev, flush, stream, steps):
-    """Per-workload device times of each call alone (all five workloads)."""
+    """Per-workload device times of each call alone (every workload but the step's two)."""
     import quantized_gemm_rank_gb300 as mc2
     res = {}
     for name, s in mc2_inputs.WORKLOADS.items():
@@ -363,6 +363,14 @@ def extra_table(dev, flush, stream, steps):
             out = torch.empty((s.m, s.n), dtype=s.dtype, device=dev)
             g = torch.empty((s.m, s.k), dtype=s.dtype, device=dev)
             fn = lambda: mc2.mc2_all_gather_mm(ch, x2, x2_is_nk=s.x2_is_nk, bias=b, out=out, gathered=g)  # noqa
+            fl = s.flops
+        elif isinstance(s, mc2_inputs.MMRSShape):
+            inp = mc2_inputs.mmrs_inputs(s, seed=0)
+            ch = [x.to(dev) for x in inp["x_chunks"]]
+            wc = [w.to(dev) for w in inp["w_chunks"]]
+            b = None if inp["bias"] is None else inp["bias"].to(dev)
+            outs = [torch.empty((s.m // s.world_size, s.n), dtype=s.dtype, device=dev) for _ in range(s.world_size)]
+            fn = lambda: mc2.mc2_matmul_reduce_scatter(ch, wc, w_is_nk=s.w_is_nk, bias=b, out_chunks=outs)  # noqa
             fl = s.flops
         else:
             inp = mc2_inputs.a2a_inputs(s, seed=0)

@@ -89,6 +89,37 @@ int mc2_all_gather_mm(const void *const *x_chunks, int world_size, int64_t m_loc
                       int gather_output, void *out, void *gathered, void *stream);
 
 /*
+ * MatmulReduceScatter  (hyper_parallel mc2.py, module docstring:
+ * matmul_reduce_scatter forward Y = ReduceScatter_m(X @ W^T), the dual of
+ * AllGatherMatmul; MatmulReduceScatterFunction.forward passes w.t()).  Rank r
+ * holds its activations X_r (m, k_local) and its weight shard W_r; the ranks'
+ * partial products are summed and the sum's row blocks scattered:
+ *
+ *   Y      = sum_r X_r @ W_r^T                                  (m, n)
+ *   out_j  = Y[j*m/R : (j+1)*m/R, :] (+ bias)                   rank j's output
+ *
+ *   The sum over ranks and k is accumulated in fp32 (blocks of 1024 k summed
+ *   in fp32 registers) and rounded once (nearest-even) to `dtype`; bias, if
+ *   given, is added in fp32 before the rounding.
+ *
+ *   x_chunks    host array of world_size device pointers, each (m, k_local)
+ *   w_chunks    host array of world_size device pointers: w (n, k_local)
+ *               row-major (w_is_nk != 0, the nn.Linear layout) or x2 = w^T
+ *               (k_local, n) row-major (w_is_nk == 0)
+ *   world_size  2, 4 or 8;  m % world_size == 0
+ *   k_local     256 <= k_local < 65535 (this kernel: k_local % 64 == 0)
+ *   n           >= 1 (this kernel: n % 8 == 0)
+ *   bias        NULL or (n) of `dtype`
+ *   dtype       MC2_F16 or MC2_BF16 for every tensor
+ *   out_chunks  host array of world_size device pointers, each (m/world_size, n)
+ *
+ * Returns MC2_OK or a negative mc2_status; nothing is launched on error.
+ */
+int mc2_matmul_reduce_scatter(const void *const *x_chunks, const void *const *w_chunks, int world_size, int64_t m,
+                              int64_t k_local, int64_t n, int w_is_nk, const void *bias, int dtype,
+                              void *const *out_chunks, void *stream);
+
+/*
  * Workspace size (bytes) that mc2_alltoall_quant_mm needs for these sizes.
  * Same argument meanings and validation as mc2_alltoall_quant_mm.
  */

@@ -23,6 +23,10 @@ Workloads (names used throughout the repository):
              [-127, 127], x2 scale (4096) fp32 ~U(1e-3, 1e-2), bias (4096) fp32
              ~N(0, 0.1).
   a2a-dyn-small  the same with chunks (512, 1024).
+  mmrs-4x2048  MatmulReduceScatter bf16, 4 ranks x activations (16384, 2048)
+             ~N(0,1) and nn.Linear weight shards w_r (8192, 2048)
+             ~N(0, std K^-1/2) with K = 8192 the unsharded contraction, no
+             bias: the row-parallel dual of ag-4x4096.
   a2a-full   AlltoAllQuantMatmul, quant mode 3 (pre-quantised int8), 8 ranks x
              (16384, 4096) int8 uniform on [-127, 127], per-token x1 scale
              (16384) fp32 ~U(1e-3, 1e-2), x2 int8 (32768, 7168), x2 scale
@@ -81,6 +85,28 @@ class A2AShape:
         return 2.0 * self.bs_local * self.n * self.k
 
 
+@dataclass(frozen=True)
+class MMRSShape:
+    world_size: int
+    m: int                          # rows of every rank's activations (the scatter splits them)
+    k_local: int                    # every rank's slice of the contraction
+    n: int
+    dtype: torch.dtype = torch.bfloat16
+    w_is_nk: bool = True            # weight shards as nn.Linear w (n, k_local); else x2 = w^T
+    bias: bool = False
+    x_std: float = 1.0
+    w_std: Optional[float] = None   # None: (world_size * k_local) ** -0.5
+    bias_std: float = 0.02
+
+    @property
+    def k(self) -> int:
+        return self.world_size * self.k_local
+
+    @property
+    def flops(self) -> float:
+        return 2.0 * self.m * self.n * self.k
+
+
 WORKLOADS = {
     "ag-tiny": AGShape(world_size=8, m_local=16, k=512, n=64, dtype=torch.float16, w_std=1.0),
     "ag-8x1024": AGShape(world_size=8, m_local=1024, k=4096, n=4096),
@@ -88,6 +114,7 @@ WORKLOADS = {
     "a2a-dyn": A2AShape(rank_size=8, bs_local=4096, h=1024, n=4096, quant_mode=7),
     "a2a-dyn-small": A2AShape(rank_size=8, bs_local=512, h=1024, n=4096, quant_mode=7),
     "a2a-full": A2AShape(rank_size=8, bs_local=16384, h=4096, n=7168, quant_mode=3),
+    "mmrs-4x2048": MMRSShape(world_size=4, m=16384, k_local=2048, n=8192),
 }
 
 
@@ -116,6 +143,18 @@ def ag_inputs(s: AGShape, seed: int = 0) -> dict:
     x2 = (torch.randn(*wshape, generator=g) * w_std).to(s.dtype)
     bias = (torch.randn(s.n, generator=g) * s.bias_std).to(s.dtype) if s.bias else None
     return {"chunks": chunks, "x2": x2, "bias": bias}
+
+
+def mmrs_inputs(s: MMRSShape, seed: int = 0) -> dict:
+    """x_chunks (R x (m, k_local)), w_chunks (R x (n, k_local), or (k_local, n)
+    when not w_is_nk), bias (n) or None."""
+    g = _gen(seed)
+    xs = [(torch.randn(s.m, s.k_local, generator=g) * s.x_std).to(s.dtype) for _ in range(s.world_size)]
+    w_std = s.k ** -0.5 if s.w_std is None else s.w_std
+    wshape = (s.n, s.k_local) if s.w_is_nk else (s.k_local, s.n)
+    ws = [(torch.randn(*wshape, generator=g) * w_std).to(s.dtype) for _ in range(s.world_size)]
+    bias = (torch.randn(s.n, generator=g) * s.bias_std).to(s.dtype) if s.bias else None
+    return {"x_chunks": xs, "w_chunks": ws, "bias": bias}
 
 
 def a2a_inputs(s: A2AShape, seed: int = 0) -> dict:

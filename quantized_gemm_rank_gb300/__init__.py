@@ -8,6 +8,7 @@ cannot be built or loaded, importing the functions raises.
 
   mc2_all_gather_mm        out = concat_m(x_chunks) @ x2 (+ bias), plus gathered
   mc2_alltoall_quant_mm    out = (Quant(permute(chunks)) @ x2) * x1s * x2s + bias
+  mc2_matmul_reduce_scatter  out_j = (sum_r X_r @ W_r^T)[rows of rank j] (+ bias)
 """
 from __future__ import annotations
 
@@ -54,6 +55,8 @@ def lib() -> ctypes.CDLL:
         L = ctypes.CDLL(path)
         L.mc2_all_gather_mm.argtypes = [_P, _INT, _I64, _I64, _P, _I64, _INT, _P, _INT, _INT, _P, _P, _P]
         L.mc2_all_gather_mm.restype = _INT
+        L.mc2_matmul_reduce_scatter.argtypes = [_P, _P, _INT, _I64, _I64, _I64, _INT, _P, _INT, _P, _P]
+        L.mc2_matmul_reduce_scatter.restype = _INT
         L.mc2_alltoall_quant_mm_workspace.argtypes = [_INT, _I64, _I64, _I64, _INT, _INT,
                                                       ctypes.POINTER(ctypes.c_size_t)]
         L.mc2_alltoall_quant_mm_workspace.restype = _INT
@@ -140,6 +143,28 @@ def mc2_all_gather_mm(x_chunks: Sequence[torch.Tensor], x2: torch.Tensor, *, x2_
     return out, (gathered if gather_output else None)
 
 
+def mc2_matmul_reduce_scatter(x_chunks: Sequence[torch.Tensor], w_chunks: Sequence[torch.Tensor], *,
+                              w_is_nk: bool = True, bias: Optional[torch.Tensor] = None,
+                              out_chunks: Optional[Sequence[torch.Tensor]] = None, stream=None):
+    """MatmulReduceScatter on the ranks' shards already resident on this GPU.
+
+    x_chunks: world_size tensors (m, k_local); w_chunks: world_size weight shards
+    (n, k_local) (or (k_local, n) with ``w_is_nk=False``).  Returns the list of
+    the ranks' outputs, each (m / world_size, n).
+    """
+    R = len(x_chunks)
+    m, k_local = x_chunks[0].shape
+    n = w_chunks[0].shape[0] if w_is_nk else w_chunks[0].shape[1]
+    dt = x_chunks[0].dtype
+    if out_chunks is None:
+        out_chunks = [torch.empty((m // R, n), dtype=dt, device=x_chunks[0].device) for _ in range(R)]
+    st = lib().mc2_matmul_reduce_scatter(_ptrs(x_chunks, "x_chunks"), _ptrs(w_chunks, "w_chunks"), R, m, k_local, n,
+                                         int(w_is_nk), _opt(bias, "bias"), _dtype_code(dt),
+                                         _ptrs(out_chunks, "out_chunks"), _stream(stream))
+    _check(st)
+    return list(out_chunks)
+
+
 def mc2_alltoall_quant_mm_workspace(rank_size: int, bs_local: int, h: int, n: int, x1_quant_mode: int,
                                     x1_dtype: torch.dtype) -> int:
     nbytes = ctypes.c_size_t(0)
@@ -218,7 +243,8 @@ def mc2_device_status() -> int:
 
 __all__ = [
     "Mc2Error", "lib", "library_path", "status_str", "last_error", "mc2_all_gather_mm",
-    "mc2_alltoall_quant_mm_workspace", "mc2_alltoall_quant_mm", "mc2_alltoall_quant_mm_no_alloc",
+    "mc2_matmul_reduce_scatter", "mc2_alltoall_quant_mm_workspace", "mc2_alltoall_quant_mm",
+    "mc2_alltoall_quant_mm_no_alloc",
     "NO_ALLOC_SCRATCH_BYTES", "mc2_device_status",
     "MC2_OK", "MC2_ERR_NULL", "MC2_ERR_SHAPE", "MC2_ERR_DTYPE", "MC2_ERR_UNSUPPORTED", "MC2_ERR_WORKSPACE",
     "MC2_ERR_CUDA", "MC2_ERR_TIMEOUT", "MC2_F16", "MC2_BF16", "MC2_F32", "MC2_I8",

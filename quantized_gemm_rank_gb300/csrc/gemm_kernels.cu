@@ -38,10 +38,10 @@ int concurrent_pairs(int num_sms) {
     return clusters;
 }
 
-template <int kG, bool kBF16, bool kIntPath>
+template <int kG, bool kBF16, bool kIntPath, bool kRS = false>
 cudaError_t launch_one(const GemmParams &p_in, int num_sms, cudaStream_t stream) {
     using Cfg = TileCfg<kG>;
-    auto kern = mc2_gemm_kernel<kG, kBF16, kIntPath>;
+    auto kern = mc2_gemm_kernel<kG, kBF16, kIntPath, kRS>;
     GemmParams p = p_in;
     // per device, once: the status word's address and the shared-memory opt-in
     static int *status_addr[64] = {nullptr};
@@ -98,6 +98,8 @@ int gemm_units(GemmKind kind, int group, int num_sms) {
     switch (kind) {
         case GEMM_F16: return concurrent_pairs<false, false>(num_sms);
         case GEMM_BF16: return concurrent_pairs<true, false>(num_sms);
+        case GEMM_RS_F16: return concurrent_pairs<false, false>(num_sms);
+        case GEMM_RS_BF16: return concurrent_pairs<true, false>(num_sms);
         default: return concurrent_pairs<false, true>(num_sms);
     }
 }
@@ -108,12 +110,16 @@ cudaError_t launch_gemm(GemmKind kind, int group, const GemmParams &p, int num_s
             case GEMM_F16: return launch_one<2, false, false>(p, num_sms, stream);
             case GEMM_BF16: return launch_one<2, true, false>(p, num_sms, stream);
             case GEMM_INT_AS_F16: return launch_one<2, false, true>(p, num_sms, stream);
+            case GEMM_RS_F16: return launch_one<2, false, false, true>(p, num_sms, stream);
+            case GEMM_RS_BF16: return launch_one<2, true, false, true>(p, num_sms, stream);
         }
     } else {
         switch (kind) {
             case GEMM_F16: return launch_one<1, false, false>(p, num_sms, stream);
             case GEMM_BF16: return launch_one<1, true, false>(p, num_sms, stream);
             case GEMM_INT_AS_F16: return launch_one<1, false, true>(p, num_sms, stream);
+            case GEMM_RS_F16: return launch_one<1, false, false, true>(p, num_sms, stream);
+            case GEMM_RS_BF16: return launch_one<1, true, false, true>(p, num_sms, stream);
         }
     }
     return cudaErrorInvalidValue;

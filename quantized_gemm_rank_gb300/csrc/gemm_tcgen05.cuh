@@ -97,6 +97,12 @@ struct GemmParams {
     int *sk_flags;                  // stream-K: partial parts written, per (tile, cta); zero at launch
     int *status;                    // device word set to -7 when a bounded wait gives up
     uint64_t wait_limit_ns;
+    // reduce-scatter instantiation only (kRS): B is rank r's weight shard for the
+    // k-slice r (same k-interleave as A), and output row i goes to rank
+    // i / out_rows at row i % out_rows
+    CUtensorMap b_rank_maps[kMaxAMaps];
+    void *out_chunks[kMaxAMaps];
+    int out_rows;
 };
 
 // ---------------------------------------------------------------------------
@@ -234,9 +240,10 @@ __device__ __forceinline__ float load16(const void *base, int idx) {
     }
 }
 
-// Store 32 consecutive 16-bit outputs of one row (col0 .. col0+31), masked at n.
-__device__ __forceinline__ void store_row32_16(void *out, int n, int row, int col0, const uint32_t (&pk)[16]) {
-    uint16_t *dst = reinterpret_cast<uint16_t *>(out) + static_cast<int64_t>(row) * n + col0;
+// Store 32 consecutive 16-bit outputs (columns col0 .. col0+31) of the row that
+// starts at row_ptr, masked at n.
+__device__ __forceinline__ void store_row32_16(uint16_t *row_ptr, int n, int col0, const uint32_t (&pk)[16]) {
+    uint16_t *dst = row_ptr + col0;
     if (col0 + 32 <= n) {
         uint4 *d4 = reinterpret_cast<uint4 *>(dst);
 #pragma unroll
@@ -248,7 +255,7 @@ __device__ __forceinline__ void store_row32_16(void *out, int n, int row, int co
     }
 }
 
-template <int kG, bool kBF16, bool kIntPath>
+template <int kG, bool kBF16, bool kIntPath, bool kRS = false>
 __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_constant__ GemmParams p) {
     using Cfg = TileCfg<kG>;
     constexpr bool kPair = kG == 2;
@@ -308,7 +315,11 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
     if (warp == 0 && lane == 0) {
         // ------------------------------------------------------------ TMA producer
         for (int i = 0; i < p.num_a_maps; ++i) ptx::prefetch_tmap(&p.a_maps[i]);
-        ptx::prefetch_tmap(&p.b_map);
+        if constexpr (kRS) {
+            for (int i = 0; i < p.num_a_maps; ++i) ptx::prefetch_tmap(&p.b_rank_maps[i]);
+        } else {
+            ptx::prefetch_tmap(&p.b_map);
+        }
         // bytes that complete the leader's full barrier per stage (both CTAs' tiles)
         constexpr uint32_t leader_bytes = Cfg::kStageBytes * kG;
         int stage = 0;
@@ -371,17 +382,30 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
                 } else if (p.a_mode == A_KINTERLEAVE) {
                     // permuted column k0 = kc * k_local + kl lives in chunk kc (k_local % kBK == 0)
                     load(sA, &p.a_maps[kc], kl, m0, a_bar);
+                    if constexpr (kRS) {
+                        // ... and so does the B slice: rank kc's weight shard at column kl
+                        const CUtensorMap *bm = &p.b_rank_maps[kc];
+                        if (p.b_mn_major) {
+#pragma unroll
+                            for (int j = 0; j < Cfg::kBRows / 64; ++j)
+                                load(sB + j * (kBK * 128), bm, n0 + 64 * j, kl, b_bar);
+                        } else {
+                            load(sB, bm, kl, n0, b_bar);
+                        }
+                    }
                     kl += kBK;
                     if (kl >= p.k_local) kl = 0, ++kc;
                 } else {
                     load(sA, &p.a_maps[0], k0, m0, a_bar);
                 }
-                if (p.b_mn_major) {
+                if constexpr (!kRS) {
+                    if (p.b_mn_major) {
 #pragma unroll
-                    for (int j = 0; j < Cfg::kBRows / 64; ++j)
-                        load(sB + j * (kBK * 128), &p.b_map, n0 + 64 * j, k0, b_bar);
-                } else {
-                    load(sB, &p.b_map, k0, n0, b_bar);
+                        for (int j = 0; j < Cfg::kBRows / 64; ++j)
+                            load(sB + j * (kBK * 128), &p.b_map, n0 + 64 * j, k0, b_bar);
+                    } else {
+                        load(sB, &p.b_map, k0, n0, b_bar);
+                    }
                 }
                 ++iters;
                 if (++stage == S) stage = 0, phase ^= 1u;
@@ -600,6 +624,12 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
             }
             if (row >= p.m) continue;
             if constexpr (!kIntPath) {
+                uint16_t *orow;
+                if constexpr (kRS)
+                    orow = reinterpret_cast<uint16_t *>(p.out_chunks[row / p.out_rows]) +
+                           static_cast<int64_t>(row % p.out_rows) * p.n;
+                else
+                    orow = reinterpret_cast<uint16_t *>(p.out) + static_cast<int64_t>(row) * p.n;
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     const int col0 = colh + c * 32;
@@ -615,7 +645,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
                         uint32_t pk[16];
 #pragma unroll
                         for (int i = 0; i < 16; ++i) pk[i] = pack2<kBF16>(v[2 * i], v[2 * i + 1]);
-                        store_row32_16(p.out, p.n, row, col0, pk);
+                        store_row32_16(orow, p.n, col0, pk);
                     }
                 }
             } else {
@@ -643,7 +673,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
                             }
                             pk[i >> 1] = pack2<true>(o[0], o[1]);
                         }
-                        store_row32_16(p.out, p.n, row, col0, pk);
+                        store_row32_16(reinterpret_cast<uint16_t *>(p.out) + static_cast<int64_t>(row) * p.n, p.n,
+                                       col0, pk);
                         if (p.acc_out != nullptr) {
                             int32_t *dst = p.acc_out + static_cast<int64_t>(row) * p.n + col0;
                             if (col0 + 32 <= p.n) {

@@ -252,6 +252,67 @@ int mc2_all_gather_mm(const void *const *x_chunks, int world_size, int64_t m_loc
     return MC2_OK;
 }
 
+int mc2_matmul_reduce_scatter(const void *const *x_chunks, const void *const *w_chunks, int world_size, int64_t m,
+                              int64_t k_local, int64_t n, int w_is_nk, const void *bias, int dtype,
+                              void *const *out_chunks, void *stream) {
+    g_last_error[0] = '\0';
+    if (!x_chunks || !w_chunks || !out_chunks) return fail(MC2_ERR_NULL, "x_chunks, w_chunks and out_chunks are required");
+    if (world_size != 2 && world_size != 4 && world_size != 8)
+        return fail(MC2_ERR_SHAPE, "world_size must be 2, 4 or 8 (got %d)", world_size);
+    for (int r = 0; r < world_size; ++r)
+        if (!x_chunks[r] || !w_chunks[r] || !out_chunks[r])
+            return fail(MC2_ERR_NULL, "x_chunks[%d], w_chunks[%d] or out_chunks[%d] is NULL", r, r, r);
+    if (dtype != MC2_F16 && dtype != MC2_BF16)
+        return fail(MC2_ERR_DTYPE, "dtype must be MC2_F16 or MC2_BF16 (got %d)", dtype);
+    if (m < 1 || n < 1) return fail(MC2_ERR_SHAPE, "empty tensors are not supported (m=%lld n=%lld)", (long long)m,
+                                    (long long)n);
+    if (m % world_size != 0)
+        return fail(MC2_ERR_SHAPE, "m = %lld is not divisible by world_size %d (the scatter splits m)", (long long)m,
+                    world_size);
+    if (k_local < 256 || k_local >= 65535)
+        return fail(MC2_ERR_SHAPE, "the contraction size k must be in [256, 65535) (got %lld)", (long long)k_local);
+    if (m > INT32_MAX || n > INT32_MAX) return fail(MC2_ERR_SHAPE, "m or n exceeds INT32_MAX");
+    if (k_local % mc2::kBK != 0)
+        return fail(MC2_ERR_UNSUPPORTED, "this kernel needs k %% 64 == 0 (a k-tile may not straddle two ranks), got %lld",
+                    (long long)k_local);
+    if (n % 8 != 0) return fail(MC2_ERR_UNSUPPORTED, "this kernel needs n %% 8 == 0 (got %lld)", (long long)n);
+    for (int r = 0; r < world_size; ++r)
+        if (!aligned16(x_chunks[r]) || !aligned16(w_chunks[r]) || !aligned16(out_chunks[r]))
+            return fail(MC2_ERR_UNSUPPORTED, "rank %d's buffers must be 16-byte aligned", r);
+    if (bias && !aligned16(bias)) return fail(MC2_ERR_UNSUPPORTED, "bias must be 16-byte aligned");
+
+    DeviceInfo dev;
+    if (int st = current_device(&dev)) return st;
+    mc2::GemmParams p;
+    memset(&p, 0, sizeof(p));
+    const int group = mc2::gemm_group_for(static_cast<int>(m));
+    // A: rank r's activations X_r (m, k_local) are k-slice r of the contraction;
+    // B: rank r's weight shard, w (n, k_local) K-major or x2 (k_local, n) N-major
+    for (int r = 0; r < world_size; ++r) {
+        if (!make_map16(&p.a_maps[r], x_chunks[r], k_local, m, mc2::kBK, mc2::kBM))
+            return fail(MC2_ERR_CUDA, "cuTensorMapEncodeTiled failed for x_chunks[%d]", r);
+        const bool okb = w_is_nk ? make_map16(&p.b_rank_maps[r], w_chunks[r], k_local, n, mc2::kBK, mc2::kBN / group)
+                                 : make_map16(&p.b_rank_maps[r], w_chunks[r], n, k_local, 64, mc2::kBK);
+        if (!okb) return fail(MC2_ERR_CUDA, "cuTensorMapEncodeTiled failed for w_chunks[%d]", r);
+        p.out_chunks[r] = out_chunks[r];
+    }
+    p.num_a_maps = world_size;
+    p.a_mode = mc2::A_KINTERLEAVE;
+    p.k_local = static_cast<int>(k_local);
+    p.b_mn_major = w_is_nk ? 0 : 1;
+    p.out_rows = static_cast<int>(m / world_size);
+    p.m = static_cast<int>(m);
+    p.n = static_cast<int>(n);
+    p.k = static_cast<int>(k_local * world_size);
+    p.kblock_tiles = kKBlockTiles;
+    p.bias16 = bias;
+    p.wait_limit_ns = kWaitLimitNs;
+    cudaError_t e = mc2::launch_gemm(dtype == MC2_BF16 ? mc2::GEMM_RS_BF16 : mc2::GEMM_RS_F16, group, p, dev.num_sms,
+                                     static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(MC2_ERR_CUDA, "GEMM launch: %s", cudaGetErrorString(e));
+    return MC2_OK;
+}
+
 int mc2_alltoall_quant_mm_workspace(int rank_size, int64_t bs_local, int64_t h, int64_t n, int x1_quant_mode,
                                     int x1_dtype, size_t *bytes) {
     g_last_error[0] = '\0';

@@ -94,6 +94,52 @@ def test_all_gather_gather_flag_consistency():
     assert st == mc2.MC2_ERR_SHAPE
 
 
+def mmrs_call(world_size=2, m=16, k_local=256, n=64, w_is_nk=1, bias=None, dtype=mc2.MC2_BF16, xs=None, ws=None,
+              outs=None):
+    xs = [FAKE] * max(world_size, 1) if xs is None else xs
+    ws = [FAKE] * max(world_size, 1) if ws is None else ws
+    outs = [FAKE] * max(world_size, 1) if outs is None else outs
+    arr = lambda v: (ctypes.c_void_p * len(v))(*v)
+    return mc2.lib().mc2_matmul_reduce_scatter(arr(xs), arr(ws), world_size, m, k_local, n, w_is_nk, bias, dtype,
+                                               arr(outs), None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(world_size=3), mc2.MC2_ERR_SHAPE),
+    (dict(world_size=1), mc2.MC2_ERR_SHAPE),
+    (dict(m=17), mc2.MC2_ERR_SHAPE),                    # m not divisible by world_size
+    (dict(m=0), mc2.MC2_ERR_SHAPE),
+    (dict(n=0), mc2.MC2_ERR_SHAPE),
+    (dict(k_local=255), mc2.MC2_ERR_SHAPE),
+    (dict(k_local=65535), mc2.MC2_ERR_SHAPE),
+    (dict(dtype=mc2.MC2_F32), mc2.MC2_ERR_DTYPE),
+    (dict(xs=[FAKE, None]), mc2.MC2_ERR_NULL),
+    (dict(ws=[None, FAKE]), mc2.MC2_ERR_NULL),
+    (dict(outs=[FAKE, None]), mc2.MC2_ERR_NULL),
+    (dict(k_local=328), mc2.MC2_ERR_UNSUPPORTED),       # a k-tile would straddle two ranks
+    (dict(n=60), mc2.MC2_ERR_UNSUPPORTED),
+    (dict(ws=[FAKE, FAKE + 8]), mc2.MC2_ERR_UNSUPPORTED),
+    (dict(bias=FAKE + 2), mc2.MC2_ERR_UNSUPPORTED),
+])
+def test_matmul_reduce_scatter_rejects(kw, status):
+    assert mmrs_call(**kw) == status, mc2.last_error()
+    assert mc2.last_error() != ""
+
+
+def test_matmul_reduce_scatter_null_arrays():
+    L = mc2.lib()
+    arr = (ctypes.c_void_p * 2)(FAKE, FAKE)
+    assert L.mc2_matmul_reduce_scatter(None, arr, 2, 16, 256, 64, 1, None, mc2.MC2_BF16, arr, None) == mc2.MC2_ERR_NULL
+    assert L.mc2_matmul_reduce_scatter(arr, arr, 2, 16, 256, 64, 1, None, mc2.MC2_BF16, None, None) == mc2.MC2_ERR_NULL
+
+
+def test_matmul_reduce_scatter_bounds_accepted_by_validation():
+    if torch.cuda.is_available():
+        pytest.skip("would launch on a real device with fake pointers")
+    for kl in (256, 65472):
+        assert mmrs_call(k_local=kl) == mc2.MC2_ERR_CUDA, mc2.last_error()
+
+
 def a2a_call(rank_size=2, bs_local=16, h=64, x1_dtype=mc2.MC2_BF16, x1_scale=None, x2=FAKE, x2_scale=FAKE,
              bias=FAKE, bias_dtype=mc2.MC2_F32, mode=7, mode2=2, n=64, out=FAKE, ws=FAKE, ws_bytes=1 << 40,
              chunks=None):
