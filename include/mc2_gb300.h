@@ -154,6 +154,9 @@ int mc2_alltoall_quant_mm_workspace(int rank_size, int64_t bs_local, int64_t h, 
  *   bias            (n), required; bias_dtype MC2_F32 or MC2_BF16
  *   n               1 <= n <= INT32_MAX (this kernel: n % 16 == 0)
  *   out             bf16 (bs_local, n)
+ *   alltoall_out    NULL or (rank_size, bs_local, h) of x1_dtype: alltoAllOutOptional,
+ *                   read as commOut, the AlltoAll's result before the permute
+ *                   (chunks[r] stored as block r); same dtype as x1 (约束说明)
  *   q_out           NULL or int8 (bs_local, rank_size*h): the quantised activations (mode 7)
  *   x1_scale_out    NULL or fp32 (bs_local): the per-token scales (mode 7)
  *   acc_out         NULL or int32 (bs_local, n): the exact accumulators (debug)
@@ -164,8 +167,8 @@ int mc2_alltoall_quant_mm_workspace(int rank_size, int64_t bs_local, int64_t h, 
 int mc2_alltoall_quant_mm(const void *const *chunks, int rank_size, int64_t bs_local, int64_t h,
                           int x1_dtype, const void *x1_scale, const int8_t *x2, const float *x2_scale,
                           const void *bias, int bias_dtype, int x1_quant_mode, int x2_quant_mode,
-                          int64_t n, void *out, int8_t *q_out, float *x1_scale_out, int32_t *acc_out,
-                          void *workspace, size_t workspace_bytes, void *stream);
+                          int64_t n, void *out, void *alltoall_out, int8_t *q_out, float *x1_scale_out,
+                          int32_t *acc_out, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * AlltoAllQuantMatmul for callers that cannot allocate device memory.  The
@@ -198,7 +201,8 @@ int mc2_alltoall_quant_mm(const void *const *chunks, int rank_size, int64_t bs_l
 int mc2_alltoall_quant_mm_no_alloc(const void *const *chunks, int rank_size, int64_t bs_local, int64_t h,
                                    int x1_dtype, const void *x1_scale, const int8_t *x2, const float *x2_scale,
                                    const void *bias, int bias_dtype, int x1_quant_mode, int x2_quant_mode, int64_t n,
-                                   void *out, int8_t *q_out, float *x1_scale_out, int32_t *acc_out, void *stream);
+                                   void *out, void *alltoall_out, int8_t *q_out, float *x1_scale_out,
+                                   int32_t *acc_out, void *stream);
 
 /* Name of a status code (static string). */
 const char *mc2_status_str(int status);

@@ -62,6 +62,7 @@ def _load():
         lib.oracle_gather.argtypes = [_P, _INT, _I64, _I64, _P]
         lib.oracle_all_gather_mm.argtypes = [_P, _INT, _I64, _I64, _P, _I64, _INT, _P, _INT, _P, _I64, _P]
         lib.oracle_permute.argtypes = [_P, _INT, _I64, _I64, _INT, _P, _I64, _P]
+        lib.oracle_comm_out.argtypes = [_P, _INT, _I64, _I64, _INT, _P]
         lib.oracle_quant_pertoken_dynamic.argtypes = [_P, _I64, _I64, _P, _INT, _P, _P]
         lib.oracle_int8_mm.argtypes = [_P, _I64, _I64, _P, _I64, _P]
         lib.oracle_dequant.argtypes = [_P, _I64, _I64, _P, _P, _P, _P]
@@ -181,6 +182,17 @@ def matmul_reduce_scatter(x_chunks: Sequence[torch.Tensor], w_chunks: Sequence[t
 
 
 # --------------------------------------------------------------------------- AlltoAllQuantMatmul
+def comm_out(chunks: Sequence[torch.Tensor]) -> torch.Tensor:
+    """commOut (R, BS/R, H): block r is the chunk received from rank r (the
+    optional alltoAllOut output)."""
+    cs = [_c(c) for c in chunks]
+    bs_local, h = cs[0].shape
+    out = torch.empty((len(cs), bs_local, h), dtype=cs[0].dtype)
+    _check(_load().oracle_comm_out(_ptr_array(cs), len(cs), bs_local, h, cs[0].element_size(), out.data_ptr()),
+           "comm_out")
+    return out
+
+
 def permute(chunks: Sequence[torch.Tensor], rows=None) -> torch.Tensor:
     """permutedOut[t, r*H + h] = chunk_r[t, h] for the requested rows t."""
     cs = [_c(c) for c in chunks]

@@ -202,6 +202,29 @@ int oracle_all_gather_mm(const uint16_t *const *chunks, int world_size, int64_t 
 /*   permutedOut  = commOut.permute(1, 0, 2).view(BS/rankSize, rankSize*H)   */
 /* The rank's received blocks are commOut[r] = chunk r, each (BS/R, H).      */
 /* permute(1,0,2) then view gives permutedOut[t, r*H + h] = chunk_r[t, h].   */
+/* [A2A] commOut = AlltoAll(x1.view(rankSize, BS/rankSize, H)): after the
+ * exchange, block r of this rank's commOut (rankSize, BS/rankSize, H) is what
+ * rank r sent it, i.e. received chunk r.  commOut[r, t, hh] = chunk_r[t, hh],
+ * returned as the optional alltoAllOut output (same dtype as x1). */
+int oracle_comm_out(const void *const *chunks, int rank_size, int64_t bs_local, int64_t h, int elem_bytes,
+                    void *comm_out) {
+    if (!chunks || !comm_out || rank_size < 1 || bs_local < 1 || h < 1) return OR_ERR_ARG;
+    if (elem_bytes != 1 && elem_bytes != 2) return OR_ERR_ARG;
+    for (int r = 0; r < rank_size; ++r) {
+        for (int64_t t = 0; t < bs_local; ++t) {
+            for (int64_t hh = 0; hh < h; ++hh) {
+                int64_t dst = ((int64_t)r * bs_local + t) * h + hh;
+                int64_t src = t * h + hh;
+                if (elem_bytes == 1)
+                    ((int8_t *)comm_out)[dst] = ((const int8_t *)chunks[r])[src];
+                else
+                    ((uint16_t *)comm_out)[dst] = ((const uint16_t *)chunks[r])[src];
+            }
+        }
+    }
+    return OR_OK;
+}
+
 /* ------------------------------------------------------------------------ */
 
 int oracle_permute(const void *const *chunks, int rank_size, int64_t bs_local, int64_t h,

@@ -61,10 +61,10 @@ def lib() -> ctypes.CDLL:
                                                       ctypes.POINTER(ctypes.c_size_t)]
         L.mc2_alltoall_quant_mm_workspace.restype = _INT
         L.mc2_alltoall_quant_mm.argtypes = [_P, _INT, _I64, _I64, _INT, _P, _P, _P, _P, _INT, _INT, _INT, _I64,
-                                            _P, _P, _P, _P, _P, ctypes.c_size_t, _P]
+                                            _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]
         L.mc2_alltoall_quant_mm.restype = _INT
         L.mc2_alltoall_quant_mm_no_alloc.argtypes = [_P, _INT, _I64, _I64, _INT, _P, _P, _P, _P, _INT, _INT, _INT,
-                                                     _I64, _P, _P, _P, _P, _P]
+                                                     _I64, _P, _P, _P, _P, _P, _P]
         L.mc2_alltoall_quant_mm_no_alloc.restype = _INT
         L.mc2_status_str.argtypes = [_INT]
         L.mc2_status_str.restype = ctypes.c_char_p
@@ -178,12 +178,15 @@ def mc2_alltoall_quant_mm(chunks: Sequence[torch.Tensor], x2: torch.Tensor, x2_s
                           x2_quant_mode: int = QUANT_PERCHANNEL, out: Optional[torch.Tensor] = None,
                           q_out: Optional[torch.Tensor] = None, x1_scale_out: Optional[torch.Tensor] = None,
                           acc_out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
-                          stream=None) -> dict:
+                          alltoall_out: Optional[torch.Tensor] = None, stream=None) -> dict:
     """AlltoAllQuantMatmul on the received chunks already resident on this GPU.
 
     chunks: rank_size tensors (bs_local, h) (bf16/fp16 for mode 7, int8 for
     mode 3); x2 int8 (rank_size*h, n); x2_scale fp32 (n); bias fp32/bf16 (n).
-    Returns dict(out, q, x1_scale, acc) with the optional outputs that were given.
+    alltoall_out: optional (rank_size, bs_local, h) tensor of the chunks' dtype
+    that receives commOut (the chunks stacked, before the permute).
+    Returns dict(out, q, x1_scale, acc, alltoall_out) with the optional outputs
+    that were given.
     """
     R = len(chunks)
     bs_local, h = chunks[0].shape
@@ -199,11 +202,12 @@ def mc2_alltoall_quant_mm(chunks: Sequence[torch.Tensor], x2: torch.Tensor, x2_s
     st = lib().mc2_alltoall_quant_mm(ptrs, R, bs_local, h, _dtype_code(x1_dtype), _opt(x1_scale, "x1_scale"),
                                      _dev(x2, "x2"), _dev(x2_scale, "x2_scale"), _dev(bias, "bias"),
                                      _dtype_code(bias.dtype), x1_quant_mode, x2_quant_mode, n, _dev(out, "out"),
-                                     _opt(q_out, "q_out"), _opt(x1_scale_out, "x1_scale_out"),
-                                     _opt(acc_out, "acc_out"), _dev(workspace, "workspace"),
-                                     workspace.numel() * workspace.element_size(), _stream(stream))
+                                     _opt(alltoall_out, "alltoall_out"), _opt(q_out, "q_out"),
+                                     _opt(x1_scale_out, "x1_scale_out"), _opt(acc_out, "acc_out"),
+                                     _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+                                     _stream(stream))
     _check(st)
-    return {"out": out, "q": q_out, "x1_scale": x1_scale_out, "acc": acc_out}
+    return {"out": out, "q": q_out, "x1_scale": x1_scale_out, "acc": acc_out, "alltoall_out": alltoall_out}
 
 
 NO_ALLOC_SCRATCH_BYTES = 32 << 20
@@ -213,7 +217,8 @@ def mc2_alltoall_quant_mm_no_alloc(chunks: Sequence[torch.Tensor], x2: torch.Ten
                                    bias: torch.Tensor, *, x1_quant_mode: int, out: torch.Tensor,
                                    x1_scale: Optional[torch.Tensor] = None, x2_quant_mode: int = QUANT_PERCHANNEL,
                                    q_out: Optional[torch.Tensor] = None, x1_scale_out: Optional[torch.Tensor] = None,
-                                   acc_out: Optional[torch.Tensor] = None, stream=None) -> dict:
+                                   acc_out: Optional[torch.Tensor] = None, alltoall_out: Optional[torch.Tensor] = None,
+                                   stream=None) -> dict:
     """The same computation as mc2_alltoall_quant_mm without a workspace.
 
     For callers that cannot allocate device memory: the library's built-in
@@ -229,11 +234,11 @@ def mc2_alltoall_quant_mm_no_alloc(chunks: Sequence[torch.Tensor], x2: torch.Ten
     st = lib().mc2_alltoall_quant_mm_no_alloc(ptrs, R, bs_local, h, _dtype_code(chunks[0].dtype),
                                               _opt(x1_scale, "x1_scale"), _dev(x2, "x2"), _dev(x2_scale, "x2_scale"),
                                               _dev(bias, "bias"), _dtype_code(bias.dtype), x1_quant_mode,
-                                              x2_quant_mode, n, _dev(out, "out"), _opt(q_out, "q_out"),
-                                              _opt(x1_scale_out, "x1_scale_out"), _opt(acc_out, "acc_out"),
-                                              _stream(stream))
+                                              x2_quant_mode, n, _dev(out, "out"), _opt(alltoall_out, "alltoall_out"),
+                                              _opt(q_out, "q_out"), _opt(x1_scale_out, "x1_scale_out"),
+                                              _opt(acc_out, "acc_out"), _stream(stream))
     _check(st)
-    return {"out": out, "q": q_out, "x1_scale": x1_scale_out, "acc": acc_out}
+    return {"out": out, "q": q_out, "x1_scale": x1_scale_out, "acc": acc_out, "alltoall_out": alltoall_out}
 
 
 def mc2_device_status() -> int:

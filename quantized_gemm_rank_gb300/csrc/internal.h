@@ -33,23 +33,26 @@ int read_and_clear_gemm_status(int *status);
 int record_error(int status, const char *msg);
 
 cudaError_t launch_quant_pertoken(const ChunkPtrs &chunks, int rank_size, int64_t bs_local, int h, bool bf16,
-                                  const void *smooth, __half *qh, int8_t *q_out, float *scale_out, int num_sms,
-                                  cudaStream_t stream);
+                                  const void *smooth, __half *qh, int8_t *q_out, float *scale_out, void *comm_out,
+                                  int num_sms, cudaStream_t stream);
 // One launch doing both the per-token dynamic quant and the x2 widening
 // (h % 8 == 0 and rank_size*h <= 32768, see a2a_prologue_fits).  Also sets
 // zero_words[0, n_zero) to 0.
 bool a2a_prologue_fits(int rank_size, int64_t bs_local, int h);
 cudaError_t launch_a2a_prologue(const ChunkPtrs &chunks, int rank_size, int64_t bs_local, int h, bool bf16,
                                 const void *smooth, __half *qh, int8_t *q_out, float *scale_out, const int8_t *x2,
-                                __half *x2h, int64_t x2_count, int *zero_words, int n_zero, cudaStream_t stream);
+                                __half *x2h, int64_t x2_count, int *zero_words, int n_zero, void *comm_out,
+                                cudaStream_t stream);
 // Also sets zero_words[0, n_zero) to 0 (the GEMM's stream-K counters).
 cudaError_t launch_widen_i8(const int8_t *src, __half *dst, int64_t count, int num_sms, int *zero_words, int n_zero,
                             cudaStream_t stream);
 // Widens each rank's int8 chunk to fp16 in its own layout at dst + r*bs_local*h
 // (h % 16 == 0); q_out (optional) receives the permuted int8 matrix.
 cudaError_t launch_widen_chunks_i8(const ChunkPtrs &chunks, int rank_size, int64_t bs_local, int h, __half *dst,
-                                   int8_t *q_out, int num_sms, cudaStream_t stream);
+                                   int8_t *q_out, int8_t *comm_out, int num_sms, cudaStream_t stream);
 cudaError_t launch_permute_widen_i8(const ChunkPtrs &chunks, int rank_size, int64_t bs_local, int h, __half *dst,
-                                    int8_t *q_out, int num_sms, cudaStream_t stream);
+                                    int8_t *q_out, int8_t *comm_out, int num_sms, cudaStream_t stream);
+// comm_out (optional, NULL for none): the received chunks stacked as
+// (rank_size, bs_local, h) in their own dtype, written by the kernel that reads them.
 
 }  // namespace mc2

@@ -325,7 +325,7 @@ int mc2_alltoall_quant_mm_workspace(int rank_size, int64_t bs_local, int64_t h, 
 int mc2_alltoall_quant_mm(const void *const *chunks, int rank_size, int64_t bs_local, int64_t h, int x1_dtype,
                           const void *x1_scale, const int8_t *x2, const float *x2_scale, const void *bias,
                           int bias_dtype, int x1_quant_mode, int x2_quant_mode, int64_t n, void *out,
-                          int8_t *q_out, float *x1_scale_out, int32_t *acc_out, void *workspace,
+                          void *alltoall_out, int8_t *q_out, float *x1_scale_out, int32_t *acc_out, void *workspace,
                           size_t workspace_bytes, void *stream) {
     g_last_error[0] = '\0';
     if (!chunks) return fail(MC2_ERR_NULL, "chunks is NULL");
@@ -346,7 +346,7 @@ int mc2_alltoall_quant_mm(const void *const *chunks, int rank_size, int64_t bs_l
         if (!aligned16(chunks[r])) return fail(MC2_ERR_UNSUPPORTED, "chunks[%d] is not 16-byte aligned", r);
     if (!aligned16(x2) || !aligned16(out) || !aligned16(x2_scale) || !aligned16(bias) ||
         (x1_scale && !aligned16(x1_scale)) || (q_out && !aligned16(q_out)) || (acc_out && !aligned16(acc_out)) ||
-        (x1_scale_out && !aligned16(x1_scale_out)))
+        (x1_scale_out && !aligned16(x1_scale_out)) || (alltoall_out && !aligned16(alltoall_out)))
         return fail(MC2_ERR_UNSUPPORTED, "all tensors must be 16-byte aligned");
     const A2AWorkspace ws = a2a_layout(rank_size, bs_local, h, n);
     if (!workspace || workspace_bytes < ws.total)
@@ -383,17 +383,19 @@ int mc2_alltoall_quant_mm(const void *const *chunks, int rank_size, int64_t bs_l
     bool x2_done = false;
     if (x1_quant_mode == MC2_QUANT_PERTOKEN_DYNAMIC && mc2::a2a_prologue_fits(rank_size, bs_local, static_cast<int>(h))) {
         e = mc2::launch_a2a_prologue(cp, rank_size, bs_local, static_cast<int>(h), x1_dtype == MC2_BF16, x1_scale, ah,
-                                     q_out, scale, x2, x2h, K * n, sk_flags, n_flags, s);
+                                     q_out, scale, x2, x2h, K * n, sk_flags, n_flags, alltoall_out, s);
         x2_done = true;
     } else if (x1_quant_mode == MC2_QUANT_PERTOKEN_DYNAMIC) {
         e = mc2::launch_quant_pertoken(cp, rank_size, bs_local, static_cast<int>(h), x1_dtype == MC2_BF16, x1_scale,
-                                       ah, q_out, scale, dev.num_sms, s);
+                                       ah, q_out, scale, alltoall_out, dev.num_sms, s);
     } else {
         // mode 3: the scales are the caller's; the int8 chunks are widened
         if (a_by_chunk)
-            e = mc2::launch_widen_chunks_i8(cp, rank_size, bs_local, static_cast<int>(h), ah, q_out, dev.num_sms, s);
+            e = mc2::launch_widen_chunks_i8(cp, rank_size, bs_local, static_cast<int>(h), ah, q_out,
+                                            static_cast<int8_t *>(alltoall_out), dev.num_sms, s);
         else
-            e = mc2::launch_permute_widen_i8(cp, rank_size, bs_local, static_cast<int>(h), ah, q_out, dev.num_sms, s);
+            e = mc2::launch_permute_widen_i8(cp, rank_size, bs_local, static_cast<int>(h), ah, q_out,
+                                             static_cast<int8_t *>(alltoall_out), dev.num_sms, s);
         if (e == cudaSuccess && x1_scale_out)
             e = cudaMemcpyAsync(x1_scale_out, x1_scale, static_cast<size_t>(bs_local) * 4, cudaMemcpyDeviceToDevice, s);
         scale = const_cast<float *>(static_cast<const float *>(x1_scale));

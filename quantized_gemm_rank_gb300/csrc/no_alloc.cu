@@ -71,7 +71,8 @@ extern "C" int mc2_alltoall_quant_mm_no_alloc(const void *const *chunks, int ran
                                               int64_t h, int x1_dtype, const void *x1_scale, const int8_t *x2,
                                               const float *x2_scale, const void *bias, int bias_dtype,
                                               int x1_quant_mode, int x2_quant_mode, int64_t n, void *out,
-                                              int8_t *q_out, float *x1_scale_out, int32_t *acc_out, void *stream) {
+                                              void *alltoall_out, int8_t *q_out, float *x1_scale_out,
+                                              int32_t *acc_out, void *stream) {
     // Sizes are checked (and the scratch need computed) on the host first, so a
     // request that does not fit is refused before any device work.
     size_t need = 0;
@@ -88,6 +89,6 @@ extern "C" int mc2_alltoall_quant_mm_no_alloc(const void *const *chunks, int ran
     st = scratch_for_current_device(&scratch);
     if (st != MC2_OK) return st;
     return mc2_alltoall_quant_mm(chunks, rank_size, bs_local, h, x1_dtype, x1_scale, x2, x2_scale, bias, bias_dtype,
-                                 x1_quant_mode, x2_quant_mode, n, out, q_out, x1_scale_out, acc_out, scratch,
+                                 x1_quant_mode, x2_quant_mode, n, out, alltoall_out, q_out, x1_scale_out, acc_out, scratch,
                                  kMaxScratchBytes, stream);
 }

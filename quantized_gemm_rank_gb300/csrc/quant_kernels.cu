@@ -5,7 +5,10 @@
 //     (permuted[t, r*h + j] = chunk_r[t, j]) without materialising the
 //     permuted bf16/fp16 matrix;
 //   * the exact int8 -> fp16 widening of the int8 operands that the tensor
-//     cores consume (sm_103a has no integer tcgen05 MMA).
+//     cores consume (sm_103a has no integer tcgen05 MMA);
+//   * the optional alltoAllOut output (commOut, the rank_size received blocks
+//     stacked as (rank_size, bs_local, h) in x1's dtype), stored from the same
+//     registers that read the chunks.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -59,7 +62,8 @@ template <bool kBF16>
 __global__ void __launch_bounds__(256) quant_pertoken_kernel(const __grid_constant__ ChunkPtrs chunks, int h, int64_t bs_local, int rank_size,
                                                              const uint16_t *__restrict__ smooth,
                                                              __half *__restrict__ qh, int8_t *__restrict__ q_out,
-                                                             float *__restrict__ scale_out) {
+                                                             float *__restrict__ scale_out,
+                                                             uint16_t *__restrict__ comm_out) {
     ptx::allow_dependent_launch();
     __shared__ float red[32];
     const int K = rank_size * h;
@@ -73,6 +77,7 @@ __global__ void __launch_bounds__(256) quant_pertoken_kernel(const __grid_consta
                 const int j = c - r * h;
                 const uint4 xv = __ldg(reinterpret_cast<const uint4 *>(
                     static_cast<const uint16_t *>(chunks.p[r]) + t * h + j));
+                if (comm_out) *reinterpret_cast<uint4 *>(comm_out + (r * bs_local + t) * h + j) = xv;
                 uint4 sv = make_uint4(0, 0, 0, 0);
                 if (smooth) sv = __ldg(reinterpret_cast<const uint4 *>(smooth + c));
                 const uint16_t *xe = reinterpret_cast<const uint16_t *>(&xv);
@@ -88,7 +93,9 @@ __global__ void __launch_bounds__(256) quant_pertoken_kernel(const __grid_consta
             for (int c = threadIdx.x; c < K; c += blockDim.x) {
                 const int r = c / h;
                 const int j = c - r * h;
-                const float x = to_f32<kBF16>(static_cast<const uint16_t *>(chunks.p[r])[t * h + j]);
+                const uint16_t xr = static_cast<const uint16_t *>(chunks.p[r])[t * h + j];
+                if (comm_out) comm_out[(r * bs_local + t) * h + j] = xr;
+                const float x = to_f32<kBF16>(xr);
                 const float y = smooth ? __fmul_rn(x, to_f32<kBF16>(smooth[c])) : x;
                 amax = fmaxf(amax, fabsf(y));
             }
@@ -182,7 +189,7 @@ __global__ void __launch_bounds__(512) a2a_prologue_kernel(const __grid_constant
                                                            const int8_t *__restrict__ x2,
                                                            __half *__restrict__ x2h, int64_t x2_vecs,
                                                            int64_t widen_ctas, int *__restrict__ zero_words,
-                                                           int n_zero) {
+                                                           int n_zero, uint16_t *__restrict__ comm_out) {
     ptx::allow_dependent_launch();
     const int64_t b = blockIdx.x;
     // the GEMM's stream-K counters start at zero (it runs after this kernel)
@@ -235,6 +242,19 @@ __global__ void __launch_bounds__(512) a2a_prologue_kernel(const __grid_constant
             const int r = c / h;
             xv[v] = __ldg(reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(chunks.p[r]) + t * h +
                                                           (c - r * h)));
+        }
+    }
+    // commOut, once every load of the row is in flight (a store right after each
+    // load would wait for it before the next load issues)
+    if (comm_out) {
+#pragma unroll
+        for (int v = 0; v < kV; ++v) {
+            const int vi = v * blockDim.x + threadIdx.x;
+            if (vi < nvec) {
+                const int c = vi * 8;
+                const int r = c / h;
+                *reinterpret_cast<uint4 *>(comm_out + (r * bs_local + t) * h + (c - r * h)) = xv[v];
+            }
         }
     }
     // y = x * s (fp32, exact for 16-bit inputs); row absmax
@@ -331,7 +351,8 @@ __global__ void __launch_bounds__(256) widen_i8_kernel(const int8_t *__restrict_
 // h % 16 == 0.
 __global__ void __launch_bounds__(256) widen_chunks_i8_kernel(const __grid_constant__ ChunkPtrs chunks, int h,
                                                               int64_t bs_local, int rank_size,
-                                                              __half *__restrict__ dst, int8_t *__restrict__ q_out) {
+                                                              __half *__restrict__ dst, int8_t *__restrict__ q_out,
+                                                              int8_t *__restrict__ comm_out) {
     ptx::allow_dependent_launch();
     const int64_t per_chunk = bs_local * h / 16;  // 16-element vectors per chunk
     const int64_t total = per_chunk * rank_size;
@@ -350,6 +371,8 @@ __global__ void __launch_bounds__(256) widen_chunks_i8_kernel(const __grid_const
         uint4 *d = reinterpret_cast<uint4 *>(dst) + 2 * i;
         d[0] = o[0];
         d[1] = o[1];
+        // commOut (rank_size, bs_local, h) is the chunks back to back: vector i
+        if (comm_out) reinterpret_cast<int4 *>(comm_out)[i] = v;
         if (q_out) {
             const int64_t t = li / vpr;
             const int j = static_cast<int>(li - t * vpr) * 16;
@@ -362,7 +385,8 @@ __global__ void __launch_bounds__(256) widen_chunks_i8_kernel(const __grid_const
 // permuted matrix): dst[t, r*h + j] = chunk_r[t, j].
 __global__ void __launch_bounds__(256) permute_widen_i8_kernel(const __grid_constant__ ChunkPtrs chunks, int h, int64_t bs_local,
                                                                int rank_size, __half *__restrict__ dst,
-                                                               int8_t *__restrict__ q_out) {
+                                                               int8_t *__restrict__ q_out,
+                                                               int8_t *__restrict__ comm_out) {
     ptx::allow_dependent_launch();
     const int K = rank_size * h;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -384,6 +408,7 @@ __global__ void __launch_bounds__(256) permute_widen_i8_kernel(const __grid_cons
             d[0] = o[0];
             d[1] = o[1];
             if (q_out) *reinterpret_cast<int4 *>(q_out + t * K + c) = v;
+            if (comm_out) *reinterpret_cast<int4 *>(comm_out + (r * bs_local + t) * h + j) = v;
         }
     } else {
         const int64_t total = bs_local * K;
@@ -395,6 +420,7 @@ __global__ void __launch_bounds__(256) permute_widen_i8_kernel(const __grid_cons
             const int8_t v = static_cast<const int8_t *>(chunks.p[r])[t * h + j];
             dst[i] = __int2half_rn(v);
             if (q_out) q_out[i] = v;
+            if (comm_out) comm_out[(r * bs_local + t) * h + j] = v;
         }
     }
 }
@@ -410,17 +436,18 @@ int grid_for(int64_t work_items, int threads, int num_sms) {
 }  // namespace
 
 cudaError_t launch_quant_pertoken(const ChunkPtrs &chunks, int rank_size, int64_t bs_local, int h, bool bf16,
-                                  const void *smooth, __half *qh, int8_t *q_out, float *scale_out, int num_sms,
-                                  cudaStream_t stream) {
+                                  const void *smooth, __half *qh, int8_t *q_out, float *scale_out, void *comm_out,
+                                  int num_sms, cudaStream_t stream) {
+    uint16_t *co = static_cast<uint16_t *>(comm_out);
     const uint16_t *sm = static_cast<const uint16_t *>(smooth);
     const int64_t rows_cap = static_cast<int64_t>(num_sms) * 64;
     const int grid = static_cast<int>(bs_local < rows_cap ? bs_local : rows_cap);
     if (bf16)
         quant_pertoken_kernel<true><<<grid, 256, 0, stream>>>(chunks, h, bs_local, rank_size, sm, qh, q_out,
-                                                              scale_out);
+                                                              scale_out, co);
     else
         quant_pertoken_kernel<false><<<grid, 256, 0, stream>>>(chunks, h, bs_local, rank_size, sm, qh, q_out,
-                                                               scale_out);
+                                                               scale_out, co);
     return cudaGetLastError();
 }
 
@@ -430,7 +457,9 @@ bool a2a_prologue_fits(int rank_size, int64_t bs_local, int h) {
 
 cudaError_t launch_a2a_prologue(const ChunkPtrs &chunks, int rank_size, int64_t bs_local, int h, bool bf16,
                                 const void *smooth, __half *qh, int8_t *q_out, float *scale_out, const int8_t *x2,
-                                __half *x2h, int64_t x2_count, int *zero_words, int n_zero, cudaStream_t stream) {
+                                __half *x2h, int64_t x2_count, int *zero_words, int n_zero, void *comm_out,
+                                cudaStream_t stream) {
+    uint16_t *co = static_cast<uint16_t *>(comm_out);
     constexpr int kV = 8;
     const int K = rank_size * h;
     int threads = 64;
@@ -445,11 +474,11 @@ cudaError_t launch_a2a_prologue(const ChunkPtrs &chunks, int rank_size, int64_t 
     if (bf16)
         a2a_prologue_kernel<true, kV><<<static_cast<unsigned>(grid), threads, 0, stream>>>(
             chunks, h, bs_local, rank_size, sm, qh, q_out, scale_out, x2, x2h, x2_vecs, widen_ctas, zero_words,
-            n_zero);
+            n_zero, co);
     else
         a2a_prologue_kernel<false, kV><<<static_cast<unsigned>(grid), threads, 0, stream>>>(
             chunks, h, bs_local, rank_size, sm, qh, q_out, scale_out, x2, x2h, x2_vecs, widen_ctas, zero_words,
-            n_zero);
+            n_zero, co);
     return cudaGetLastError();
 }
 
@@ -460,18 +489,18 @@ cudaError_t launch_widen_i8(const int8_t *src, __half *dst, int64_t count, int n
 }
 
 cudaError_t launch_widen_chunks_i8(const ChunkPtrs &chunks, int rank_size, int64_t bs_local, int h, __half *dst,
-                                   int8_t *q_out, int num_sms, cudaStream_t stream) {
+                                   int8_t *q_out, int8_t *comm_out, int num_sms, cudaStream_t stream) {
     const int64_t items = bs_local * static_cast<int64_t>(rank_size) * h / 16;
     widen_chunks_i8_kernel<<<grid_for(items, 256, num_sms), 256, 0, stream>>>(chunks, h, bs_local, rank_size, dst,
-                                                                             q_out);
+                                                                             q_out, comm_out);
     return cudaGetLastError();
 }
 
 cudaError_t launch_permute_widen_i8(const ChunkPtrs &chunks, int rank_size, int64_t bs_local, int h, __half *dst,
-                                    int8_t *q_out, int num_sms, cudaStream_t stream) {
+                                    int8_t *q_out, int8_t *comm_out, int num_sms, cudaStream_t stream) {
     const int64_t items = bs_local * static_cast<int64_t>(rank_size) * h / ((h % 16 == 0) ? 16 : 1);
     permute_widen_i8_kernel<<<grid_for(items, 256, num_sms), 256, 0, stream>>>(chunks, h, bs_local, rank_size, dst,
-                                                                              q_out);
+                                                                              q_out, comm_out);
     return cudaGetLastError();
 }
 

@@ -142,12 +142,13 @@ def test_matmul_reduce_scatter_bounds_accepted_by_validation():
 
 def a2a_call(rank_size=2, bs_local=16, h=64, x1_dtype=mc2.MC2_BF16, x1_scale=None, x2=FAKE, x2_scale=FAKE,
              bias=FAKE, bias_dtype=mc2.MC2_F32, mode=7, mode2=2, n=64, out=FAKE, ws=FAKE, ws_bytes=1 << 40,
-             chunks=None):
+             chunks=None, a2a_out=None):
     if chunks is None:
         chunks = [FAKE] * max(rank_size, 1)
     arr = (ctypes.c_void_p * len(chunks))(*chunks)
     return mc2.lib().mc2_alltoall_quant_mm(arr, rank_size, bs_local, h, x1_dtype, x1_scale, x2, x2_scale, bias,
-                                           bias_dtype, mode, mode2, n, out, None, None, None, ws, ws_bytes, None)
+                                           bias_dtype, mode, mode2, n, out, a2a_out, None, None, None, ws, ws_bytes,
+                                           None)
 
 
 @pytest.mark.parametrize("kw,status", [
@@ -176,6 +177,7 @@ def a2a_call(rank_size=2, bs_local=16, h=64, x1_dtype=mc2.MC2_BF16, x1_scale=Non
     (dict(ws_bytes=16), mc2.MC2_ERR_WORKSPACE),
     (dict(n=40), mc2.MC2_ERR_UNSUPPORTED),
     (dict(out=FAKE + 4), mc2.MC2_ERR_UNSUPPORTED),
+    (dict(a2a_out=FAKE + 8), mc2.MC2_ERR_UNSUPPORTED),
 ])
 def test_alltoall_rejects(kw, status):
     assert a2a_call(**kw) == status, mc2.last_error()

@@ -138,6 +138,41 @@ def test_without_debug_outputs_matches():
     assert_bits_equal(a["out"], b["out"], "out with/without debug outputs")
 
 
+@pytest.mark.parametrize("name", ["dyn-bf16-ragged", "dyn-fp16-scalar-h", "full-int8-ragged", "full-int8-scalar-h",
+                                  "full-int8-3kblocks"])
+def test_alltoall_out_is_comm_out(name):
+    """alltoAllOut (commOut): every received chunk as block r, bit for bit, and
+    the main outputs unchanged by asking for it."""
+    shape = CASES[name]
+    inp = mc2_inputs.a2a_inputs(shape, seed=17)
+    dev = torch.device("cuda")
+    chunks = [c.to(dev) for c in inp["chunks"]]
+    x1s = None if inp["x1_scale"] is None else inp["x1_scale"].to(dev)
+    args = (chunks, inp["x2"].to(dev), inp["x2_scale"].to(dev), inp["bias"].to(dev))
+    co = torch.full((shape.rank_size, shape.bs_local, shape.h), 7, dtype=chunks[0].dtype, device=dev)
+    a = mc2.mc2_alltoall_quant_mm(*args, x1_quant_mode=shape.quant_mode, x1_scale=x1s, alltoall_out=co)
+    b = mc2.mc2_alltoall_quant_mm(*args, x1_quant_mode=shape.quant_mode, x1_scale=x1s)
+    torch.cuda.synchronize()
+    assert mc2.mc2_device_status() == mc2.MC2_OK
+    assert_bits_equal(co.cpu(), oracle.comm_out(inp["chunks"]), f"{name}: alltoall_out")
+    assert_bits_equal(a["out"].cpu(), b["out"].cpu(), f"{name}: out with/without alltoall_out")
+    ref = run_oracle(inp, shape)
+    assert_bits_equal(a["out"].cpu(), ref["out"], f"{name}: out")
+
+
+def test_alltoall_out_full_size_dynamic():
+    shape = mc2_inputs.WORKLOADS["a2a-dyn"]
+    inp = mc2_inputs.a2a_inputs(shape, seed=0)
+    dev = torch.device("cuda")
+    chunks = [c.to(dev) for c in inp["chunks"]]
+    co = torch.empty((shape.rank_size, shape.bs_local, shape.h), dtype=chunks[0].dtype, device=dev)
+    mc2.mc2_alltoall_quant_mm(chunks, inp["x2"].to(dev), inp["x2_scale"].to(dev), inp["bias"].to(dev),
+                              x1_quant_mode=7, x1_scale=inp["x1_scale"].to(dev), alltoall_out=co)
+    torch.cuda.synchronize()
+    assert mc2.mc2_device_status() == mc2.MC2_OK
+    assert_bits_equal(co.cpu(), oracle.comm_out(inp["chunks"]), "a2a-dyn: alltoall_out")
+
+
 def test_quant_ties_and_near_ties_on_gpu():
     """Exact half-integer quotients (scale 1: every k + 0.5 for k in [-126, 125]),
     values a few bf16 ulps around them, and the hand-derived golden rows: the GPU

@@ -1,6 +1,7 @@
 """Pins for the AlltoAllQuantMatmul oracle ("aclnnAlltoAllQuantMatmul", 计算公式).
 
 * permute: brute-force index tracing of AlltoAll + permute(1,0,2) + view with torch
+* commOut (alltoAllOut): the same tracing, element by element from each rank's x1
 * quant: hand-derived rows (ties, smooth scale, zero row), and closed-form
   properties on random rows: max|q| = 127, |q*scale - y| <= scale/2
 * int8 matmul: numpy's integer matmul, the all-127 accumulator bound, overflow
@@ -52,6 +53,32 @@ def test_permute_index_tracing(R, elem):
         sub = oracle.permute(chunks if elem == torch.int8 else [c.view(torch.bfloat16) for c in chunks],
                              rows=[3, 0])
         assert torch.equal(sub.view(elem), want[[3, 0]])
+
+
+@pytest.mark.parametrize("R", [2, 4, 8])
+@pytest.mark.parametrize("elem", [torch.int16, torch.int8])
+def test_comm_out_index_tracing(R, elem):
+    """commOut on rank j, traced element by element with Python loops from
+    every rank's x1 (BS, H): rank r sends rows [j*BS/R, (j+1)*BS/R) of its x1
+    to rank j, which stores them as block r."""
+    BS, H = 2 * R, 5
+    x1 = [torch.tensor([[(r * 53 + i * 7 + h * 3) % 251 - 125 for h in range(H)] for i in range(BS)],
+                       dtype=elem) for r in range(R)]
+    for j in range(R):
+        want = torch.empty((R, BS // R, H), dtype=elem)
+        for r in range(R):
+            for t in range(BS // R):
+                for h in range(H):
+                    want[r, t, h] = x1[r][j * (BS // R) + t, h]
+        chunks = [x1[r][j * (BS // R):(j + 1) * (BS // R)].contiguous() for r in range(R)]
+        if elem == torch.int16:
+            got = oracle.comm_out([c.view(torch.bfloat16) for c in chunks]).view(torch.int16)
+        else:
+            got = oracle.comm_out(chunks)
+        assert torch.equal(got, want)
+        # and its permute(1, 0, 2).view is the permuted matrix
+        P = oracle.permute(chunks if elem == torch.int8 else [c.view(torch.bfloat16) for c in chunks])
+        assert torch.equal(got.permute(1, 0, 2).reshape(BS // R, R * H), P.view(elem))
 
 
 def test_quant_golden_rows():

@@ -68,6 +68,6 @@ def test_no_alloc_refuses_sizes_beyond_its_scratch():
     fake = 0x10000
     arr = (ctypes.c_void_p * 8)(*([fake] * 8))
     st = mc2.lib().mc2_alltoall_quant_mm_no_alloc(arr, 8, s.bs_local, s.h, mc2.MC2_BF16, None, fake, fake, fake,
-                                                  mc2.MC2_F32, 7, 2, s.n, fake, None, None, None, None)
+                                                  mc2.MC2_F32, 7, 2, s.n, fake, None, None, None, None, None)
     assert st == mc2.MC2_ERR_WORKSPACE
     assert "built-in scratch" in mc2.last_error()
