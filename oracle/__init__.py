@@ -63,6 +63,7 @@ def _load():
         lib.oracle_all_gather_mm.argtypes = [_P, _INT, _I64, _I64, _P, _I64, _INT, _P, _INT, _P, _I64, _P]
         lib.oracle_permute.argtypes = [_P, _INT, _I64, _I64, _INT, _P, _I64, _P]
         lib.oracle_comm_out.argtypes = [_P, _INT, _I64, _I64, _INT, _P]
+        lib.oracle_matmul_weight_grad.argtypes = [_P, _P, _I64, _I64, _I64, _INT, _P, _I64, _P, _P]
         lib.oracle_quant_pertoken_dynamic.argtypes = [_P, _I64, _I64, _P, _INT, _P, _P]
         lib.oracle_int8_mm.argtypes = [_P, _I64, _I64, _P, _I64, _P]
         lib.oracle_dequant.argtypes = [_P, _I64, _I64, _P, _P, _P, _P]
@@ -179,6 +180,23 @@ def matmul_reduce_scatter(x_chunks: Sequence[torch.Tensor], w_chunks: Sequence[t
                                               int(w_is_nk), _ptr(b), isb, _ptr(r), nr, out.data_ptr())
     _check(rc, "matmul_reduce_scatter")
     return out
+
+
+def matmul_weight_grad(dy: torch.Tensor, x: torch.Tensor, *, rows=None, with_bias: bool = True):
+    """dW = dY^T @ X (n, k) (or only ``rows`` of it) and dB = sum_t dY[t, :] (n)
+    or None; dY (m, n) and X (m, k) of one 16-bit type.  Returns (dw, db)."""
+    d = _c(dy)
+    xx = _c(x)
+    m, n = d.shape
+    k = xx.shape[1]
+    isb = _is_bf16(d.dtype)
+    r, nr = _rows_arg(rows)
+    dw = torch.empty((nr if r is not None else n, k), dtype=d.dtype)
+    db = torch.empty((n,), dtype=d.dtype) if with_bias else None
+    rc = _load().oracle_matmul_weight_grad(d.data_ptr(), xx.data_ptr(), m, n, k, isb, _ptr(r), nr,
+                                           dw.data_ptr(), _ptr(db))
+    _check(rc, "matmul_weight_grad")
+    return dw, db
 
 
 # --------------------------------------------------------------------------- AlltoAllQuantMatmul

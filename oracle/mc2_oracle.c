@@ -453,3 +453,61 @@ int oracle_matmul_reduce_scatter(const uint16_t *const *x_chunks, const uint16_t
     free(tab);
     return OR_OK;
 }
+
+/* ------------------------------------------------------------------------ */
+/* [MC2] Weight and bias gradients of the fused linear layers                 */
+/* ("hyper_parallel .../mc2.py": module docstring, dW = dY^T @ AllGather_m(X) */
+/* for all_gather_matmul and dW = AllGather_m(dY)^T @ X for                    */
+/* matmul_reduce_scatter; AllGatherMatmulFunction.backward: grad_w =          */
+/* grad_out.t().matmul(gathered), grad_bias = grad_out.sum(dim=0)).            */
+/*   dw[i, j] = sum_t dy[t, i] * x[t, j]     dy (m, n), x (m, k), dw (n, k)    */
+/*   db[i]    = sum_t dy[t, i]                                   db (n)        */
+/* Reading: both sums exact (fp64 here, ascending t) and rounded once to the   */
+/* operand type.  dw is computed for the requested rows i (all when rows is    */
+/* NULL) into dw (n_rows, k); db (all n) when db is non-NULL.                  */
+/* ------------------------------------------------------------------------ */
+int oracle_matmul_weight_grad(const uint16_t *dy, const uint16_t *x, int64_t m, int64_t n, int64_t k, int is_bf16,
+                              const int64_t *rows, int64_t n_rows, uint16_t *dw, uint16_t *db) {
+    if (!dy || !x || m < 1 || n < 1 || k < 1) return OR_ERR_ARG;
+    if (!rows) n_rows = n;
+    if (n_rows > 0 && !dw) return OR_ERR_ARG;
+    for (int64_t ii = 0; ii < n_rows; ++ii) {
+        int64_t i = rows ? rows[ii] : ii;
+        if (i < 0 || i >= n) return OR_ERR_ARG;
+    }
+    float *tab = (float *)malloc(65536 * sizeof(float));
+    if (!tab) return OR_ERR_NOMEM;
+    build_decode_table(is_bf16, tab);
+    int err = OR_OK;
+#pragma omp parallel
+    {
+        double *acc = (double *)malloc((size_t)k * sizeof(double));
+        if (!acc) {
+#pragma omp atomic write
+            err = OR_ERR_NOMEM;
+        }
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t ii = 0; ii < n_rows; ++ii) {
+            if (!acc) continue;
+            int64_t i = rows ? rows[ii] : ii;
+            for (int64_t j = 0; j < k; ++j) acc[j] = 0.0;
+            for (int64_t t = 0; t < m; ++t) {
+                double a = (double)tab[dy[t * n + i]];     /* dY^T[i, t] = dY[t, i] */
+                const uint16_t *xrow = x + t * k;
+                for (int64_t j = 0; j < k; ++j) acc[j] += a * (double)tab[xrow[j]];
+            }
+            for (int64_t j = 0; j < k; ++j) dw[ii * k + j] = oracle_encode16_rne(acc[j], is_bf16);
+        }
+        free(acc);
+    }
+    if (err == OR_OK && db) {
+#pragma omp parallel for
+        for (int64_t i = 0; i < n; ++i) {
+            double s = 0.0;
+            for (int64_t t = 0; t < m; ++t) s += (double)tab[dy[t * n + i]];
+            db[i] = oracle_encode16_rne(s, is_bf16);
+        }
+    }
+    free(tab);
+    return err;
+}
