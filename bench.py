@@ -364,6 +364,14 @@ def extra_table(dev, flush, stream, steps):
             g = torch.empty((s.m, s.k), dtype=s.dtype, device=dev)
             fn = lambda: mc2.mc2_all_gather_mm(ch, x2, x2_is_nk=s.x2_is_nk, bias=b, out=out, gathered=g)  # noqa
             fl = s.flops
+        elif isinstance(s, mc2_inputs.WGradShape):
+            inp = mc2_inputs.wgrad_inputs(s, seed=0)
+            ch = inp["dy"].to(dev)
+            wc = inp["x"].to(dev)
+            dwo = torch.empty((s.n, s.k), dtype=s.dtype, device=dev)
+            dbo = torch.empty((s.n,), dtype=s.dtype, device=dev)
+            fn = lambda: mc2.mc2_matmul_weight_grad(ch, wc, dw=dwo, db=dbo)  # noqa
+            fl = s.flops
         elif isinstance(s, mc2_inputs.MMRSShape):
             inp = mc2_inputs.mmrs_inputs(s, seed=0)
             ch = [x.to(dev) for x in inp["x_chunks"]]

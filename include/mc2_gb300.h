@@ -120,6 +120,30 @@ int mc2_matmul_reduce_scatter(const void *const *x_chunks, const void *const *w_
                               void *const *out_chunks, void *stream);
 
 /*
+ * Weight and bias gradients of the fused linear layers  (hyper_parallel
+ * mc2.py, module docstring: all_gather_matmul backward dW = dY^T @
+ * AllGather_m(X), matmul_reduce_scatter backward dW = AllGather_m(dY)^T @ X;
+ * AllGatherMatmulFunction.backward: grad_w = grad_out.t().matmul(gathered),
+ * grad_bias = grad_out.sum(dim=0)).  The all-gathered operand is the one the
+ * forward call returned (the `gathered` output of mc2_all_gather_mm).
+ *
+ *   dw[i, j] = sum_t dy[t, i] * x[t, j]        (n, k), the nn.Linear weight layout
+ *   db[i]    = sum_t dy[t, i]                  (n)
+ *
+ *   Both sums are accumulated in fp32 (dw in blocks of 1024 rows summed in fp32
+ *   registers) and rounded once (nearest-even) to `dtype`.
+ *
+ *   dy     (m, n) row-major          x    (m, k) row-major
+ *   dw     (n, k) row-major          db   NULL or (n)
+ *   dtype  MC2_F16 or MC2_BF16 for every tensor
+ *   m, n, k >= 1 and <= INT32_MAX  (this kernel: n % 8 == 0, k % 8 == 0)
+ *
+ * Returns MC2_OK or a negative mc2_status; nothing is launched on error.
+ */
+int mc2_matmul_weight_grad(const void *dy, int64_t m, int64_t n, const void *x, int64_t k, int dtype, void *dw,
+                           void *db, void *stream);
+
+/*
  * Workspace size (bytes) that mc2_alltoall_quant_mm needs for these sizes.
  * Same argument meanings and validation as mc2_alltoall_quant_mm.
  */

@@ -27,6 +27,10 @@ Workloads (names used throughout the repository):
              ~N(0,1) and nn.Linear weight shards w_r (8192, 2048)
              ~N(0, std K^-1/2) with K = 8192 the unsharded contraction, no
              bias: the row-parallel dual of ag-4x4096.
+  wgrad-ag-4x4096  weight/bias gradient of the ag-4x4096 layer: dY (16384, 7168)
+             bf16 ~N(0, std m^-1/2) (the gradient of a token-mean loss, so that
+             dW ~ N(0, 1)), gathered X (16384, 8192) bf16 ~N(0,1) -> dW (7168, 8192),
+             dB (7168).
   a2a-full   AlltoAllQuantMatmul, quant mode 3 (pre-quantised int8), 8 ranks x
              (16384, 4096) int8 uniform on [-127, 127], per-token x1 scale
              (16384) fp32 ~U(1e-3, 1e-2), x2 int8 (32768, 7168), x2 scale
@@ -107,6 +111,20 @@ class MMRSShape:
         return 2.0 * self.m * self.n * self.k
 
 
+@dataclass(frozen=True)
+class WGradShape:
+    m: int                          # rows of dY and X: the contraction (all gathered tokens)
+    n: int                          # output features (rows of dW)
+    k: int                          # input features (columns of dW)
+    dtype: torch.dtype = torch.bfloat16
+    dy_std: Optional[float] = None  # None: m ** -0.5 (a token-mean loss), so dW ~ N(0, 1)
+    x_std: float = 1.0
+
+    @property
+    def flops(self) -> float:
+        return 2.0 * self.m * self.n * self.k
+
+
 WORKLOADS = {
     "ag-tiny": AGShape(world_size=8, m_local=16, k=512, n=64, dtype=torch.float16, w_std=1.0),
     "ag-8x1024": AGShape(world_size=8, m_local=1024, k=4096, n=4096),
@@ -115,6 +133,7 @@ WORKLOADS = {
     "a2a-dyn-small": A2AShape(rank_size=8, bs_local=512, h=1024, n=4096, quant_mode=7),
     "a2a-full": A2AShape(rank_size=8, bs_local=16384, h=4096, n=7168, quant_mode=3),
     "mmrs-4x2048": MMRSShape(world_size=4, m=16384, k_local=2048, n=8192),
+    "wgrad-ag-4x4096": WGradShape(m=16384, n=7168, k=8192),
 }
 
 
@@ -155,6 +174,15 @@ def mmrs_inputs(s: MMRSShape, seed: int = 0) -> dict:
     ws = [(torch.randn(*wshape, generator=g) * w_std).to(s.dtype) for _ in range(s.world_size)]
     bias = (torch.randn(s.n, generator=g) * s.bias_std).to(s.dtype) if s.bias else None
     return {"x_chunks": xs, "w_chunks": ws, "bias": bias}
+
+
+def wgrad_inputs(s: WGradShape, seed: int = 0) -> dict:
+    """dy (m, n), x (m, k)."""
+    g = _gen(seed)
+    dy_std = s.m ** -0.5 if s.dy_std is None else s.dy_std
+    dy = (torch.randn(s.m, s.n, generator=g) * dy_std).to(s.dtype)
+    x = (torch.randn(s.m, s.k, generator=g) * s.x_std).to(s.dtype)
+    return {"dy": dy, "x": x}
 
 
 def a2a_inputs(s: A2AShape, seed: int = 0) -> dict:

@@ -9,6 +9,7 @@ cannot be built or loaded, importing the functions raises.
   mc2_all_gather_mm        out = concat_m(x_chunks) @ x2 (+ bias), plus gathered
   mc2_alltoall_quant_mm    out = (Quant(permute(chunks)) @ x2) * x1s * x2s + bias
   mc2_matmul_reduce_scatter  out_j = (sum_r X_r @ W_r^T)[rows of rank j] (+ bias)
+  mc2_matmul_weight_grad   dw = dy^T @ x, db = dy.sum(0)
 """
 from __future__ import annotations
 
@@ -57,6 +58,8 @@ def lib() -> ctypes.CDLL:
         L.mc2_all_gather_mm.restype = _INT
         L.mc2_matmul_reduce_scatter.argtypes = [_P, _P, _INT, _I64, _I64, _I64, _INT, _P, _INT, _P, _P]
         L.mc2_matmul_reduce_scatter.restype = _INT
+        L.mc2_matmul_weight_grad.argtypes = [_P, _I64, _I64, _P, _I64, _INT, _P, _P, _P]
+        L.mc2_matmul_weight_grad.restype = _INT
         L.mc2_alltoall_quant_mm_workspace.argtypes = [_INT, _I64, _I64, _I64, _INT, _INT,
                                                       ctypes.POINTER(ctypes.c_size_t)]
         L.mc2_alltoall_quant_mm_workspace.restype = _INT
@@ -165,6 +168,25 @@ def mc2_matmul_reduce_scatter(x_chunks: Sequence[torch.Tensor], w_chunks: Sequen
     return list(out_chunks)
 
 
+def mc2_matmul_weight_grad(dy: torch.Tensor, x: torch.Tensor, *, with_bias: bool = True,
+                           dw: Optional[torch.Tensor] = None, db: Optional[torch.Tensor] = None, stream=None):
+    """dW = dY^T @ X (n, k) and, with ``with_bias``, dB = dY.sum(0) (n).
+
+    dy (m, n) and x (m, k) of one 16-bit type on this GPU (for the all-gather
+    layer, x is the ``gathered`` output of its forward call).  Returns (dw, db).
+    """
+    m, n = dy.shape
+    k = x.shape[1]
+    if dw is None:
+        dw = torch.empty((n, k), dtype=dy.dtype, device=dy.device)
+    if with_bias and db is None:
+        db = torch.empty((n,), dtype=dy.dtype, device=dy.device)
+    st = lib().mc2_matmul_weight_grad(_dev(dy, "dy"), m, n, _dev(x, "x"), k, _dtype_code(dy.dtype), _dev(dw, "dw"),
+                                      _opt(db if with_bias else None, "db"), _stream(stream))
+    _check(st)
+    return dw, (db if with_bias else None)
+
+
 def mc2_alltoall_quant_mm_workspace(rank_size: int, bs_local: int, h: int, n: int, x1_quant_mode: int,
                                     x1_dtype: torch.dtype) -> int:
     nbytes = ctypes.c_size_t(0)
@@ -248,7 +270,7 @@ def mc2_device_status() -> int:
 
 __all__ = [
     "Mc2Error", "lib", "library_path", "status_str", "last_error", "mc2_all_gather_mm",
-    "mc2_matmul_reduce_scatter", "mc2_alltoall_quant_mm_workspace", "mc2_alltoall_quant_mm",
+    "mc2_matmul_reduce_scatter", "mc2_matmul_weight_grad", "mc2_alltoall_quant_mm_workspace", "mc2_alltoall_quant_mm",
     "mc2_alltoall_quant_mm_no_alloc",
     "NO_ALLOC_SCRATCH_BYTES", "mc2_device_status",
     "MC2_OK", "MC2_ERR_NULL", "MC2_ERR_SHAPE", "MC2_ERR_DTYPE", "MC2_ERR_UNSUPPORTED", "MC2_ERR_WORKSPACE",

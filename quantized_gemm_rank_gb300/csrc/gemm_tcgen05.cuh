@@ -70,7 +70,9 @@ struct TileCfg {
     static constexpr uint32_t kSmemBytes = kStages * kStageBytes + 1024 + 1024;
 };
 
-enum AMode : int { A_SINGLE = 0, A_MCONCAT = 1, A_KINTERLEAVE = 2 };
+// A_SINGLE_MN: one map over an (k, m) row-major matrix, i.e. A = that matrix
+// transposed, read M-major (the weight gradient's dY^T)
+enum AMode : int { A_SINGLE = 0, A_MCONCAT = 1, A_KINTERLEAVE = 2, A_SINGLE_MN = 3 };
 
 struct GemmParams {
     CUtensorMap a_maps[kMaxAMaps];  // A operand: one map, or one per rank's chunk
@@ -395,6 +397,10 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
                     }
                     kl += kBK;
                     if (kl >= p.k_local) kl = 0, ++kc;
+                } else if (p.a_mode == A_SINGLE_MN) {
+                    // M-major A: 64-wide M slabs of the (k, m) matrix, like an N-major B
+#pragma unroll
+                    for (int j = 0; j < kBM / 64; ++j) load(sA + j * (kBK * 128), &p.a_maps[0], m0 + 64 * j, k0, a_bar);
                 } else {
                     load(sA, &p.a_maps[0], k0, m0, a_bar);
                 }
@@ -423,11 +429,14 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
         }
     } else if (warp == 1 && lane == 0 && leader) {
         // ------------------------------------------------------------ MMA issuer
-        const uint32_t idesc = ptx::idesc_f16(kBF16 && !kIntPath, p.b_mn_major != 0, Cfg::kTileM, kBN);
+        const bool a_mn = p.a_mode == A_SINGLE_MN;
+        const uint32_t idesc = ptx::idesc_f16(kBF16 && !kIntPath, p.b_mn_major != 0, Cfg::kTileM, kBN, a_mn);
         // descriptors of stage 0, k-slice 0; later ones add to the address field
-        // (>> 4 units): +2 per 16-wide k-slice of A, +stage bytes per stage
+        // (>> 4 units): per 16-wide k-slice +2 (K-major: 32 bytes into the
+        // swizzled row) or +128 (MN-major: 16 rows of 128 bytes), +stage bytes per stage
         const uint32_t s0 = ptx::smem_u32(smem);
-        const uint64_t a_desc0 = ptx::smem_desc_sw128(s0, 16, 1024);
+        const uint64_t a_desc0 = a_mn ? ptx::smem_desc_sw128(s0, kBK * 128, 1024) : ptx::smem_desc_sw128(s0, 16, 1024);
+        const uint32_t a_kk = a_mn ? (2048u >> 4) : (32u >> 4);
         const uint64_t b_desc0 = p.b_mn_major ? ptx::smem_desc_sw128(s0 + kATileBytes, kBK * 128, 1024)
                                               : ptx::smem_desc_sw128(s0 + kATileBytes, 16, 1024);
         const uint32_t b_kk = p.b_mn_major ? (2048u >> 4) : (32u >> 4);
@@ -468,9 +477,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
                 const uint64_t ad = a_desc0 + stage_off;
                 const uint64_t bd = b_desc0 + stage_off;
                 ptx::mma_f16_ss<kG>(d_tmem, ad, bd, idesc, kin > 0 ? 1u : 0u);
-                ptx::mma_f16_ss<kG>(d_tmem, ad + 2, bd + b_kk, idesc, 1u);
-                ptx::mma_f16_ss<kG>(d_tmem, ad + 4, bd + 2 * b_kk, idesc, 1u);
-                ptx::mma_f16_ss<kG>(d_tmem, ad + 6, bd + 3 * b_kk, idesc, 1u);
+                ptx::mma_f16_ss<kG>(d_tmem, ad + a_kk, bd + b_kk, idesc, 1u);
+                ptx::mma_f16_ss<kG>(d_tmem, ad + 2 * a_kk, bd + 2 * b_kk, idesc, 1u);
+                ptx::mma_f16_ss<kG>(d_tmem, ad + 3 * a_kk, bd + 3 * b_kk, idesc, 1u);
                 ptx::mma_commit<kG>(release0 + 8u * stage);
                 if (++stage == S) {
                     stage = 0;

@@ -313,6 +313,51 @@ int mc2_matmul_reduce_scatter(const void *const *x_chunks, const void *const *w_
     return MC2_OK;
 }
 
+int mc2_matmul_weight_grad(const void *dy, int64_t m, int64_t n, const void *x, int64_t k, int dtype, void *dw,
+                           void *db, void *stream) {
+    g_last_error[0] = '\0';
+    if (!dy || !x || !dw) return fail(MC2_ERR_NULL, "dy, x and dw are required");
+    if (dtype != MC2_F16 && dtype != MC2_BF16)
+        return fail(MC2_ERR_DTYPE, "dtype must be MC2_F16 or MC2_BF16 (got %d)", dtype);
+    if (m < 1 || n < 1 || k < 1)
+        return fail(MC2_ERR_SHAPE, "empty tensors are not supported (m=%lld n=%lld k=%lld)", (long long)m,
+                    (long long)n, (long long)k);
+    if (m > INT32_MAX || n > INT32_MAX || k > INT32_MAX) return fail(MC2_ERR_SHAPE, "m, n or k exceeds INT32_MAX");
+    if (n % 8 != 0 || k % 8 != 0)
+        return fail(MC2_ERR_UNSUPPORTED, "this kernel needs n %% 8 == 0 and k %% 8 == 0 (got n=%lld k=%lld)",
+                    (long long)n, (long long)k);
+    if (!aligned16(dy) || !aligned16(x) || !aligned16(dw) || (db && !aligned16(db)))
+        return fail(MC2_ERR_UNSUPPORTED, "all tensors must be 16-byte aligned");
+
+    DeviceInfo dev;
+    if (int st = current_device(&dev)) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaSuccess;
+    if (db) {
+        e = mc2::launch_colsum16(dy, m, static_cast<int>(n), dtype == MC2_BF16, db, s);
+        if (e != cudaSuccess) return fail(MC2_ERR_CUDA, "bias-gradient launch: %s", cudaGetErrorString(e));
+    }
+    // dW (n, k) = dY^T @ X: A = dY^T read M-major from dY (m, n), B = X (m, k) N-major,
+    // the contraction runs down the m rows of both
+    mc2::GemmParams p;
+    memset(&p, 0, sizeof(p));
+    if (!make_map16(&p.a_maps[0], dy, n, m, 64, mc2::kBK)) return fail(MC2_ERR_CUDA, "cuTensorMapEncodeTiled failed for dy");
+    if (!make_map16(&p.b_map, x, k, m, 64, mc2::kBK)) return fail(MC2_ERR_CUDA, "cuTensorMapEncodeTiled failed for x");
+    p.num_a_maps = 1;
+    p.a_mode = mc2::A_SINGLE_MN;
+    p.b_mn_major = 1;
+    p.m = static_cast<int>(n);
+    p.n = static_cast<int>(k);
+    p.k = static_cast<int>(m);
+    p.kblock_tiles = kKBlockTiles;
+    p.out = dw;
+    p.wait_limit_ns = kWaitLimitNs;
+    const int group = mc2::gemm_group_for(static_cast<int>(n));
+    e = mc2::launch_gemm(dtype == MC2_BF16 ? mc2::GEMM_BF16 : mc2::GEMM_F16, group, p, dev.num_sms, s);
+    if (e != cudaSuccess) return fail(MC2_ERR_CUDA, "GEMM launch: %s", cudaGetErrorString(e));
+    return MC2_OK;
+}
+
 int mc2_alltoall_quant_mm_workspace(int rank_size, int64_t bs_local, int64_t h, int64_t n, int x1_quant_mode,
                                     int x1_dtype, size_t *bytes) {
     g_last_error[0] = '\0';

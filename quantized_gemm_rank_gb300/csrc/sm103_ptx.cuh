@@ -269,11 +269,12 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
 
 // Instruction descriptor of kind::f16 with fp32 accumulation.
 //   bits 4-5 D format (1 = f32), 7-9 A format, 10-12 B format (0 = f16,
-//   1 = bf16), 15 A major (0 = K), 16 B major (1 = MN), 17-22 N >> 3,
+//   1 = bf16), 15 A major (1 = MN), 16 B major (1 = MN), 17-22 N >> 3,
 //   24-28 M >> 4.
-__host__ __device__ constexpr uint32_t idesc_f16(bool bf16, bool b_mn_major, int M, int N) {
-    return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) | ((b_mn_major ? 1u : 0u) << 16) |
-           (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+__host__ __device__ constexpr uint32_t idesc_f16(bool bf16, bool b_mn_major, int M, int N, bool a_mn_major = false) {
+    return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) | ((a_mn_major ? 1u : 0u) << 15) |
+           ((b_mn_major ? 1u : 0u) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
+           (static_cast<uint32_t>(M >> 4) << 24);
 }
 
 // ----------------------------------------------------------------- registers

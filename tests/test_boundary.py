@@ -140,6 +140,27 @@ def test_matmul_reduce_scatter_bounds_accepted_by_validation():
         assert mmrs_call(k_local=kl) == mc2.MC2_ERR_CUDA, mc2.last_error()
 
 
+def wg_call(m=64, n=64, k=64, dtype=mc2.MC2_BF16, dy=FAKE, x=FAKE, dw=FAKE, db=None):
+    return mc2.lib().mc2_matmul_weight_grad(dy, m, n, x, k, dtype, dw, db, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(dy=None), mc2.MC2_ERR_NULL),
+    (dict(x=None), mc2.MC2_ERR_NULL),
+    (dict(dw=None), mc2.MC2_ERR_NULL),
+    (dict(dtype=mc2.MC2_I8), mc2.MC2_ERR_DTYPE),
+    (dict(m=0), mc2.MC2_ERR_SHAPE),
+    (dict(n=0), mc2.MC2_ERR_SHAPE),
+    (dict(k=2 ** 31), mc2.MC2_ERR_SHAPE),
+    (dict(n=60), mc2.MC2_ERR_UNSUPPORTED),
+    (dict(k=12), mc2.MC2_ERR_UNSUPPORTED),
+    (dict(db=FAKE + 2), mc2.MC2_ERR_UNSUPPORTED),
+])
+def test_weight_grad_rejects(kw, status):
+    assert wg_call(**kw) == status, mc2.last_error()
+    assert mc2.last_error() != ""
+
+
 def a2a_call(rank_size=2, bs_local=16, h=64, x1_dtype=mc2.MC2_BF16, x1_scale=None, x2=FAKE, x2_scale=FAKE,
              bias=FAKE, bias_dtype=mc2.MC2_F32, mode=7, mode2=2, n=64, out=FAKE, ws=FAKE, ws_bytes=1 << 40,
              chunks=None, a2a_out=None):
