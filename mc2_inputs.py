@@ -31,6 +31,12 @@ Workloads (names used throughout the repository):
              bf16 ~N(0, std m^-1/2) (the gradient of a token-mean loss, so that
              dW ~ N(0, 1)), gathered X (16384, 8192) bf16 ~N(0,1) -> dW (7168, 8192),
              dB (7168).
+  qar-8x4096x8192  QuantAllReduce, 8 ranks x int8 (4096, 8192) uniform on
+             [-127, 127] with pertoken-pergroup fp32 scales (4096, 64)
+             ~U(1e-3, 1e-2), bf16 output.
+  qar-mx-8x4096x8192  QuantAllReduce, 8 ranks x fp8 e4m3fn (4096, 8192) (values
+             N(0, 64^2) cast to e4m3fn, saturated at +-448) with mx e8m0 scales
+             (4096, 128, 2), codes uniform on [118, 134], bf16 output.
   a2a-full   AlltoAllQuantMatmul, quant mode 3 (pre-quantised int8), 8 ranks x
              (16384, 4096) int8 uniform on [-127, 127], per-token x1 scale
              (16384) fp32 ~U(1e-3, 1e-2), x2 int8 (32768, 7168), x2 scale
@@ -125,6 +131,23 @@ class WGradShape:
         return 2.0 * self.m * self.n * self.k
 
 
+@dataclass(frozen=True)
+class QARShape:
+    world_size: int
+    bs: int                         # tokens (b * s)
+    h: int                          # hidden size, 128-aligned, [1024, 8192]
+    x_kind: str = "int8"            # "int8" | "e4m3" | "e5m2"
+    scale_kind: str = "fp32"        # "fp32": (bs, h/128) | "e8m0": (bs, h/64, 2)
+    out_dtype: torch.dtype = torch.bfloat16
+
+    @property
+    def bytes(self) -> float:
+        """Bytes the op must move: every rank's data and scales read once, the output written once."""
+        sb = self.h // 128 * 4 if self.scale_kind == "fp32" else self.h // 32
+        ob = torch.empty((), dtype=self.out_dtype).element_size()
+        return float(self.bs) * (self.world_size * (self.h + sb) + self.h * ob)
+
+
 WORKLOADS = {
     "ag-tiny": AGShape(world_size=8, m_local=16, k=512, n=64, dtype=torch.float16, w_std=1.0),
     "ag-8x1024": AGShape(world_size=8, m_local=1024, k=4096, n=4096),
@@ -134,6 +157,8 @@ WORKLOADS = {
     "a2a-full": A2AShape(rank_size=8, bs_local=16384, h=4096, n=7168, quant_mode=3),
     "mmrs-4x2048": MMRSShape(world_size=4, m=16384, k_local=2048, n=8192),
     "wgrad-ag-4x4096": WGradShape(m=16384, n=7168, k=8192),
+    "qar-8x4096x8192": QARShape(world_size=8, bs=4096, h=8192),
+    "qar-mx-8x4096x8192": QARShape(world_size=8, bs=4096, h=8192, x_kind="e4m3", scale_kind="e8m0"),
 }
 
 
@@ -183,6 +208,27 @@ def wgrad_inputs(s: WGradShape, seed: int = 0) -> dict:
     dy = (torch.randn(s.m, s.n, generator=g) * dy_std).to(s.dtype)
     x = (torch.randn(s.m, s.k, generator=g) * s.x_std).to(s.dtype)
     return {"dy": dy, "x": x}
+
+
+def qar_inputs(s: QARShape, seed: int = 0) -> dict:
+    """x_chunks: R x (bs, h) uint8 codes; scale_chunks: R x fp32 (bs, h/128) or
+    R x uint8 e8m0 codes (bs, h/64, 2)."""
+    g = _gen(seed)
+    xs, ss = [], []
+    for _ in range(s.world_size):
+        if s.x_kind == "int8":
+            xs.append(_randint8(g, (s.bs, s.h)).view(torch.uint8))
+        elif s.x_kind == "e4m3":
+            v = (torch.randn(s.bs, s.h, generator=g) * 64.0).clamp(-448.0, 448.0)
+            xs.append(v.to(torch.float8_e4m3fn).view(torch.uint8))
+        else:
+            v = (torch.randn(s.bs, s.h, generator=g) * 1024.0).clamp(-57344.0, 57344.0)
+            xs.append(v.to(torch.float8_e5m2).view(torch.uint8))
+        if s.scale_kind == "fp32":
+            ss.append(torch.rand(s.bs, s.h // 128, generator=g) * 9e-3 + 1e-3)
+        else:
+            ss.append(torch.randint(118, 135, (s.bs, s.h // 64, 2), generator=g, dtype=torch.uint8))
+    return {"x_chunks": xs, "scale_chunks": ss}
 
 
 def a2a_inputs(s: A2AShape, seed: int = 0) -> dict:

@@ -11,8 +11,10 @@ Pages followed (title -- section):
   * "torch_npu.npu_all_gather_base_mm" -- 功能说明, 接口原型, 输出说明, 约束说明
   * "aclnnAlltoAllQuantMatmul" -- 功能说明 / 计算公式 (dynamic- and full-quant)
   * "hyper_parallel .../tensor_parallel/mc2.py" -- module docstring (the
-    all_gather_matmul / matmul_reduce_scatter duals), AllGatherMatmulFunction
-    and MatmulReduceScatterFunction.forward
+    all_gather_matmul / matmul_reduce_scatter duals and their dW), and
+    AllGatherMatmulFunction / MatmulReduceScatterFunction
+  * "QuantAllReduce" (mc2/quant_all_reduce) -- 功能说明 (formula), 参数说明,
+    约束说明 (int8 / fp8 data, pertoken-pergroup fp32 or mx e8m0 scales)
 
 Every function here is pinned by ``tests/test_oracle_*.py`` against closed
 forms, brute force and independent library routines.
@@ -64,6 +66,11 @@ def _load():
         lib.oracle_permute.argtypes = [_P, _INT, _I64, _I64, _INT, _P, _I64, _P]
         lib.oracle_comm_out.argtypes = [_P, _INT, _I64, _I64, _INT, _P]
         lib.oracle_matmul_weight_grad.argtypes = [_P, _P, _I64, _I64, _I64, _INT, _P, _I64, _P, _P]
+        lib.oracle_decode_fp8.restype = ctypes.c_double
+        lib.oracle_decode_fp8.argtypes = [ctypes.c_uint8, _INT]
+        lib.oracle_decode_e8m0.restype = ctypes.c_double
+        lib.oracle_decode_e8m0.argtypes = [ctypes.c_uint8]
+        lib.oracle_quant_all_reduce.argtypes = [_P, _P, _INT, _I64, _I64, _INT, _INT, _INT, _P]
         lib.oracle_quant_pertoken_dynamic.argtypes = [_P, _I64, _I64, _P, _INT, _P, _P]
         lib.oracle_int8_mm.argtypes = [_P, _I64, _I64, _P, _I64, _P]
         lib.oracle_dequant.argtypes = [_P, _I64, _I64, _P, _P, _P, _P]
@@ -330,3 +337,36 @@ def alltoall_quant_mm(chunks: Sequence[torch.Tensor], x2: torch.Tensor, x2_scale
                                           acc.data_ptr())
     _check(rc, "alltoall_quant_mm")
     return {"out": out.view(torch.bfloat16), "q": q, "x1_scale": sc, "acc": acc}
+
+
+# --------------------------------------------------------------------------- QuantAllReduce
+X_KINDS = {"int8": 0, "e4m3": 1, "e5m2": 2}
+SCALE_KINDS = {"fp32": 0, "e8m0": 1}
+_OUT_KINDS = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
+
+
+def decode_fp8(code: int, fmt: str) -> float:
+    """Value of one fp8 code ("e4m3" = E4M3FN, "e5m2")."""
+    return _load().oracle_decode_fp8(code & 0xFF, 1 if fmt == "e5m2" else 0)
+
+
+def decode_e8m0(code: int) -> float:
+    return _load().oracle_decode_e8m0(code & 0xFF)
+
+
+def quant_all_reduce(x_chunks: Sequence[torch.Tensor], scale_chunks: Sequence[torch.Tensor], *, x_kind: str,
+                     scale_kind: str, out_dtype: torch.dtype = torch.bfloat16) -> torch.Tensor:
+    """out = sum_r dequant(x_r, scales_r), (bs, h).  x_r: (bs, h) 1-byte codes
+    (uint8/int8 tensors holding int8, e4m3fn or e5m2 bits); scales_r: fp32
+    (bs, h/128) or e8m0 codes (bs, h/64, 2) as uint8."""
+    xs = [_c(x).view(torch.uint8) for x in x_chunks]
+    if scale_kind == "fp32":
+        ss = [_c(s.float()) for s in scale_chunks]
+    else:
+        ss = [_c(s).view(torch.uint8) for s in scale_chunks]
+    bs, h = xs[0].shape
+    out = torch.empty((bs, h), dtype=out_dtype)
+    rc = _load().oracle_quant_all_reduce(_ptr_array(xs), _ptr_array(ss), len(xs), bs, h, X_KINDS[x_kind],
+                                         SCALE_KINDS[scale_kind], _OUT_KINDS[out_dtype], out.data_ptr())
+    _check(rc, "quant_all_reduce")
+    return out

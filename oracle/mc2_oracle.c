@@ -17,6 +17,8 @@
  *         约束说明 (constraints).
  *   [MC2] "hyper_parallel .../tensor_parallel/mc2.py" (coverage listing) --
  *         module docstring and AllGatherMatmulFunction.forward.
+ *   [QAR] "QuantAllReduce" (ops-transformer mc2/quant_all_reduce) -- 功能说明
+ *         (formula), 参数说明 (parameters), 约束说明 (constraints).
  *
  * Precision.  The pages do not fix the accumulation precision of the bf16 /
  * fp16 matmul, so the oracle accumulates in fp64 and rounds once to the
@@ -510,4 +512,79 @@ int oracle_matmul_weight_grad(const uint16_t *dy, const uint16_t *x, int64_t m, 
     }
     free(tab);
     return err;
+}
+
+/* ------------------------------------------------------------------------ */
+/* [QAR] Low-bit element formats, decoded from their definitions.             */
+/*   FP8 E4M3FN: 1 sign, 4 exponent (bias 7), 3 mantissa bits; exponent 0 is  */
+/*   subnormal (m/8 * 2^-6); no infinities; S.1111.111 is NaN.                */
+/*   FP8 E5M2: 1 sign, 5 exponent (bias 15), 2 mantissa bits; exponent 0 is   */
+/*   subnormal (m/4 * 2^-14); exponent 31 is inf (m = 0) or NaN.              */
+/*   E8M0 (mx scale): an unsigned biased exponent, 2^(e - 127); 0xFF is NaN.  */
+/* ------------------------------------------------------------------------ */
+double oracle_decode_fp8(uint8_t v, int is_e5m2) {
+    int sign = (v >> 7) & 1;
+    int e, m;
+    double mag;
+    if (is_e5m2) {
+        e = (v >> 2) & 0x1F;
+        m = v & 0x3;
+        if (e == 31) return m == 0 ? (sign ? -INFINITY : INFINITY) : NAN;
+        mag = e == 0 ? ldexp((double)m / 4.0, -14) : ldexp(1.0 + (double)m / 4.0, e - 15);
+    } else {
+        e = (v >> 3) & 0xF;
+        m = v & 0x7;
+        if (e == 15 && m == 7) return NAN;
+        mag = e == 0 ? ldexp((double)m / 8.0, -6) : ldexp(1.0 + (double)m / 8.0, e - 7);
+    }
+    return sign ? -mag : mag;
+}
+
+double oracle_decode_e8m0(uint8_t v) {
+    if (v == 0xFF) return NAN;
+    return ldexp(1.0, (int)v - 127);
+}
+
+/* ------------------------------------------------------------------------ */
+/* [QAR] QuantAllReduce:  AllGatherData = AllGather(x),                       */
+/*   AllGatherScales = AllGather(scales),                                     */
+/*   output = Reduce(AllGatherScales * AllGatherData), Reduce = sum over the  */
+/*   ranks (reduceOp "sum").  Rank r's x_r (bs, h) and scales_r are given     */
+/* side by side; every rank receives the same output (bs, h):                 */
+/*   out[t, j] = sum_r dec(x_r[t, j]) * dec(scales_r[t, j / G])               */
+/*   x_kind 0 int8, 1 fp8 e4m3fn, 2 fp8 e5m2                                  */
+/*   scale_kind 0: fp32, one per token per group of G = 128 (pertoken-        */
+/*     pergroup, scales (bs, h/128));  1: e8m0, one per group of G = 32 (mx,  */
+/*     scales (bs, h/64, 2) read flat as (bs, h/32)).                         */
+/*   out_kind 0 fp32, 1 fp16, 2 bf16.                                         */
+/* Reading: the products are exact in fp64 (at most 8 + 24 significant      */
+/* bits), summed in fp64 in rank order and rounded once, nearest-even, to    */
+/* the output type.                                                           */
+/* ------------------------------------------------------------------------ */
+int oracle_quant_all_reduce(const uint8_t *const *x_chunks, const void *const *scale_chunks, int world_size,
+                            int64_t bs, int64_t h, int x_kind, int scale_kind, int out_kind, void *out) {
+    if (!x_chunks || !scale_chunks || !out || world_size < 1 || bs < 1 || h < 1) return OR_ERR_ARG;
+    if (x_kind < 0 || x_kind > 2 || scale_kind < 0 || scale_kind > 1 || out_kind < 0 || out_kind > 2)
+        return OR_ERR_ARG;
+    int64_t G = scale_kind == 0 ? 128 : 32;
+    if (h % G != 0) return OR_ERR_ARG;
+    int64_t groups = h / G;
+#pragma omp parallel for
+    for (int64_t t = 0; t < bs; ++t) {
+        for (int64_t j = 0; j < h; ++j) {
+            double s = 0.0;
+            for (int r = 0; r < world_size; ++r) {
+                uint8_t xv = x_chunks[r][t * h + j];
+                double x = x_kind == 0 ? (double)(int8_t)xv : oracle_decode_fp8(xv, x_kind == 2);
+                double sc = scale_kind == 0 ? (double)((const float *)scale_chunks[r])[t * groups + j / G]
+                                            : oracle_decode_e8m0(((const uint8_t *)scale_chunks[r])[t * groups + j / G]);
+                s += x * sc;
+            }
+            if (out_kind == 0)
+                ((float *)out)[t * h + j] = (float)s;
+            else
+                ((uint16_t *)out)[t * h + j] = oracle_encode16_rne(s, out_kind == 2);
+        }
+    }
+    return OR_OK;
 }
