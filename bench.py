@@ -348,8 +348,9 @@ def run_reference(args):
 
 
 # ----------------------------------------------------------------------------- main
-def extra_table(dev, flush, stream, steps):
-    """Per-workload device times of each call alone (every workload but the step's two)."""
+def extra_table(dev, flush, stream, steps, hbm_peak):
+    """Per-workload device times of each call alone (every workload but the step's two);
+    the HBM-bound QuantAllReduce workloads report GB/s against the HBM peak."""
     import quantized_gemm_rank_gb300 as mc2
     res = {}
     for name, s in mc2_inputs.WORKLOADS.items():
@@ -372,6 +373,18 @@ def extra_table(dev, flush, stream, steps):
             dbo = torch.empty((s.n,), dtype=s.dtype, device=dev)
             fn = lambda: mc2.mc2_matmul_weight_grad(ch, wc, dw=dwo, db=dbo)  # noqa
             fl = s.flops
+        elif isinstance(s, mc2_inputs.QARShape):
+            inp = mc2_inputs.qar_inputs(s, seed=0)
+            ch = [x.to(dev) for x in inp["x_chunks"]]
+            wc = [x.to(dev) for x in inp["scale_chunks"]]
+            out = torch.empty((s.bs, s.h), dtype=s.out_dtype, device=dev)
+            fn = lambda: mc2.mc2_quant_all_reduce(ch, wc, x_kind=s.x_kind, out_dtype=s.out_dtype, out=out)  # noqa
+            t = statistics.median(time_device(fn, steps, 3, flush, stream))
+            gbs = s.bytes / (t * 1e-3) / 1e9
+            res[name] = {"us": round(t * 1e3, 2), "gbs": round(gbs, 1), "hbm_frac": round(gbs / hbm_peak, 4)}
+            del inp, ch
+            torch.cuda.empty_cache()
+            continue
         elif isinstance(s, mc2_inputs.MMRSShape):
             inp = mc2_inputs.mmrs_inputs(s, seed=0)
             ch = [x.to(dev) for x in inp["x_chunks"]]
@@ -460,7 +473,7 @@ def main():
     mc2 = step.mc2
     assert mc2.mc2_device_status() == mc2.MC2_OK, "a bounded device wait gave up"
 
-    extra = None if (args.no_extra or args.profile or rank != 0) else extra_table(dev, flush, stream, 10)
+    extra = None if (args.no_extra or args.profile or rank != 0) else extra_table(dev, flush, stream, 10, peaks["hbm"])
     cpu = oracle_baseline(ag_s, a2a_s, step.host) if (rank == 0 and world == 1 and not args.profile) else None
 
     traffic = AG_GEMM_TRAFFIC if (AG_GEMM_TRAFFIC is not None and AG_GEMM_TRAFFIC_SRC_HASH == kernel_src_hash()) \

@@ -1,10 +1,12 @@
 /*
  * mc2_gb300.h -- C ABI of the GB300 (sm_103a) MC2 fused-linear library.
  *
- * Two operations, each the compute hot path of one communication-compute
- * fused linear.  The world_size (rankSize) shards that a collective would
- * deliver are separate device buffers on one GPU; the library reads them in
- * place and never runs a collective.
+ * The compute hot paths of the communication-compute fused operations:
+ * AllGatherMatmul, AlltoAllQuantMatmul, MatmulReduceScatter (with the weight
+ * gradient of the fused linear layers) and QuantAllReduce.  The world_size
+ * (rankSize) shards that a collective would deliver are separate device
+ * buffers on one GPU; the library reads them in place and never runs a
+ * collective.
  *
  * Conventions shared by every call
  *   - Every tensor is a DEVICE pointer, row-major and contiguous, owned by the
@@ -44,7 +46,15 @@ typedef enum {
     MC2_ERR_TIMEOUT = -7      /* a bounded device-side wait gave up (see mc2_device_status) */
 } mc2_status;
 
-typedef enum { MC2_F16 = 1, MC2_BF16 = 2, MC2_F32 = 3, MC2_I8 = 4 } mc2_dtype;
+typedef enum {
+    MC2_F16 = 1,
+    MC2_BF16 = 2,
+    MC2_F32 = 3,
+    MC2_I8 = 4,
+    MC2_F8E4M3 = 5,   /* fp8 E4M3FN: bias 7, no infinities, S.1111.111 is NaN */
+    MC2_F8E5M2 = 6,   /* fp8 E5M2: bias 15, IEEE-style infinities and NaNs */
+    MC2_E8M0 = 7      /* mx scale: an unsigned biased exponent, value 2^(code - 127), 0xFF is NaN */
+} mc2_dtype;
 
 /* Quant-mode enumeration of "aclnnAlltoAllQuantMatmul" (函数原型, the
  * x1QuantMode / x2QuantMode / commQuantMode values). */
@@ -142,6 +152,36 @@ int mc2_matmul_reduce_scatter(const void *const *x_chunks, const void *const *w_
  */
 int mc2_matmul_weight_grad(const void *dy, int64_t m, int64_t n, const void *x, int64_t k, int dtype, void *dw,
                            void *db, void *stream);
+
+/*
+ * QuantAllReduce  ("QuantAllReduce", ops-transformer mc2/quant_all_reduce:
+ * 功能说明 formula output = Reduce(AllGather(scales) * AllGather(x)), reduceOp
+ * "sum"; 参数说明 and 约束说明 for the types, the scale layouts and H).
+ *
+ *   out[t, j] = sum over r of dec(x_r[t, j]) * dec(scales_r[t, j / G])
+ *
+ *   Every rank receives the same sum, so one output is written.  The products
+ *   are added in rank order by fp32 fused multiply-adds and rounded once
+ *   (nearest-even) to out_dtype.
+ *
+ *   x_chunks      host array of world_size device pointers, each (bs, h) codes
+ *                 of x_dtype (a (b, s, h) tensor is passed with bs = b * s)
+ *   scale_chunks  host array of world_size device pointers:
+ *                   scale_dtype MC2_F32  -> fp32 (bs, h / 128): pertoken-pergroup,
+ *                                           G = 128
+ *                   scale_dtype MC2_E8M0 -> e8m0 codes (bs, h / 64, 2), read flat
+ *                                           as (bs, h / 32): mx, G = 32
+ *   world_size    2, 4 or 8
+ *   bs            tokens, >= 1
+ *   h             hidden size, a multiple of 128 in [1024, 8192]
+ *   x_dtype       MC2_I8, MC2_F8E4M3 or MC2_F8E5M2 (HiFloat8 is not supported);
+ *                 MC2_E8M0 scales need an fp8 x_dtype
+ *   out_dtype     MC2_F32, MC2_F16 or MC2_BF16;  out (bs, h)
+ *
+ * Returns MC2_OK or a negative mc2_status; nothing is launched on error.
+ */
+int mc2_quant_all_reduce(const void *const *x_chunks, const void *const *scale_chunks, int world_size, int64_t bs,
+                         int64_t h, int x_dtype, int scale_dtype, int out_dtype, void *out, void *stream);
 
 /*
  * Workspace size (bytes) that mc2_alltoall_quant_mm needs for these sizes.

@@ -10,6 +10,7 @@ cannot be built or loaded, importing the functions raises.
   mc2_alltoall_quant_mm    out = (Quant(permute(chunks)) @ x2) * x1s * x2s + bias
   mc2_matmul_reduce_scatter  out_j = (sum_r X_r @ W_r^T)[rows of rank j] (+ bias)
   mc2_matmul_weight_grad   dw = dy^T @ x, db = dy.sum(0)
+  mc2_quant_all_reduce     out = sum_r dequant(x_r, scales_r)  (int8/fp8 codes)
 """
 from __future__ import annotations
 
@@ -31,6 +32,7 @@ MC2_ERR_CUDA = -6
 MC2_ERR_TIMEOUT = -7
 
 MC2_F16, MC2_BF16, MC2_F32, MC2_I8 = 1, 2, 3, 4
+MC2_F8E4M3, MC2_F8E5M2, MC2_E8M0 = 5, 6, 7
 QUANT_PERCHANNEL = 2
 QUANT_PERTOKEN = 3
 QUANT_PERTOKEN_DYNAMIC = 7
@@ -60,6 +62,8 @@ def lib() -> ctypes.CDLL:
         L.mc2_matmul_reduce_scatter.restype = _INT
         L.mc2_matmul_weight_grad.argtypes = [_P, _I64, _I64, _P, _I64, _INT, _P, _P, _P]
         L.mc2_matmul_weight_grad.restype = _INT
+        L.mc2_quant_all_reduce.argtypes = [_P, _P, _INT, _I64, _I64, _INT, _INT, _INT, _P, _P]
+        L.mc2_quant_all_reduce.restype = _INT
         L.mc2_alltoall_quant_mm_workspace.argtypes = [_INT, _I64, _I64, _I64, _INT, _INT,
                                                       ctypes.POINTER(ctypes.c_size_t)]
         L.mc2_alltoall_quant_mm_workspace.restype = _INT
@@ -187,6 +191,39 @@ def mc2_matmul_weight_grad(dy: torch.Tensor, x: torch.Tensor, *, with_bias: bool
     return dw, (db if with_bias else None)
 
 
+_QAR_X = {"int8": MC2_I8, "e4m3": MC2_F8E4M3, "e5m2": MC2_F8E5M2}
+_QAR_X_BY_DTYPE = {torch.int8: "int8", torch.float8_e4m3fn: "e4m3", torch.float8_e5m2: "e5m2"}
+
+
+def mc2_quant_all_reduce(x_chunks: Sequence[torch.Tensor], scale_chunks: Sequence[torch.Tensor], *,
+                         x_kind: Optional[str] = None, out_dtype: torch.dtype = torch.bfloat16,
+                         out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """QuantAllReduce of the ranks' quantised shards resident on this GPU.
+
+    x_chunks: world_size tensors (bs, h) or (b, s, h) of one-byte codes: int8,
+    float8_e4m3fn or float8_e5m2 (or uint8 with ``x_kind`` "int8" | "e4m3" |
+    "e5m2").  scale_chunks: fp32 (bs, h/128) per-token-per-group scales, or e8m0
+    codes (bs, h/64, 2) as uint8 (mx).  Returns out of the same leading shape
+    as x in ``out_dtype`` (fp32, fp16 or bf16).
+    """
+    x0 = x_chunks[0]
+    if x_kind is None:
+        if x0.dtype not in _QAR_X_BY_DTYPE:
+            raise ValueError("x_kind is required for x of dtype %s" % x0.dtype)
+        x_kind = _QAR_X_BY_DTYPE[x0.dtype]
+    h = x0.shape[-1]
+    bs = x0.numel() // h
+    s0 = scale_chunks[0]
+    sdt = MC2_F32 if s0.dtype == torch.float32 else MC2_E8M0
+    if out is None:
+        out = torch.empty(x0.shape, dtype=out_dtype, device=x0.device)
+    st = lib().mc2_quant_all_reduce(_ptrs(x_chunks, "x_chunks"), _ptrs(scale_chunks, "scale_chunks"),
+                                    len(x_chunks), bs, h, _QAR_X[x_kind], sdt, _dtype_code(out.dtype),
+                                    _dev(out, "out"), _stream(stream))
+    _check(st)
+    return out
+
+
 def mc2_alltoall_quant_mm_workspace(rank_size: int, bs_local: int, h: int, n: int, x1_quant_mode: int,
                                     x1_dtype: torch.dtype) -> int:
     nbytes = ctypes.c_size_t(0)
@@ -270,10 +307,12 @@ def mc2_device_status() -> int:
 
 __all__ = [
     "Mc2Error", "lib", "library_path", "status_str", "last_error", "mc2_all_gather_mm",
-    "mc2_matmul_reduce_scatter", "mc2_matmul_weight_grad", "mc2_alltoall_quant_mm_workspace", "mc2_alltoall_quant_mm",
+    "mc2_matmul_reduce_scatter", "mc2_matmul_weight_grad", "mc2_quant_all_reduce",
+    "mc2_alltoall_quant_mm_workspace", "mc2_alltoall_quant_mm",
     "mc2_alltoall_quant_mm_no_alloc",
     "NO_ALLOC_SCRATCH_BYTES", "mc2_device_status",
     "MC2_OK", "MC2_ERR_NULL", "MC2_ERR_SHAPE", "MC2_ERR_DTYPE", "MC2_ERR_UNSUPPORTED", "MC2_ERR_WORKSPACE",
     "MC2_ERR_CUDA", "MC2_ERR_TIMEOUT", "MC2_F16", "MC2_BF16", "MC2_F32", "MC2_I8",
+    "MC2_F8E4M3", "MC2_F8E5M2", "MC2_E8M0",
     "QUANT_PERCHANNEL", "QUANT_PERTOKEN", "QUANT_PERTOKEN_DYNAMIC",
 ]

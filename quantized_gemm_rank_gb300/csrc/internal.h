@@ -58,4 +58,11 @@ cudaError_t launch_colsum16(const void *dy, int64_t m, int n, bool bf16, void *d
 // comm_out (optional, NULL for none): the received chunks stacked as
 // (rank_size, bs_local, h) in their own dtype, written by the kernel that reads them.
 
+// QuantAllReduce over `elems` elements (a multiple of 16) of each rank:
+// x_kind 0 int8 / 1 e4m3fn / 2 e5m2; scale_kind 0 fp32 per 128 / 1 e8m0 per 32;
+// out_kind 0 fp32 / 1 fp16 / 2 bf16; ranks 2, 4 or 8.
+cudaError_t launch_quant_all_reduce(const void *const *x_chunks, const void *const *scale_chunks, int ranks,
+                                    int64_t elems, int x_kind, int scale_kind, int out_kind, void *out, int num_sms,
+                                    cudaStream_t stream);
+
 }  // namespace mc2

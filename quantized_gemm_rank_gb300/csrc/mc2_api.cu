@@ -358,6 +358,42 @@ int mc2_matmul_weight_grad(const void *dy, int64_t m, int64_t n, const void *x, 
     return MC2_OK;
 }
 
+int mc2_quant_all_reduce(const void *const *x_chunks, const void *const *scale_chunks, int world_size, int64_t bs,
+                         int64_t h, int x_dtype, int scale_dtype, int out_dtype, void *out, void *stream) {
+    g_last_error[0] = '\0';
+    if (!x_chunks || !scale_chunks || !out) return fail(MC2_ERR_NULL, "x_chunks, scale_chunks and out are required");
+    if (world_size != 2 && world_size != 4 && world_size != 8)
+        return fail(MC2_ERR_SHAPE, "world_size must be 2, 4 or 8 (got %d)", world_size);
+    for (int r = 0; r < world_size; ++r)
+        if (!x_chunks[r] || !scale_chunks[r]) return fail(MC2_ERR_NULL, "x_chunks[%d] or scale_chunks[%d] is NULL", r, r);
+    if (bs < 1) return fail(MC2_ERR_SHAPE, "empty tensors are not supported (bs=%lld)", (long long)bs);
+    if (h < 1024 || h > 8192 || h % 128 != 0)
+        return fail(MC2_ERR_SHAPE, "H must be a multiple of 128 in [1024, 8192] (got %lld)", (long long)h);
+    if (x_dtype != MC2_I8 && x_dtype != MC2_F8E4M3 && x_dtype != MC2_F8E5M2)
+        return fail(MC2_ERR_DTYPE, "x must be MC2_I8, MC2_F8E4M3 or MC2_F8E5M2 (got %d)", x_dtype);
+    if (scale_dtype != MC2_F32 && scale_dtype != MC2_E8M0)
+        return fail(MC2_ERR_DTYPE, "scales must be MC2_F32 or MC2_E8M0 (got %d)", scale_dtype);
+    if (scale_dtype == MC2_E8M0 && x_dtype == MC2_I8)
+        return fail(MC2_ERR_DTYPE, "e8m0 (mx) scales need fp8 x (MC2_F8E4M3 or MC2_F8E5M2)");
+    if (out_dtype != MC2_F32 && out_dtype != MC2_F16 && out_dtype != MC2_BF16)
+        return fail(MC2_ERR_DTYPE, "out must be MC2_F32, MC2_F16 or MC2_BF16 (got %d)", out_dtype);
+    if (bs > INT64_MAX / 8192) return fail(MC2_ERR_SHAPE, "bs too large");
+    for (int r = 0; r < world_size; ++r)
+        if (!aligned16(x_chunks[r]) || !aligned16(scale_chunks[r]))
+            return fail(MC2_ERR_UNSUPPORTED, "x_chunks[%d] and scale_chunks[%d] must be 16-byte aligned", r, r);
+    if (!aligned16(out)) return fail(MC2_ERR_UNSUPPORTED, "out must be 16-byte aligned");
+
+    DeviceInfo dev;
+    if (int st = current_device(&dev)) return st;
+    const int x_kind = x_dtype == MC2_I8 ? 0 : (x_dtype == MC2_F8E4M3 ? 1 : 2);
+    const int out_kind = out_dtype == MC2_F32 ? 0 : (out_dtype == MC2_F16 ? 1 : 2);
+    cudaError_t e = mc2::launch_quant_all_reduce(x_chunks, scale_chunks, world_size, bs * h, x_kind,
+                                                 scale_dtype == MC2_E8M0 ? 1 : 0, out_kind, out, dev.num_sms,
+                                                 static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(MC2_ERR_CUDA, "QuantAllReduce launch: %s", cudaGetErrorString(e));
+    return MC2_OK;
+}
+
 int mc2_alltoall_quant_mm_workspace(int rank_size, int64_t bs_local, int64_t h, int64_t n, int x1_quant_mode,
                                     int x1_dtype, size_t *bytes) {
     g_last_error[0] = '\0';

@@ -6,7 +6,10 @@ Constraints come from "torch_npu.npu_all_gather_base_mm" (参数说明/约束说
 world_size 2/4/8, k in [256, 65535), 2-D fp16/bf16 operands of one dtype) and
 "aclnnAlltoAllQuantMatmul" (约束说明: rankSize 2/4/8, BS and N <= INT32_MAX, no
 empty tensors, non-null x1/x2/x2Scale/output/bias, x1QuantMode 3 or 7,
-x2QuantMode 2, rankSize*H a multiple of 16 in [1, 35000]).
+x2QuantMode 2, rankSize*H a multiple of 16 in [1, 35000]) and "QuantAllReduce"
+(参数说明/约束说明: ranks 2/4/8, x int8 or fp8, scales fp32 or e8m0 with e8m0
+only for fp8 x, output fp32/fp16/bf16, H in [1024, 8192] and 128-aligned, no
+empty tensors).
 """
 import ctypes
 import glob
@@ -229,3 +232,58 @@ def test_binding_refuses_cpu_tensors():
         mc2.mc2_all_gather_mm(x, torch.zeros(256, 64, dtype=torch.bfloat16),
                               out=torch.zeros(32, 64, dtype=torch.bfloat16),
                               gathered=torch.zeros(32, 256, dtype=torch.bfloat16))
+
+
+def qar_call(world_size=2, bs=4, h=1024, x_dtype=mc2.MC2_I8, scale_dtype=mc2.MC2_F32, out_dtype=mc2.MC2_BF16,
+             xs=None, ss=None, out=FAKE):
+    xs = [FAKE] * max(world_size, 1) if xs is None else xs
+    ss = [FAKE] * max(world_size, 1) if ss is None else ss
+    xa = (ctypes.c_void_p * len(xs))(*xs)
+    sa = (ctypes.c_void_p * len(ss))(*ss)
+    return mc2.lib().mc2_quant_all_reduce(xa, sa, world_size, bs, h, x_dtype, scale_dtype, out_dtype, out, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(world_size=3), mc2.MC2_ERR_SHAPE),
+    (dict(world_size=1), mc2.MC2_ERR_SHAPE),
+    (dict(world_size=16), mc2.MC2_ERR_SHAPE),
+    (dict(bs=0), mc2.MC2_ERR_SHAPE),
+    (dict(h=896), mc2.MC2_ERR_SHAPE),
+    (dict(h=8320), mc2.MC2_ERR_SHAPE),
+    (dict(h=1088), mc2.MC2_ERR_SHAPE),
+    (dict(h=1023), mc2.MC2_ERR_SHAPE),
+    (dict(x_dtype=mc2.MC2_BF16), mc2.MC2_ERR_DTYPE),
+    (dict(x_dtype=mc2.MC2_E8M0), mc2.MC2_ERR_DTYPE),
+    (dict(scale_dtype=mc2.MC2_BF16), mc2.MC2_ERR_DTYPE),
+    (dict(x_dtype=mc2.MC2_I8, scale_dtype=mc2.MC2_E8M0), mc2.MC2_ERR_DTYPE),
+    (dict(out_dtype=mc2.MC2_I8), mc2.MC2_ERR_DTYPE),
+    (dict(out_dtype=mc2.MC2_F8E4M3), mc2.MC2_ERR_DTYPE),
+    (dict(out=None), mc2.MC2_ERR_NULL),
+    (dict(xs=[FAKE, None]), mc2.MC2_ERR_NULL),
+    (dict(ss=[None, FAKE]), mc2.MC2_ERR_NULL),
+    (dict(out=FAKE + 8), mc2.MC2_ERR_UNSUPPORTED),
+    (dict(xs=[FAKE, FAKE + 4]), mc2.MC2_ERR_UNSUPPORTED),
+    (dict(ss=[FAKE + 4, FAKE]), mc2.MC2_ERR_UNSUPPORTED),
+])
+def test_quant_all_reduce_rejects(kw, status):
+    assert qar_call(**kw) == status, mc2.last_error()
+    assert mc2.last_error() != ""
+
+
+def test_quant_all_reduce_null_arrays():
+    L = mc2.lib()
+    assert L.mc2_quant_all_reduce(None, None, 2, 4, 1024, mc2.MC2_I8, mc2.MC2_F32, mc2.MC2_BF16, FAKE,
+                                  None) == mc2.MC2_ERR_NULL
+
+
+def test_quant_all_reduce_bounds_accepted_by_validation():
+    if torch.cuda.is_available():
+        pytest.skip("would launch on a real device with fake pointers")
+    # H = 1024 and 8192 are the ends of the page's range; every type pairing
+    # the page allows passes validation (and then fails only for want of a GPU)
+    for h in (1024, 8192):
+        assert qar_call(h=h) == mc2.MC2_ERR_CUDA, mc2.last_error()
+    for xd in (mc2.MC2_F8E4M3, mc2.MC2_F8E5M2):
+        for sd in (mc2.MC2_F32, mc2.MC2_E8M0):
+            for od in (mc2.MC2_F32, mc2.MC2_F16, mc2.MC2_BF16):
+                assert qar_call(world_size=8, x_dtype=xd, scale_dtype=sd, out_dtype=od) == mc2.MC2_ERR_CUDA
