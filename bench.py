@@ -46,10 +46,11 @@ FLUSH_BYTES = 512 << 20
 
 # DRAM bytes (read + write) per launch of the bf16 all-gather GEMM on the
 # ag-8x1024 workload, from the ncu capture summarised in
-# profiles/gemm_bf16_ag-8x1024.md, and the hash of the kernel sources the
-# capture was taken with (the figure is reported only while they match).
-AG_GEMM_TRAFFIC = 289.18e6          # dram__bytes_read.sum 180.24 MB + dram__bytes_write.sum 108.94 MB
-AG_GEMM_TRAFFIC_SRC_HASH = "a216b89705c82ca7"
+# profiles/gemm_bf16_ag-8x1024.md, and the hash of the GEMM's sources
+# (GEMM_SOURCES) the capture was taken with: the figure is reported only
+# while they match.
+AG_GEMM_TRAFFIC = 286.80e6          # dram__bytes_read.sum 177.04 MB + dram__bytes_write.sum 109.77 MB
+AG_GEMM_TRAFFIC_SRC_HASH = "5d0b2599e5dd6105"
 
 
 def parse_args():
@@ -61,13 +62,19 @@ def parse_args():
     ap.add_argument("--no-extra", action="store_true", help="skip the per-workload table")
     ap.add_argument("--profile", action="store_true",
                     help="only the timed steps (no e2e, per-workload table or CPU baseline): for ncu")
+    ap.add_argument("--workload", default=None, choices=sorted(mc2_inputs.WORKLOADS),
+                    help="with --profile: time only this workload's call")
     return ap.parse_args()
 
 
-def kernel_src_hash() -> str:
+GEMM_SOURCES = ("gemm_tcgen05.cuh", "gemm_kernels.cu", "sm103_ptx.cuh")
+
+
+def kernel_src_hash(names=GEMM_SOURCES) -> str:
+    """Hash of the sources that define the measured kernel (the GEMM by default)."""
     h = hashlib.sha256()
     d = os.path.join(ROOT, "quantized_gemm_rank_gb300", "csrc")
-    for name in sorted(os.listdir(d)):
+    for name in sorted(names):
         with open(os.path.join(d, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
@@ -348,67 +355,81 @@ def run_reference(args):
 
 
 # ----------------------------------------------------------------------------- main
+def workload_call(s, dev):
+    """Device-resident inputs of one workload and a closure that runs its call.
+    Returns (fn, work, unit): work is FLOPs (or OPs) for the GEMMs, bytes for
+    the HBM-bound QuantAllReduce."""
+    import quantized_gemm_rank_gb300 as mc2
+    if isinstance(s, mc2_inputs.QARShape):
+        inp = mc2_inputs.qar_inputs(s, seed=0)
+        xs = [x.to(dev) for x in inp["x_chunks"]]
+        ss = [x.to(dev) for x in inp["scale_chunks"]]
+        out = torch.empty((s.bs, s.h), dtype=s.out_dtype, device=dev)
+        return (lambda: mc2.mc2_quant_all_reduce(xs, ss, x_kind=s.x_kind, out_dtype=s.out_dtype, out=out)), \
+            s.bytes, "bytes"
+    if isinstance(s, mc2_inputs.AGShape):
+        inp = mc2_inputs.ag_inputs(s, seed=0)
+        ch = [c.to(dev) for c in inp["chunks"]]
+        x2 = inp["x2"].to(dev)
+        b = None if inp["bias"] is None else inp["bias"].to(dev)
+        out = torch.empty((s.m, s.n), dtype=s.dtype, device=dev)
+        g = torch.empty((s.m, s.k), dtype=s.dtype, device=dev)
+        return (lambda: mc2.mc2_all_gather_mm(ch, x2, x2_is_nk=s.x2_is_nk, bias=b, out=out, gathered=g)), \
+            s.flops, "flops"
+    if isinstance(s, mc2_inputs.WGradShape):
+        inp = mc2_inputs.wgrad_inputs(s, seed=0)
+        dy, x = inp["dy"].to(dev), inp["x"].to(dev)
+        dwo = torch.empty((s.n, s.k), dtype=s.dtype, device=dev)
+        dbo = torch.empty((s.n,), dtype=s.dtype, device=dev)
+        return (lambda: mc2.mc2_matmul_weight_grad(dy, x, dw=dwo, db=dbo)), s.flops, "flops"
+    if isinstance(s, mc2_inputs.MMRSShape):
+        inp = mc2_inputs.mmrs_inputs(s, seed=0)
+        xs = [x.to(dev) for x in inp["x_chunks"]]
+        ws = [w.to(dev) for w in inp["w_chunks"]]
+        b = None if inp["bias"] is None else inp["bias"].to(dev)
+        outs = [torch.empty((s.m // s.world_size, s.n), dtype=s.dtype, device=dev) for _ in range(s.world_size)]
+        return (lambda: mc2.mc2_matmul_reduce_scatter(xs, ws, w_is_nk=s.w_is_nk, bias=b, out_chunks=outs)), \
+            s.flops, "flops"
+    inp = mc2_inputs.a2a_inputs(s, seed=0)
+    ch = [c.to(dev) for c in inp["chunks"]]
+    x1s = None if inp["x1_scale"] is None else inp["x1_scale"].to(dev)
+    x2, x2s, b = inp["x2"].to(dev), inp["x2_scale"].to(dev), inp["bias"].to(dev)
+    out = torch.empty((s.bs_local, s.n), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(mc2.mc2_alltoall_quant_mm_workspace(s.rank_size, s.bs_local, s.h, s.n, s.quant_mode,
+                                                         ch[0].dtype), dtype=torch.uint8, device=dev)
+    return (lambda: mc2.mc2_alltoall_quant_mm(ch, x2, x2s, b, x1_quant_mode=s.quant_mode, x1_scale=x1s, out=out,
+                                              workspace=ws)), s.ops, "flops"
+
+
 def extra_table(dev, flush, stream, steps, hbm_peak):
     """Per-workload device times of each call alone (every workload but the step's two);
     the HBM-bound QuantAllReduce workloads report GB/s against the HBM peak."""
-    import quantized_gemm_rank_gb300 as mc2
     res = {}
     for name, s in mc2_inputs.WORKLOADS.items():
         if name in (AG_NAME, A2A_NAME):
             continue
-        if isinstance(s, mc2_inputs.AGShape):
-            inp = mc2_inputs.ag_inputs(s, seed=0)
-            ch = [c.to(dev) for c in inp["chunks"]]
-            x2 = inp["x2"].to(dev)
-            b = None if inp["bias"] is None else inp["bias"].to(dev)
-            out = torch.empty((s.m, s.n), dtype=s.dtype, device=dev)
-            g = torch.empty((s.m, s.k), dtype=s.dtype, device=dev)
-            fn = lambda: mc2.mc2_all_gather_mm(ch, x2, x2_is_nk=s.x2_is_nk, bias=b, out=out, gathered=g)  # noqa
-            fl = s.flops
-        elif isinstance(s, mc2_inputs.WGradShape):
-            inp = mc2_inputs.wgrad_inputs(s, seed=0)
-            ch = inp["dy"].to(dev)
-            wc = inp["x"].to(dev)
-            dwo = torch.empty((s.n, s.k), dtype=s.dtype, device=dev)
-            dbo = torch.empty((s.n,), dtype=s.dtype, device=dev)
-            fn = lambda: mc2.mc2_matmul_weight_grad(ch, wc, dw=dwo, db=dbo)  # noqa
-            fl = s.flops
-        elif isinstance(s, mc2_inputs.QARShape):
-            inp = mc2_inputs.qar_inputs(s, seed=0)
-            ch = [x.to(dev) for x in inp["x_chunks"]]
-            wc = [x.to(dev) for x in inp["scale_chunks"]]
-            out = torch.empty((s.bs, s.h), dtype=s.out_dtype, device=dev)
-            fn = lambda: mc2.mc2_quant_all_reduce(ch, wc, x_kind=s.x_kind, out_dtype=s.out_dtype, out=out)  # noqa
-            t = statistics.median(time_device(fn, steps, 3, flush, stream))
-            gbs = s.bytes / (t * 1e-3) / 1e9
-            res[name] = {"us": round(t * 1e3, 2), "gbs": round(gbs, 1), "hbm_frac": round(gbs / hbm_peak, 4)}
-            del inp, ch
-            torch.cuda.empty_cache()
-            continue
-        elif isinstance(s, mc2_inputs.MMRSShape):
-            inp = mc2_inputs.mmrs_inputs(s, seed=0)
-            ch = [x.to(dev) for x in inp["x_chunks"]]
-            wc = [w.to(dev) for w in inp["w_chunks"]]
-            b = None if inp["bias"] is None else inp["bias"].to(dev)
-            outs = [torch.empty((s.m // s.world_size, s.n), dtype=s.dtype, device=dev) for _ in range(s.world_size)]
-            fn = lambda: mc2.mc2_matmul_reduce_scatter(ch, wc, w_is_nk=s.w_is_nk, bias=b, out_chunks=outs)  # noqa
-            fl = s.flops
-        else:
-            inp = mc2_inputs.a2a_inputs(s, seed=0)
-            ch = [c.to(dev) for c in inp["chunks"]]
-            x1s = None if inp["x1_scale"] is None else inp["x1_scale"].to(dev)
-            x2, x2s, b = inp["x2"].to(dev), inp["x2_scale"].to(dev), inp["bias"].to(dev)
-            out = torch.empty((s.bs_local, s.n), dtype=torch.bfloat16, device=dev)
-            ws = torch.empty(mc2.mc2_alltoall_quant_mm_workspace(s.rank_size, s.bs_local, s.h, s.n, s.quant_mode,
-                                                                 ch[0].dtype), dtype=torch.uint8, device=dev)
-            fn = lambda: mc2.mc2_alltoall_quant_mm(ch, x2, x2s, b, x1_quant_mode=s.quant_mode,  # noqa
-                                                   x1_scale=x1s, out=out, workspace=ws)
-            fl = s.ops
+        fn, work, unit = workload_call(s, dev)
         t = statistics.median(time_device(fn, steps, 3, flush, stream))
-        res[name] = {"us": round(t * 1e3, 2), "tflops": round(fl / (t * 1e-3) / 1e12, 1)}
-        del inp, ch
+        if unit == "bytes":
+            gbs = work / (t * 1e-3) / 1e9
+            res[name] = {"us": round(t * 1e3, 2), "gbs": round(gbs, 1), "hbm_frac": round(gbs / hbm_peak, 4)}
+        else:
+            res[name] = {"us": round(t * 1e3, 2), "tflops": round(work / (t * 1e-3) / 1e12, 1)}
+        del fn
         torch.cuda.empty_cache()
     return res
+
+
+def profile_workload(name, args):
+    """--profile --workload NAME: only W + K calls of that workload (for ncu)."""
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    fn, work, unit = workload_call(mc2_inputs.WORKLOADS[name], dev)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    t = statistics.median(time_device(fn, args.steps, args.warmup, flush, stream))
+    print(json.dumps({"workload": name, "ms": round(t, 4), "work": work, "unit": unit}), flush=True)
+    return 0
 
 
 def main():
@@ -417,6 +438,8 @@ def main():
         return run_reference(args)
     if args.warmup < 3:
         args.warmup = 3
+    if args.profile and args.workload:
+        return profile_workload(args.workload, args)
     rank, world, local = dist_setup(args.gpus)
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)

@@ -125,6 +125,17 @@ cudaError_t launch_gemm(GemmKind kind, int group, const GemmParams &p, int num_s
     return cudaErrorInvalidValue;
 }
 
+int *device_status_word() {
+    static int *addr[64] = {nullptr};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+    if (dev < 64 && addr[dev]) return addr[dev];
+    int *p = nullptr;
+    if (cudaGetSymbolAddress(reinterpret_cast<void **>(&p), g_gemm_status) != cudaSuccess) return nullptr;
+    if (dev < 64) addr[dev] = p;
+    return p;
+}
+
 int read_and_clear_gemm_status(int *status) {
     int zero = 0;
     cudaError_t e = cudaMemcpyFromSymbol(status, g_gemm_status, sizeof(int));

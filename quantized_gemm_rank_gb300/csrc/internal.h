@@ -28,6 +28,8 @@ int gemm_units(GemmKind kind, int group, int num_sms);
 constexpr int kSkMaxUnits = 76;
 cudaError_t launch_gemm(GemmKind kind, int group, const GemmParams &p, int num_sms, cudaStream_t stream);
 int read_and_clear_gemm_status(int *status);
+// Device address of the status word that bounded waits set to -7 (cached per device).
+int *device_status_word();
 
 // Records `msg` as this thread's mc2_last_error() text and returns `status`.
 int record_error(int status, const char *msg);
@@ -42,7 +44,7 @@ bool a2a_prologue_fits(int rank_size, int64_t bs_local, int h);
 cudaError_t launch_a2a_prologue(const ChunkPtrs &chunks, int rank_size, int64_t bs_local, int h, bool bf16,
                                 const void *smooth, __half *qh, int8_t *q_out, float *scale_out, const int8_t *x2,
                                 __half *x2h, int64_t x2_count, int *zero_words, int n_zero, void *comm_out,
-                                cudaStream_t stream);
+                                int *status, uint64_t wait_limit_ns, cudaStream_t stream);
 // Also sets zero_words[0, n_zero) to 0 (the GEMM's stream-K counters).
 cudaError_t launch_widen_i8(const int8_t *src, __half *dst, int64_t count, int num_sms, int *zero_words, int n_zero,
                             cudaStream_t stream);

@@ -464,7 +464,8 @@ int mc2_alltoall_quant_mm(const void *const *chunks, int rank_size, int64_t bs_l
     bool x2_done = false;
     if (x1_quant_mode == MC2_QUANT_PERTOKEN_DYNAMIC && mc2::a2a_prologue_fits(rank_size, bs_local, static_cast<int>(h))) {
         e = mc2::launch_a2a_prologue(cp, rank_size, bs_local, static_cast<int>(h), x1_dtype == MC2_BF16, x1_scale, ah,
-                                     q_out, scale, x2, x2h, K * n, sk_flags, n_flags, alltoall_out, s);
+                                     q_out, scale, x2, x2h, K * n, sk_flags, n_flags, alltoall_out,
+                                     mc2::device_status_word(), kWaitLimitNs, s);
         x2_done = true;
     } else if (x1_quant_mode == MC2_QUANT_PERTOKEN_DYNAMIC) {
         e = mc2::launch_quant_pertoken(cp, rank_size, bs_local, static_cast<int>(h), x1_dtype == MC2_BF16, x1_scale,

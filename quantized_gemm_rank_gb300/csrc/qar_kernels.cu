@@ -11,8 +11,8 @@
 // The products are added in rank order by fp32 fused multiply-adds and the sum
 // is rounded once (nearest-even) to the output type.
 //
-// HBM-bound: each rank's codes are read once (16-byte streaming loads, one per
-// rank in flight per thread), the output written once.  Because G divides H,
+// HBM-bound: each rank's codes are read once (16-byte streaming loads, one or
+// two per rank in flight per thread), the output written once.  Because G divides H,
 // the scale of flat element e is scales_r[e / G] whatever the row, so the
 // kernel runs over the flat (bs * H) range with no row arithmetic.
 #include <cuda_bf16.h>
@@ -75,57 +75,83 @@ struct QarPtrs {
     const void *s[8];
 };
 
+// One vector: 16 elements of every rank, summed and stored.
+template <int kX, int kS, int kOut, int kR>
+__device__ __forceinline__ void reduce_store(const uint4 (&xv)[kR], const float (&sc)[kR], void *__restrict__ out,
+                                             int64_t v) {
+    float acc[kVec];
+#pragma unroll
+    for (int i = 0; i < kVec; ++i) acc[i] = 0.0f;   // the sum starts at +0, as the reduction's definition
+#pragma unroll
+    for (int r = 0; r < kR; ++r) {
+        float f[kVec];
+        if constexpr (kX == 0)
+            decode_i8(xv[r], f);
+        else
+            decode_f8<kX == 2>(xv[r], f);
+#pragma unroll
+        for (int i = 0; i < kVec; ++i) acc[i] = __fmaf_rn(f[i], sc[r], acc[i]);
+    }
+    if constexpr (kOut == 0) {
+        float4 *o = reinterpret_cast<float4 *>(out) + v * 4;
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            __stcs(o + q, make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]));
+    } else {
+        uint32_t w[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            if constexpr (kOut == 1) {
+                const __half2 h2 = __floats2half2_rn(acc[2 * i], acc[2 * i + 1]);
+                w[i] = *reinterpret_cast<const uint32_t *>(&h2);
+            } else {
+                const __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
+                w[i] = *reinterpret_cast<const uint32_t *>(&b2);
+            }
+        }
+        uint4 *o = reinterpret_cast<uint4 *>(out) + v * 2;
+        __stcs(o, make_uint4(w[0], w[1], w[2], w[3]));
+        __stcs(o + 1, make_uint4(w[4], w[5], w[6], w[7]));
+    }
+}
+
+template <int kS, int kR>
+__device__ __forceinline__ void load_vec(const QarPtrs &p, int64_t v, uint4 (&xv)[kR], float (&sc)[kR]) {
+#pragma unroll
+    for (int r = 0; r < kR; ++r) xv[r] = __ldcs(reinterpret_cast<const uint4 *>(p.x[r]) + v);
+#pragma unroll
+    for (int r = 0; r < kR; ++r) {
+        if constexpr (kS == 0)
+            sc[r] = __ldg(static_cast<const float *>(p.s[r]) + (v >> 3));                  // G = 128 = 8 vectors
+        else
+            sc[r] = decode_e8m0(__ldg(static_cast<const uint8_t *>(p.s[r]) + (v >> 1)));  // G = 32
+    }
+}
+
 // kX: 0 int8, 1 e4m3fn, 2 e5m2.  kS: 0 fp32 per 128, 1 e8m0 per 32.
-// kOut: 0 fp32, 1 fp16, 2 bf16.  kR: ranks.
+// kOut: 0 fp32, 1 fp16, 2 bf16.  kR: ranks.  With int8 codes each thread
+// takes two vectors per step (v and v + stride, the loads of both in flight
+// before either is reduced); the fp8 decode needs more registers, and there
+// one vector per step keeps more threads resident.
 template <int kX, int kS, int kOut, int kR>
 __global__ void __launch_bounds__(kThreads) quant_all_reduce_kernel(QarPtrs p, int64_t nvec, void *__restrict__ out) {
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
-    for (int64_t v = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; v < nvec; v += stride) {
-        uint4 xv[kR];
-        float sc[kR];
-#pragma unroll
-        for (int r = 0; r < kR; ++r) xv[r] = __ldcs(reinterpret_cast<const uint4 *>(p.x[r]) + v);
-#pragma unroll
-        for (int r = 0; r < kR; ++r) {
-            if constexpr (kS == 0)
-                sc[r] = __ldg(static_cast<const float *>(p.s[r]) + (v >> 3));           // G = 128 = 8 vectors
-            else
-                sc[r] = decode_e8m0(__ldg(static_cast<const uint8_t *>(p.s[r]) + (v >> 1)));  // G = 32
+    int64_t v = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
+    if constexpr (kX == 0) {
+        for (; v + stride < nvec; v += 2 * stride) {
+            uint4 xa[kR], xb[kR];
+            float sa[kR], sb[kR];
+            load_vec<kS, kR>(p, v, xa, sa);
+            load_vec<kS, kR>(p, v + stride, xb, sb);
+            reduce_store<kX, kS, kOut, kR>(xa, sa, out, v);
+            reduce_store<kX, kS, kOut, kR>(xb, sb, out, v + stride);
         }
-        float acc[kVec];
-#pragma unroll
-        for (int i = 0; i < kVec; ++i) acc[i] = 0.0f;   // the sum starts at +0, as the reduction's definition
-#pragma unroll
-        for (int r = 0; r < kR; ++r) {
-            float f[kVec];
-            if constexpr (kX == 0)
-                decode_i8(xv[r], f);
-            else
-                decode_f8<kX == 2>(xv[r], f);
-#pragma unroll
-            for (int i = 0; i < kVec; ++i) acc[i] = __fmaf_rn(f[i], sc[r], acc[i]);
-        }
-        if constexpr (kOut == 0) {
-            float4 *o = reinterpret_cast<float4 *>(out) + v * 4;
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-                __stcs(o + q, make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]));
-        } else {
-            uint32_t w[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                if constexpr (kOut == 1) {
-                    const __half2 h2 = __floats2half2_rn(acc[2 * i], acc[2 * i + 1]);
-                    w[i] = *reinterpret_cast<const uint32_t *>(&h2);
-                } else {
-                    const __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
-                    w[i] = *reinterpret_cast<const uint32_t *>(&b2);
-                }
-            }
-            uint4 *o = reinterpret_cast<uint4 *>(out) + v * 2;
-            __stcs(o, make_uint4(w[0], w[1], w[2], w[3]));
-            __stcs(o + 1, make_uint4(w[4], w[5], w[6], w[7]));
-        }
+    }
+    for (; v < nvec; v += stride) {
+        uint4 xa[kR];
+        float sa[kR];
+        load_vec<kS, kR>(p, v, xa, sa);
+        reduce_store<kX, kS, kOut, kR>(xa, sa, out, v);
     }
 }
 

@@ -147,11 +147,13 @@ __global__ void __launch_bounds__(256) quant_pertoken_kernel(const __grid_consta
 
 // ---------------------------------------------------------------------------
 // Fused prologue of the dynamic-quant scenario, for h % 8 == 0 and
-// rank_size*h <= 512*64: one launch whose CTAs take one of two roles,
+// rank_size*h <= 32768: one launch whose CTAs take one of two roles,
 // interleaved so that both run side by side on every SM --
-//   * quant CTAs (one per permuted row): the row stays in registers (kV 16-byte
-//     vectors per thread, vector v of thread i = permuted columns
-//     (v*blockDim + i)*8 .. +7), so it is read from HBM once;
+//   * quant CTAs (one per permuted row t): one thread copies the row's
+//     rank_size pieces chunk_r[t, 0:h] into shared memory with bulk async
+//     copies, which lays them out as the permuted row P[t, :] (piece r at
+//     columns r*h ..); both passes then read the row from shared memory, so a
+//     CTA holds no row in registers and many rows are in flight per SM;
 //   * widen CTAs: a contiguous slice of x2, int8 -> fp16; their number follows
 //     the size of x2 (about four 16-byte vectors per thread), and CTA b is a
 //     widen CTA when floor((b+1)W/G) > floor(bW/G) (W widen CTAs of G), which
@@ -170,6 +172,7 @@ __global__ void __launch_bounds__(256) quant_pertoken_kernel(const __grid_consta
 // keeps k inside [-127, 127], and the low byte of fl(qa + M) is k mod 256,
 // i.e. the int8 q.
 constexpr float kRoundMagic = 12582912.0f;  // 1.5 * 2^23
+constexpr int kPrologueThreads = 128;
 
 template <bool kBF16>
 __device__ __forceinline__ float2 unpack2(uint32_t w) {
@@ -180,17 +183,21 @@ __device__ __forceinline__ float2 unpack2(uint32_t w) {
     }
 }
 
-template <bool kBF16, int kV>
-__global__ void __launch_bounds__(512) a2a_prologue_kernel(const __grid_constant__ ChunkPtrs chunks, int h,
-                                                           int64_t bs_local, int rank_size,
-                                                           const uint16_t *__restrict__ smooth,
-                                                           __half *__restrict__ qh, int8_t *__restrict__ q_out,
-                                                           float *__restrict__ scale_out,
-                                                           const int8_t *__restrict__ x2,
-                                                           __half *__restrict__ x2h, int64_t x2_vecs,
-                                                           int64_t widen_ctas, int *__restrict__ zero_words,
-                                                           int n_zero, uint16_t *__restrict__ comm_out) {
-    ptx::allow_dependent_launch();
+template <bool kBF16>
+__device__ __forceinline__ uint4 smooth_vec(const uint16_t *smooth, int vi) {
+    if (smooth) return __ldg(reinterpret_cast<const uint4 *>(smooth + vi * 8));
+    return kBF16 ? make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u)    // bf16 1.0
+                 : make_uint4(0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u);   // fp16 1.0
+}
+
+template <bool kBF16>
+__global__ void __launch_bounds__(kPrologueThreads) a2a_prologue_kernel(
+    const __grid_constant__ ChunkPtrs chunks, int h, int64_t bs_local, int rank_size,
+    const uint16_t *__restrict__ smooth, __half *__restrict__ qh, int8_t *__restrict__ q_out,
+    float *__restrict__ scale_out, const int8_t *__restrict__ x2, __half *__restrict__ x2h, int64_t x2_vecs,
+    int64_t widen_ctas, int *__restrict__ zero_words, int n_zero, uint16_t *__restrict__ comm_out, int *status,
+    uint64_t wait_limit_ns) {
+    extern __shared__ __align__(128) uint8_t prow[];   // the permuted row (K bf16/fp16), then its mbarrier
     const int64_t b = blockIdx.x;
     // the GEMM's stream-K counters start at zero (it runs after this kernel)
     if (b == gridDim.x - 1)
@@ -224,48 +231,48 @@ __global__ void __launch_bounds__(512) a2a_prologue_kernel(const __grid_constant
                 reinterpret_cast<uint4 *>(x2h)[2 * i + 1] = o[1];
             }
         }
+        ptx::allow_dependent_launch();
         return;
     }
     // ---- quant role: permuted row t
     const int64_t t = b - before;
-    if (t >= bs_local) return;
+    if (t >= bs_local) {
+        ptx::allow_dependent_launch();
+        return;
+    }
     __shared__ float red[32];
     const int K = rank_size * h;
     const int nvec = K / 8;
-    uint4 xv[kV];
-#pragma unroll
-    for (int v = 0; v < kV; ++v) {
-        const int vi = v * blockDim.x + threadIdx.x;
-        xv[v] = make_uint4(0, 0, 0, 0);
-        if (vi < nvec) {
+    const uint32_t row_s = ptx::smem_u32(prow);
+    const uint32_t bar = row_s + static_cast<uint32_t>(K) * 2u;   // K * 2 is a multiple of 16
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(bar, 1);
+        ptx::fence_proxy_async_smem();
+        ptx::mbar_arrive_expect_tx(bar, static_cast<uint32_t>(K) * 2u);
+        for (int r = 0; r < rank_size; ++r)
+            ptx::bulk_load_1d(row_s + static_cast<uint32_t>(r * h) * 2u,
+                              static_cast<const uint16_t *>(chunks.p[r]) + t * h, static_cast<uint32_t>(h) * 2u, bar);
+    }
+    __syncthreads();   // the barrier is initialised before anyone polls it
+    if (!ptx::mbar_wait(bar, 0, wait_limit_ns)) {
+        if (threadIdx.x == 0 && status) atomicExch(status, -7);
+        return;
+    }
+    const uint4 *rowv = reinterpret_cast<const uint4 *>(prow);
+    // commOut: the received pieces in their own layout (rank_size, bs_local, h)
+    if (comm_out) {
+        for (int vi = threadIdx.x; vi < nvec; vi += blockDim.x) {
             const int c = vi * 8;
             const int r = c / h;
-            xv[v] = __ldg(reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(chunks.p[r]) + t * h +
-                                                          (c - r * h)));
-        }
-    }
-    // commOut, once every load of the row is in flight (a store right after each
-    // load would wait for it before the next load issues)
-    if (comm_out) {
-#pragma unroll
-        for (int v = 0; v < kV; ++v) {
-            const int vi = v * blockDim.x + threadIdx.x;
-            if (vi < nvec) {
-                const int c = vi * 8;
-                const int r = c / h;
-                *reinterpret_cast<uint4 *>(comm_out + (r * bs_local + t) * h + (c - r * h)) = xv[v];
-            }
+            *reinterpret_cast<uint4 *>(comm_out + (r * bs_local + t) * h + (c - r * h)) = rowv[vi];
         }
     }
     // y = x * s (fp32, exact for 16-bit inputs); row absmax
     float amax = 0.0f;
-#pragma unroll
-    for (int v = 0; v < kV; ++v) {
-        const int vi = v * blockDim.x + threadIdx.x;
-        const uint32_t *xw = reinterpret_cast<const uint32_t *>(&xv[v]);
-        uint4 sv = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);  // bf16 1.0
-        if (!kBF16) sv = make_uint4(0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u);  // fp16 1.0
-        if (smooth && vi < nvec) sv = __ldg(reinterpret_cast<const uint4 *>(smooth + vi * 8));
+    for (int vi = threadIdx.x; vi < nvec; vi += blockDim.x) {
+        const uint4 xv = rowv[vi];
+        const uint4 sv = smooth_vec<kBF16>(smooth, vi);
+        const uint32_t *xw = reinterpret_cast<const uint32_t *>(&xv);
         const uint32_t *sw = reinterpret_cast<const uint32_t *>(&sv);
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -281,14 +288,10 @@ __global__ void __launch_bounds__(512) a2a_prologue_kernel(const __grid_constant
     const float2 rcp2 = make_float2(rcp, rcp);
     const float2 magic2 = make_float2(kRoundMagic, kRoundMagic);
     const float2 nmagic2 = make_float2(-kRoundMagic, -kRoundMagic);
-#pragma unroll
-    for (int v = 0; v < kV; ++v) {
-        const int vi = v * blockDim.x + threadIdx.x;
-        if (vi >= nvec) continue;
-        const uint32_t *xw = reinterpret_cast<const uint32_t *>(&xv[v]);
-        uint4 sv = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
-        if (!kBF16) sv = make_uint4(0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u);
-        if (smooth) sv = __ldg(reinterpret_cast<const uint4 *>(smooth + vi * 8));
+    for (int vi = threadIdx.x; vi < nvec; vi += blockDim.x) {
+        const uint4 xv = rowv[vi];
+        const uint4 sv = smooth_vec<kBF16>(smooth, vi);
+        const uint32_t *xw = reinterpret_cast<const uint32_t *>(&xv);
         const uint32_t *sw = reinterpret_cast<const uint32_t *>(&sv);
         uint4 hv;
         __half2 *hh = reinterpret_cast<__half2 *>(&hv);
@@ -320,12 +323,16 @@ __global__ void __launch_bounds__(512) a2a_prologue_kernel(const __grid_constant
             *reinterpret_cast<uint2 *>(q_out + t * K + vi * 8) = iv;
         }
     }
+    // The GEMM that follows is launched once every CTA of this grid has got here
+    // (it still waits for the whole grid to finish before reading): triggering
+    // at the end, not the start, keeps its CTAs, which need a whole SM, from
+    // taking SMs that the remaining CTAs of this grid still need.
+    ptx::allow_dependent_launch();
 }
 
 // int8 -> fp16, exact, 16 elements per thread-iteration.
 __global__ void __launch_bounds__(256) widen_i8_kernel(const int8_t *__restrict__ src, __half *__restrict__ dst,
                                                        int64_t count, int *__restrict__ zero_words, int n_zero) {
-    ptx::allow_dependent_launch();
     // the GEMM's stream-K counters start at zero (it runs after this kernel)
     if (blockIdx.x == 0)
         for (int i = threadIdx.x; i < n_zero; i += blockDim.x) zero_words[i] = 0;
@@ -343,6 +350,8 @@ __global__ void __launch_bounds__(256) widen_i8_kernel(const int8_t *__restrict_
     }
     for (int64_t i = nvec * 16 + static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < count; i += stride)
         dst[i] = __int2half_rn(src[i]);
+    // the GEMM that follows launches once every CTA got here (see a2a_prologue_kernel)
+    ptx::allow_dependent_launch();
 }
 
 // Each rank's int8 chunk -> fp16 in its own layout (dst + r * bs_local * h), so
@@ -458,12 +467,12 @@ bool a2a_prologue_fits(int rank_size, int64_t bs_local, int h) {
 cudaError_t launch_a2a_prologue(const ChunkPtrs &chunks, int rank_size, int64_t bs_local, int h, bool bf16,
                                 const void *smooth, __half *qh, int8_t *q_out, float *scale_out, const int8_t *x2,
                                 __half *x2h, int64_t x2_count, int *zero_words, int n_zero, void *comm_out,
-                                cudaStream_t stream) {
+                                int *status, uint64_t wait_limit_ns, cudaStream_t stream) {
     uint16_t *co = static_cast<uint16_t *>(comm_out);
-    constexpr int kV = 8;
     const int K = rank_size * h;
-    int threads = 64;
-    while (threads * kV * 8 < K) threads *= 2;
+    constexpr int threads = kPrologueThreads;
+    // the permuted row and its mbarrier
+    const size_t smem = static_cast<size_t>(K) * 2 + 16;
     // one quant CTA per row; widen CTAs for ~4 vectors per thread
     const int64_t x2_vecs = x2_count / 16;
     int64_t widen_ctas = (x2_vecs + 4ll * threads - 1) / (4ll * threads);
@@ -471,14 +480,17 @@ cudaError_t launch_a2a_prologue(const ChunkPtrs &chunks, int rank_size, int64_t 
     if (widen_ctas > (1ll << 30)) widen_ctas = 1ll << 30;
     const int64_t grid = bs_local + widen_ctas;
     const uint16_t *sm = static_cast<const uint16_t *>(smooth);
-    if (bf16)
-        a2a_prologue_kernel<true, kV><<<static_cast<unsigned>(grid), threads, 0, stream>>>(
-            chunks, h, bs_local, rank_size, sm, qh, q_out, scale_out, x2, x2h, x2_vecs, widen_ctas, zero_words,
-            n_zero, co);
-    else
-        a2a_prologue_kernel<false, kV><<<static_cast<unsigned>(grid), threads, 0, stream>>>(
-            chunks, h, bs_local, rank_size, sm, qh, q_out, scale_out, x2, x2h, x2_vecs, widen_ctas, zero_words,
-            n_zero, co);
+    auto kern = bf16 ? a2a_prologue_kernel<true> : a2a_prologue_kernel<false>;
+    // rows above 48 KiB need the opt-in (raised once per process and type)
+    static size_t opted[2] = {48 * 1024, 48 * 1024};
+    if (smem > opted[bf16 ? 1 : 0]) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024 + 16);
+        if (e != cudaSuccess) return e;
+        opted[bf16 ? 1 : 0] = 64 * 1024 + 16;
+    }
+    kern<<<static_cast<unsigned>(grid), threads, smem, stream>>>(chunks, h, bs_local, rank_size, sm, qh, q_out,
+                                                                 scale_out, x2, x2h, x2_vecs, widen_ctas, zero_words,
+                                                                 n_zero, co, status, wait_limit_ns);
     return cudaGetLastError();
 }
 
