@@ -30,6 +30,30 @@ __device__ __forceinline__ float to_f32(uint16_t v) {
     }
 }
 
+// Four int8 values (one 32-bit word) -> four exact fp16 values, without a
+// conversion instruction: flipping the sign bits gives x + 128 in [0, 255];
+// as the low mantissa byte under the fp16 exponent of 1024 (0x64) that is
+// the half 1024 + x + 128, and subtracting 1152 (0x6480) leaves x exactly.
+__device__ __forceinline__ uint2 i8x4_to_f16x4(uint32_t w) {
+    const uint32_t b = w ^ 0x80808080u;
+    const uint32_t lo = __byte_perm(b, 0x64646464u, 0x4140u);   // halves 1024 + b0, 1024 + b1
+    const uint32_t hi = __byte_perm(b, 0x64646464u, 0x4342u);   // halves 1024 + b2, 1024 + b3
+    const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
+    const __half2 l = __hsub2(*reinterpret_cast<const __half2 *>(&lo), bias);
+    const __half2 h = __hsub2(*reinterpret_cast<const __half2 *>(&hi), bias);
+    return make_uint2(*reinterpret_cast<const uint32_t *>(&l), *reinterpret_cast<const uint32_t *>(&h));
+}
+
+// 16 int8 values -> 16 fp16 values (two 16-byte vectors).
+__device__ __forceinline__ void i8x16_to_f16x16(const int4 &v, uint4 (&o)[2]) {
+    const uint2 a = i8x4_to_f16x4(static_cast<uint32_t>(v.x));
+    const uint2 b = i8x4_to_f16x4(static_cast<uint32_t>(v.y));
+    const uint2 c = i8x4_to_f16x4(static_cast<uint32_t>(v.z));
+    const uint2 d = i8x4_to_f16x4(static_cast<uint32_t>(v.w));
+    o[0] = make_uint4(a.x, a.y, b.x, b.y);
+    o[1] = make_uint4(c.x, c.y, d.x, d.y);
+}
+
 __device__ __forceinline__ float block_max(float v, float *red) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
@@ -221,12 +245,8 @@ __global__ void __launch_bounds__(kPrologueThreads) a2a_prologue_kernel(
             for (int u = 0; u < 4; ++u) {
                 const int64_t i = i0 + u * blockDim.x;
                 if (i >= end) break;
-                const int8_t *e = reinterpret_cast<const int8_t *>(&v[u]);
                 uint4 o[2];
-                __half2 *oh = reinterpret_cast<__half2 *>(o);
-#pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    oh[j] = __floats2half2_rn(static_cast<float>(e[2 * j]), static_cast<float>(e[2 * j + 1]));
+                i8x16_to_f16x16(v[u], o);
                 reinterpret_cast<uint4 *>(x2h)[2 * i] = o[0];
                 reinterpret_cast<uint4 *>(x2h)[2 * i + 1] = o[1];
             }
@@ -340,11 +360,8 @@ __global__ void __launch_bounds__(256) widen_i8_kernel(const int8_t *__restrict_
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < nvec; i += stride) {
         const int4 v = __ldg(reinterpret_cast<const int4 *>(src) + i);
-        const int8_t *e = reinterpret_cast<const int8_t *>(&v);
         uint4 o[2];
-        uint16_t *oe = reinterpret_cast<uint16_t *>(o);
-#pragma unroll
-        for (int j = 0; j < 16; ++j) oe[j] = __half_as_ushort(__int2half_rn(e[j]));
+        i8x16_to_f16x16(v, o);
         reinterpret_cast<uint4 *>(dst)[2 * i] = o[0];
         reinterpret_cast<uint4 *>(dst)[2 * i + 1] = o[1];
     }
@@ -371,12 +388,8 @@ __global__ void __launch_bounds__(256) widen_chunks_i8_kernel(const __grid_const
         const int r = static_cast<int>(i / per_chunk);
         const int64_t li = i - r * per_chunk;
         const int4 v = __ldg(reinterpret_cast<const int4 *>(chunks.p[r]) + li);
-        const int8_t *e = reinterpret_cast<const int8_t *>(&v);
         uint4 o[2];
-        __half2 *oh = reinterpret_cast<__half2 *>(o);
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-            oh[j] = __floats2half2_rn(static_cast<float>(e[2 * j]), static_cast<float>(e[2 * j + 1]));
+        i8x16_to_f16x16(v, o);
         uint4 *d = reinterpret_cast<uint4 *>(dst) + 2 * i;
         d[0] = o[0];
         d[1] = o[1];
@@ -408,11 +421,8 @@ __global__ void __launch_bounds__(256) permute_widen_i8_kernel(const __grid_cons
             const int r = c / h;
             const int j = c - r * h;
             const int4 v = __ldg(reinterpret_cast<const int4 *>(static_cast<const int8_t *>(chunks.p[r]) + t * h + j));
-            const int8_t *e = reinterpret_cast<const int8_t *>(&v);
             uint4 o[2];
-            uint16_t *oe = reinterpret_cast<uint16_t *>(o);
-#pragma unroll
-            for (int q = 0; q < 16; ++q) oe[q] = __half_as_ushort(__int2half_rn(e[q]));
+            i8x16_to_f16x16(v, o);
             uint4 *d = reinterpret_cast<uint4 *>(dst + t * K + c);
             d[0] = o[0];
             d[1] = o[1];
