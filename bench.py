@@ -111,12 +111,20 @@ def barrier(world):
 
 
 def max_over_ranks(x: float, world: int) -> float:
+    """The largest x over the ranks (the slowest rank's time), for any backend."""
     if world == 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_tflops(flops_per_rank: float, world: int, ms: float) -> float:
+    """Whole-job throughput: the work of every replica over the slowest rank's
+    time per step (weak scaling: each rank runs its own step)."""
+    return world * flops_per_rank / (ms * 1e-3) / 1e12
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -481,7 +489,7 @@ def main():
 
     ms = sum(step_ms) / len(step_ms)
     ms = max_over_ranks(ms, world)
-    value = world * step.flops / (ms * 1e-3) / 1e12
+    value = job_tflops(step.flops, world, ms)
     ag_mean = sum(ag_ms) / len(ag_ms)
     ag_tflops = ag_s.flops / (ag_mean * 1e-3) / 1e12
 
@@ -491,7 +499,7 @@ def main():
     else:
         e2e_ms, h2d, d2h = time_e2e(step, max(3, args.steps // 3), 2, dev)
         e2e_ms = max_over_ranks(e2e_ms, world)
-    e2e_value = world * step.flops / (e2e_ms * 1e-3) / 1e12
+    e2e_value = job_tflops(step.flops, world, e2e_ms)
 
     mc2 = step.mc2
     assert mc2.mc2_device_status() == mc2.MC2_OK, "a bounded device wait gave up"
