@@ -240,50 +240,75 @@ def time_device(fn, steps, warmup, flush, stream):
     return times
 
 
+def _arena(tensors, device):
+    """One flat buffer holding tensors shaped like `tensors` back to back (offsets
+    rounded up to 256 bytes; pinned when on the host) and the views of it."""
+    offs, off = [], 0
+    for t in tensors:
+        offs.append(off)
+        off += (t.numel() * t.element_size() + 255) // 256 * 256
+    if device.type == "cpu":
+        buf = torch.empty(off, dtype=torch.uint8, pin_memory=True)
+    else:
+        buf = torch.empty(off, dtype=torch.uint8, device=device)
+    views = [buf[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape) for o, t in zip(offs, tensors)]
+    return buf, views
+
+
 def time_e2e(step: Step, steps, warmup, dev):
     """Same step through the public calls with HOST buffers: every step copies all
     of its inputs from pinned host memory to the device and all of its outputs
-    back.  Two device buffer sets and three streams (upload, compute, download)
-    ordered by events let step i+1's upload and step i-1's download run while
-    step i computes, as a caller streaming batches would."""
+    back.  A step's inputs sit back to back in one pinned buffer (and its
+    outputs in another), as a caller streaming batches would stage them, so
+    each direction is one copy per step.  Three device buffer sets and three
+    streams (upload, compute, download) ordered by events let step i+1's upload
+    and step i-1's download run while step i computes."""
     ag, a2 = step.host["ag"], step.host["a2a"]
-    h_in = [c.pin_memory() for c in ag["chunks"]] + [ag["x2"].pin_memory()] + \
-           [c.pin_memory() for c in a2["chunks"]] + [a2["x2"].pin_memory(), a2["x2_scale"].pin_memory(),
-                                                     a2["bias"].pin_memory()]
+    host_in = list(ag["chunks"]) + [ag["x2"]] + list(a2["chunks"]) + [a2["x2"], a2["x2_scale"], a2["bias"]]
     if a2["x1_scale"] is not None:
-        h_in.append(a2["x1_scale"].pin_memory())
-    sets = [step, Step(dev, step.ag_s, step.a2a_s, host=step.host)]
-
-    def dev_in(st):
-        d = st.ag_chunks + [st.ag_x2] + st.a_chunks + [st.a_x2, st.a_x2s, st.a_bias]
-        return d + ([st.a_x1s] if st.a_x1s is not None else [])
-
-    def dev_out(st):
-        return [st.ag_out] + ([st.ag_gathered] if st.ag_gathered is not None else []) + [st.a_out]
-
-    h_out = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in dev_out(st)] for st in sets]
-    h2d = sum(t.numel() * t.element_size() for t in h_in)
-    d2h = sum(t.numel() * t.element_size() for t in h_out[0])
+        host_in.append(a2["x1_scale"])
+    h_in_buf, h_in = _arena(host_in, torch.device("cpu"))
+    for v, t in zip(h_in, host_in):
+        v.copy_(t)
+    nsets = 3
+    sets = [step] + [Step(dev, step.ag_s, step.a2a_s, host=step.host) for _ in range(nsets - 1)]
+    R = len(ag["chunks"])
+    d_in_bufs, d_out_bufs, h_out_bufs = [], [], []
+    for st in sets:
+        buf, v = _arena(host_in, dev)
+        st.ag_chunks, st.ag_x2 = v[:R], v[R]
+        st.a_chunks = v[R + 1:2 * R + 1]
+        st.a_x2, st.a_x2s, st.a_bias = v[2 * R + 1], v[2 * R + 2], v[2 * R + 3]
+        st.a_x1s = v[2 * R + 4] if a2["x1_scale"] is not None else None
+        d_in_bufs.append(buf)
+        outs = [st.ag_out] + ([st.ag_gathered] if st.ag_gathered is not None else []) + [st.a_out]
+        obuf, ov = _arena(outs, dev)
+        st.ag_out = ov[0]
+        if st.ag_gathered is not None:
+            st.ag_gathered = ov[1]
+        st.a_out = ov[-1]
+        d_out_bufs.append(obuf)
+        h_out_bufs.append(_arena(outs, torch.device("cpu"))[0])
+    h2d = h_in_buf.numel()
+    d2h = h_out_bufs[0].numel()
     up, comp, down = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
     ev = [{k: torch.cuda.Event() for k in ("up", "comp", "down")} for _ in sets]
 
     def one(i):
-        b = i % 2
+        b = i % nsets
         st, e = sets[b], ev[b]
-        up.wait_event(e["comp"])           # step i-2 has finished reading this set's inputs
+        up.wait_event(e["comp"])           # step i-3 has finished reading this set's inputs
         with torch.cuda.stream(up):
-            for d, h in zip(dev_in(st), h_in):
-                d.copy_(h, non_blocking=True)
+            d_in_bufs[b].copy_(h_in_buf, non_blocking=True)
         e["up"].record(up)
         comp.wait_event(e["up"])
-        comp.wait_event(e["down"])         # step i-2's outputs of this set are on the host
+        comp.wait_event(e["down"])         # step i-3's outputs of this set are on the host
         with torch.cuda.stream(comp):
             st.run()
         e["comp"].record(comp)
         down.wait_event(e["comp"])
         with torch.cuda.stream(down):
-            for h, d in zip(h_out[b], dev_out(st)):
-                h.copy_(d, non_blocking=True)
+            h_out_bufs[b].copy_(d_out_bufs[b], non_blocking=True)
         e["down"].record(down)
 
     for i in range(warmup):
@@ -497,7 +522,7 @@ def main():
     if args.profile:
         e2e_ms, h2d, d2h = float("nan"), 0, 0
     else:
-        e2e_ms, h2d, d2h = time_e2e(step, max(3, args.steps // 3), 2, dev)
+        e2e_ms, h2d, d2h = time_e2e(step, args.steps, 3, dev)
         e2e_ms = max_over_ranks(e2e_ms, world)
     e2e_value = job_tflops(step.flops, world, e2e_ms)
 
