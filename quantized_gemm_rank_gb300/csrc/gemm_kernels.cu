@@ -10,15 +10,15 @@ namespace {
 
 // CTA pairs of this instantiation that fit on the device at once, from the
 // occupancy calculator (cached per device).
-template <bool kBF16, bool kIntPath>
+template <bool kBF16, bool kIntPath, bool kRS = false>
 int concurrent_pairs(int num_sms) {
-    using Cfg = TileCfg<2>;
+    using Cfg = TileCfg<2, !kRS && !kIntPath>;
     static int cached[64] = {0};
     int dev = 0;
     cudaGetDevice(&dev);
     int clusters = dev < 64 ? cached[dev] : 0;
     if (clusters == 0) {
-        auto kern = mc2_gemm_kernel<2, kBF16, kIntPath>;
+        auto kern = mc2_gemm_kernel<2, kBF16, kIntPath, kRS>;
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
         cudaLaunchConfig_t cfg = {};
         cudaLaunchAttribute attr[1];
@@ -40,7 +40,7 @@ int concurrent_pairs(int num_sms) {
 
 template <int kG, bool kBF16, bool kIntPath, bool kRS = false>
 cudaError_t launch_one(const GemmParams &p_in, int num_sms, cudaStream_t stream) {
-    using Cfg = TileCfg<kG>;
+    using Cfg = TileCfg<kG, !kRS && !kIntPath>;
     auto kern = mc2_gemm_kernel<kG, kBF16, kIntPath, kRS>;
     GemmParams p = p_in;
     // per device, once: the status word's address and the shared-memory opt-in
@@ -76,7 +76,7 @@ cudaError_t launch_one(const GemmParams &p_in, int num_sms, cudaStream_t stream)
         attr[1].val.clusterDim.y = 1;
         attr[1].val.clusterDim.z = 1;
         cfg.numAttrs = 2;
-        const int clusters = concurrent_pairs<kBF16, kIntPath>(num_sms);
+        const int clusters = concurrent_pairs<kBF16, kIntPath, kRS>(num_sms);
         // with a stream-K tail every co-resident pair takes part
         const int grid_clusters = (p.sk_tiles > 0 || num_tiles >= clusters) ? clusters : num_tiles;
         cfg.gridDim = dim3(2 * grid_clusters, 1, 1);
@@ -98,8 +98,8 @@ int gemm_units(GemmKind kind, int group, int num_sms) {
     switch (kind) {
         case GEMM_F16: return concurrent_pairs<false, false>(num_sms);
         case GEMM_BF16: return concurrent_pairs<true, false>(num_sms);
-        case GEMM_RS_F16: return concurrent_pairs<false, false>(num_sms);
-        case GEMM_RS_BF16: return concurrent_pairs<true, false>(num_sms);
+        case GEMM_RS_F16: return concurrent_pairs<false, false, true>(num_sms);
+        case GEMM_RS_BF16: return concurrent_pairs<true, false, true>(num_sms);
         default: return concurrent_pairs<false, true>(num_sms);
     }
 }

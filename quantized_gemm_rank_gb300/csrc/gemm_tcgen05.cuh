@@ -59,15 +59,23 @@ constexpr int kNumThreads = 128 + kNumEpiWarps * 32;
 constexpr uint32_t kATileBytes = kBM * kBK * 2;  // 16 KiB
 constexpr uint32_t kTmemCols = 512;              // two 256-column fp32 accumulators
 constexpr int kGroupM = 8;                       // m-tiles per raster group (L2 reuse of B)
+// Output staging for the TMA-store epilogue: per epilogue warp one 32-row x
+// 64-column 16-bit slab (128-byte rows, 128-byte swizzle).
+constexpr uint32_t kEpiSlabBytes = 32 * 128;
+constexpr uint32_t kEpiStageBytes = kNumEpiWarps * kEpiSlabBytes;
 
-template <int kG>
+// kTmaOut: the epilogue stores through shared staging slabs (the float path);
+// only then is the staging area reserved, leaving the rest of the SM's
+// shared/L1 space to the L1 cache that the integer epilogue's loads use.
+template <int kG, bool kTmaOut = false>
 struct TileCfg {
     static constexpr int kTileM = kBM * kG;               // rows per tile
     static constexpr int kBRows = kBN / kG;               // rows of B (N) per CTA
     static constexpr uint32_t kBTileBytes = kBRows * kBK * 2;
     static constexpr uint32_t kStageBytes = kATileBytes + kBTileBytes;
     static constexpr int kStages = kG == 1 ? 4 : 6;
-    static constexpr uint32_t kSmemBytes = kStages * kStageBytes + 1024 + 1024;
+    // stages | barriers (1 KiB) | epilogue staging | alignment slack (1 KiB)
+    static constexpr uint32_t kSmemBytes = kStages * kStageBytes + 1024 + (kTmaOut ? kEpiStageBytes : 0) + 1024;
 };
 
 // A_SINGLE_MN: one map over an (k, m) row-major matrix, i.e. A = that matrix
@@ -78,6 +86,8 @@ struct GemmParams {
     CUtensorMap a_maps[kMaxAMaps];  // A operand: one map, or one per rank's chunk
     CUtensorMap b_map;              // B operand: (n, k) K-major or (k, n) N-major
     CUtensorMap g_map;              // gathered output (m, k), same box and swizzle as A
+    CUtensorMap out_map;            // out (m, n) 16-bit: box 64 columns x 32 rows, 128-byte swizzle
+                                    // (every instantiation but the reduce-scatter)
     int num_a_maps;
     int a_mode;
     int a_box_rows;                 // A_MCONCAT: rows per TMA box (divides m_local and kBM)
@@ -259,7 +269,8 @@ __device__ __forceinline__ void store_row32_16(uint16_t *row_ptr, int n, int col
 
 template <int kG, bool kBF16, bool kIntPath, bool kRS = false>
 __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_constant__ GemmParams p) {
-    using Cfg = TileCfg<kG>;
+    constexpr bool kTmaOut = !kRS && !kIntPath;  // epilogue stores through shared slabs and TMA
+    using Cfg = TileCfg<kG, kTmaOut>;
     constexpr bool kPair = kG == 2;
     constexpr int S = Cfg::kStages;
     extern __shared__ uint8_t smem_raw[];
@@ -271,6 +282,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
     uint64_t *tfull_bar = bars + 3 * S;       // accumulator buffer ready
     uint64_t *tempty_bar = bars + 3 * S + 2;  // accumulator buffer drained (the leader's counts both CTAs)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 3 * S + 4);
+    // the epilogue's output slabs, after the 1 KiB barrier area (1024-byte aligned)
+    uint8_t *epi_stage = smem + S * Cfg::kStageBytes + 1024;
     __shared__ int abort_flag_s;
     volatile int *abort_flag = &abort_flag_s;
 
@@ -631,76 +644,115 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
                     });
                 }
             }
-            if (row >= p.m) continue;
-            if constexpr (!kIntPath) {
-                uint16_t *orow;
-                if constexpr (kRS)
-                    orow = reinterpret_cast<uint16_t *>(p.out_chunks[row / p.out_rows]) +
-                           static_cast<int64_t>(row % p.out_rows) * p.n;
-                else
-                    orow = reinterpret_cast<uint16_t *>(p.out) + static_cast<int64_t>(row) * p.n;
+            const bool row_ok = row < p.m;
+            if constexpr (kRS || kIntPath) {
+                if (!row_ok) continue;   // no warp-wide steps below on these paths
+            }
+            // Float path: this warp's 32 rows x 128 columns leave as two 64-column
+            // slabs: rounded 16-bit values go to its shared staging slab (128-byte
+            // rows, chunk j of row r at ((j ^ (r % 8)) * 16)), then one TMA store per
+            // slab; rows and columns past the output are clipped by the TMA unit.
+            // The reduce-scatter writes rows straight to the ranks' outputs, and the
+            // integer path (whose dequant leaves fewer registers) straight from its
+            // registers.
+            uint8_t *slab = reinterpret_cast<uint8_t *>(epi_stage) + (warp - 4) * kEpiSlabBytes;
+            const int slab_row0 = mb * Cfg::kTileM + kBM * static_cast<int>(cr) + 32 * q;
+            auto put = [&](int c, const uint32_t (&pk)[16]) {
+                if constexpr (kRS) {
+                    uint16_t *orow = reinterpret_cast<uint16_t *>(p.out_chunks[row / p.out_rows]) +
+                                     static_cast<int64_t>(row % p.out_rows) * p.n;
+                    store_row32_16(orow, p.n, colh + c * 32, pk);
+                } else if constexpr (!kTmaOut) {
+                    if (row_ok && colh + c * 32 < p.n)
+                        store_row32_16(reinterpret_cast<uint16_t *>(p.out) + static_cast<int64_t>(row) * p.n, p.n,
+                                       colh + c * 32, pk);
+                } else {
+                    if ((c & 1) == 0) {
+                        // the slab's previous store has finished reading it
+                        if (lane == 0) ptx::bulk_wait_group_read<0>();
+                        __syncwarp();
+                    }
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const int col0 = colh + c * 32;
-                    if (col0 < p.n) {
-                        float v[32];
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) v[i] = sum[c * 32 + i];
-                        if (p.bias16 != nullptr) {
-#pragma unroll
-                            for (int i = 0; i < 32; ++i)
-                                v[i] = __fadd_rn(v[i], load16<kBF16>(p.bias16, min(col0 + i, p.n - 1)));
+                    for (int j = 0; j < 4; ++j) {
+                        const int j16 = (c & 1) * 4 + j;
+                        *reinterpret_cast<uint4 *>(slab + lane * 128 + ((j16 ^ (lane & 7)) << 4)) =
+                            make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                    }
+                    if ((c & 1) == 1) {
+                        ptx::fence_proxy_async_smem();
+                        __syncwarp();
+                        const int scol = colh + (c >> 1) * 64;
+                        if (lane == 0 && scol < p.n) {
+                            ptx::tma_store_2d(&p.out_map, scol, slab_row0, ptx::smem_u32(slab));
+                            ptx::bulk_commit_group();
                         }
-                        uint32_t pk[16];
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) pk[i] = pack2<kBF16>(v[2 * i], v[2 * i + 1]);
-                        store_row32_16(orow, p.n, col0, pk);
                     }
                 }
-            } else {
-                const float s1 = p.x1_scale[row];
+            };
+            if constexpr (!kIntPath) {
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     const int col0 = colh + c * 32;
-                    if (col0 < p.n) {
-                        uint32_t pk[16];
+                    if (kRS && col0 >= p.n) continue;
+                    float v[32];
 #pragma unroll
-                        for (int i = 0; i < 32; i += 2) {
-                            float o[2];
+                    for (int i = 0; i < 32; ++i) v[i] = sum[c * 32 + i];
+                    if (p.bias16 != nullptr) {
 #pragma unroll
-                            for (int e = 0; e < 2; ++e) {
-                                const int col = min(col0 + i + e, p.n - 1);
-                                float v = __int2float_rn(sum[c * 32 + i + e]);
-                                v = __fmul_rn(v, s1);
-                                v = __fmul_rn(v, p.x2_scale[col]);
-                                if (p.bias_q != nullptr) {
-                                    const float bv = p.bias_q_bf16 ? load16<true>(p.bias_q, col)
-                                                                   : reinterpret_cast<const float *>(p.bias_q)[col];
-                                    v = __fadd_rn(v, bv);
-                                }
-                                o[e] = v;
+                        for (int i = 0; i < 32; ++i)
+                            v[i] = __fadd_rn(v[i], load16<kBF16>(p.bias16, min(col0 + i, p.n - 1)));
+                    }
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) pk[i] = pack2<kBF16>(v[2 * i], v[2 * i + 1]);
+                    put(c, pk);
+                }
+            } else {
+                const float s1 = row_ok ? p.x1_scale[row] : 0.0f;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int col0 = colh + c * 32;
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 32; i += 2) {
+                        float o[2];
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const int col = min(col0 + i + e, p.n - 1);
+                            float v = __int2float_rn(sum[c * 32 + i + e]);
+                            v = __fmul_rn(v, s1);
+                            v = __fmul_rn(v, p.x2_scale[col]);
+                            if (p.bias_q != nullptr) {
+                                const float bv = p.bias_q_bf16 ? load16<true>(p.bias_q, col)
+                                                               : reinterpret_cast<const float *>(p.bias_q)[col];
+                                v = __fadd_rn(v, bv);
                             }
-                            pk[i >> 1] = pack2<true>(o[0], o[1]);
+                            o[e] = v;
                         }
-                        store_row32_16(reinterpret_cast<uint16_t *>(p.out) + static_cast<int64_t>(row) * p.n, p.n,
-                                       col0, pk);
-                        if (p.acc_out != nullptr) {
-                            int32_t *dst = p.acc_out + static_cast<int64_t>(row) * p.n + col0;
-                            if (col0 + 32 <= p.n) {
+                        pk[i >> 1] = pack2<true>(o[0], o[1]);
+                    }
+                    put(c, pk);
+                    if (p.acc_out != nullptr && row_ok && col0 < p.n) {
+                        int32_t *dst = p.acc_out + static_cast<int64_t>(row) * p.n + col0;
+                        if (col0 + 32 <= p.n) {
 #pragma unroll
-                                for (int j = 0; j < 8; ++j)
-                                    reinterpret_cast<int4 *>(dst)[j] =
-                                        make_int4(sum[c * 32 + 4 * j], sum[c * 32 + 4 * j + 1],
-                                                  sum[c * 32 + 4 * j + 2], sum[c * 32 + 4 * j + 3]);
-                            } else {
+                            for (int j = 0; j < 8; ++j)
+                                reinterpret_cast<int4 *>(dst)[j] =
+                                    make_int4(sum[c * 32 + 4 * j], sum[c * 32 + 4 * j + 1], sum[c * 32 + 4 * j + 2],
+                                              sum[c * 32 + 4 * j + 3]);
+                        } else {
 #pragma unroll
-                                for (int i = 0; i < 32; ++i)
-                                    if (col0 + i < p.n) dst[i] = sum[c * 32 + i];
-                            }
+                            for (int i = 0; i < 32; ++i)
+                                if (col0 + i < p.n) dst[i] = sum[c * 32 + i];
                         }
                     }
                 }
             }
+        }
+        // every output store has completed before the CTA can exit
+        if constexpr (!kRS && !kIntPath) {
+            if (lane == 0) ptx::bulk_wait_group<0>();
+            __syncwarp();
         }
     }
 

@@ -244,6 +244,8 @@ int mc2_all_gather_mm(const void *const *x_chunks, int world_size, int64_t m_loc
     p.k = static_cast<int>(k);
     p.kblock_tiles = kKBlockTiles;
     p.out = out;
+    if (!make_map16(&p.out_map, p.out, static_cast<uint64_t>(p.n), static_cast<uint64_t>(p.m), 64, 32))
+        return fail(MC2_ERR_CUDA, "cuTensorMapEncodeTiled failed for the output");
     p.bias16 = bias;
     p.wait_limit_ns = kWaitLimitNs;
     cudaError_t e = mc2::launch_gemm(dtype == MC2_BF16 ? mc2::GEMM_BF16 : mc2::GEMM_F16, group, p, dev.num_sms,
@@ -351,6 +353,8 @@ int mc2_matmul_weight_grad(const void *dy, int64_t m, int64_t n, const void *x, 
     p.k = static_cast<int>(m);
     p.kblock_tiles = kKBlockTiles;
     p.out = dw;
+    if (!make_map16(&p.out_map, p.out, static_cast<uint64_t>(p.n), static_cast<uint64_t>(p.m), 64, 32))
+        return fail(MC2_ERR_CUDA, "cuTensorMapEncodeTiled failed for the output");
     p.wait_limit_ns = kWaitLimitNs;
     const int group = mc2::gemm_group_for(static_cast<int>(n));
     e = mc2::launch_gemm(dtype == MC2_BF16 ? mc2::GEMM_BF16 : mc2::GEMM_F16, group, p, dev.num_sms, s);
@@ -506,6 +510,8 @@ int mc2_alltoall_quant_mm(const void *const *chunks, int rank_size, int64_t bs_l
     p.k = static_cast<int>(K);
     p.kblock_tiles = kKBlockTiles;
     p.out = out;
+    if (!make_map16(&p.out_map, p.out, static_cast<uint64_t>(p.n), static_cast<uint64_t>(p.m), 64, 32))
+        return fail(MC2_ERR_CUDA, "cuTensorMapEncodeTiled failed for the output");
     p.x1_scale = scale;
     p.x2_scale = x2_scale;
     p.bias_q = bias;
