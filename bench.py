@@ -365,7 +365,7 @@ def run_reference(args):
     ag_s, a2a_s = mc2_inputs.WORKLOADS[AG_NAME], mc2_inputs.WORKLOADS[A2A_NAME]
     host = {"ag": mc2_inputs.ag_inputs(ag_s, seed=0), "a2a": mc2_inputs.a2a_inputs(a2a_s, seed=0)}
     import oracle
-    rows = 64
+    rows = 16   # ~0.1 s of oracle work per step on 16 cores, so K steps end within minutes
     for _ in range(args.warmup):
         oracle_sample(rows, rows, ag_s, a2a_s, host)
     t0 = time.perf_counter()
