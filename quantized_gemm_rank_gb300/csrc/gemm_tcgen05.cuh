@@ -95,6 +95,7 @@ struct GemmParams {
     int m_local;                    // A_MCONCAT: rows per chunk
     int k_local;                    // A_KINTERLEAVE: columns per chunk
     int b_mn_major;
+    int b_3d;                       // N-major B through a 3-D map [n/64][k][64]: one box per stage
     int gather;
     int kblock_tiles;               // integer path: k-tiles per exact fp32 block
     void *out;                      // (m, n): dtype (float path) / bf16 (integer path)
@@ -341,6 +342,89 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
         uint32_t phase = 0;
         int iters = 0;
         bool ok = true;
+        // B copy form, fixed for the launch: 0 K-major box, 1 N-major boxes, 2 one 3-D N-major box
+        const int b_mode = !p.b_mn_major ? 0 : (p.b_3d ? 2 : 1);
+        // A form: the AMode, with the all-gather split into one box per k-tile (4) or several
+        const int a_form = p.a_mode == A_MCONCAT && p.a_box_rows == kBM ? 4 : p.a_mode;
+        // addresses of stage 0 (stage s adds s * 8 to a barrier, s * kStageBytes to a tile);
+        // the pair's peer signals the leader's full barrier at the same offset
+        const uint32_t full0 = ptx::smem_u32(&full_bar[0]);
+        const uint32_t empty0 = ptx::smem_u32(&empty_bar[0]);
+        const uint32_t sA0 = ptx::smem_u32(smem);
+        const uint32_t sig0 = (kPair && !leader) ? ptx::mapa(full0, 0) : full0;
+        auto load = [&](uint32_t dst, const CUtensorMap *m, int c0, int c1, uint32_t bar) {
+            if constexpr (kPair)
+                ptx::tma_load_2d_pair(dst, m, c0, c1, bar);
+            else
+                ptx::tma_load_2d(dst, m, c0, c1, bar);
+        };
+        // one work tile's k-tiles, with the copy forms as compile-time constants
+        auto k_loop = [&](auto a_c, auto b_c, int kt_begin, int kt_end, int m0, int n0, int a_chunk0, int a_row0,
+                          int a_nbox, int kc, int kl) {
+            constexpr int AF = decltype(a_c)::value;
+            constexpr int BF = decltype(b_c)::value;
+            for (int kt = kt_begin; kt < kt_end; ++kt) {
+                if (!wait_or_abort<kPair>(empty0 + 8u * stage, phase ^ 1u, p, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t sA = sA0 + stage * Cfg::kStageBytes;
+                const uint32_t sB = sA + kATileBytes;
+                const uint32_t bar = sig0 + 8u * stage;
+                if (leader) ptx::mbar_arrive_expect_tx(full0 + 8u * stage, leader_bytes);
+                const int k0 = kt * kBK;
+                if constexpr (AF == 4) {
+                    load(sA, &p.a_maps[a_chunk0], k0, a_row0, bar);
+                } else if constexpr (AF == A_MCONCAT) {
+                    // walk the tile's boxes through the chunks (box_rows divides m_local)
+                    int c = a_chunk0, li = a_row0;
+                    for (int j = 0; j < a_nbox; ++j) {
+                        load(sA + j * p.a_box_rows * 128, &p.a_maps[c], k0, li, bar);
+                        li += p.a_box_rows;
+                        if (li >= p.m_local && c < p.num_a_maps - 1) li -= p.m_local, ++c;
+                    }
+                } else if constexpr (AF == A_KINTERLEAVE) {
+                    // permuted column k0 = kc * k_local + kl lives in chunk kc (k_local % kBK == 0)
+                    load(sA, &p.a_maps[kc], kl, m0, bar);
+                    if constexpr (kRS) {
+                        // ... and so does the B slice: rank kc's weight shard at column kl
+                        const CUtensorMap *bm = &p.b_rank_maps[kc];
+                        if constexpr (BF != 0) {
+#pragma unroll
+                            for (int j = 0; j < Cfg::kBRows / 64; ++j)
+                                load(sB + j * (kBK * 128), bm, n0 + 64 * j, kl, bar);
+                        } else {
+                            load(sB, bm, kl, n0, bar);
+                        }
+                    }
+                    kl += kBK;
+                    if (kl >= p.k_local) kl = 0, ++kc;
+                } else if constexpr (AF == A_SINGLE_MN) {
+                    // M-major A: 64-wide M slabs of the (k, m) matrix, like an N-major B
+#pragma unroll
+                    for (int j = 0; j < kBM / 64; ++j) load(sA + j * (kBK * 128), &p.a_maps[0], m0 + 64 * j, k0, bar);
+                } else {
+                    load(sA, &p.a_maps[0], k0, m0, bar);
+                }
+                if constexpr (!kRS) {
+                    if constexpr (BF == 0) {
+                        load(sB, &p.b_map, k0, n0, bar);
+                    } else if constexpr (BF == 2) {
+                        // all kBRows / 64 column groups in one copy, group j at sB + j * 8 KiB
+                        if constexpr (kPair)
+                            ptx::tma_load_3d_pair(sB, &p.b_map, 0, k0, n0 >> 6, bar);
+                        else
+                            ptx::tma_load_3d(sB, &p.b_map, 0, k0, n0 >> 6, bar);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < Cfg::kBRows / 64; ++j)
+                            load(sB + j * (kBK * 128), &p.b_map, n0 + 64 * j, k0, bar);
+                    }
+                }
+                ++iters;
+                if (++stage == S) stage = 0, phase ^= 1u;
+            }
+        };
         for (int wi = 0; wi < sched.count() && ok; ++wi) {
             const Work w = sched.get(wi);
             const int kt_begin = w.kb0 * p.kblock_tiles, kt_end = min(num_k, w.kb1 * p.kblock_tiles);
@@ -365,69 +449,23 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
                 }
                 a_nbox = kBM / p.a_box_rows;
             }
-            for (int kt = kt_begin; kt < kt_end; ++kt) {
-                if (!wait_or_abort<kPair>(ptx::smem_u32(&empty_bar[stage]), phase ^ 1u, p, abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                const uint32_t local_full = ptx::smem_u32(&full_bar[stage]);
-                const uint32_t sA = ptx::smem_u32(smem + stage * Cfg::kStageBytes);
-                const uint32_t sB = sA + kATileBytes;
-                uint32_t a_bar = local_full, b_bar = local_full;
-                if (leader) {
-                    ptx::mbar_arrive_expect_tx(local_full, leader_bytes);
-                } else {
-                    a_bar = b_bar = ptx::mapa(local_full, 0);
-                }
-                const int k0 = kt * kBK;
-                auto load = [&](uint32_t dst, const CUtensorMap *m, int c0, int c1, uint32_t bar) {
-                    if constexpr (kPair)
-                        ptx::tma_load_2d_pair(dst, m, c0, c1, bar);
-                    else
-                        ptx::tma_load_2d(dst, m, c0, c1, bar);
-                };
-                if (p.a_mode == A_MCONCAT) {
-                    // walk the tile's boxes through the chunks (box_rows divides m_local)
-                    int c = a_chunk0, li = a_row0;
-                    for (int j = 0; j < a_nbox; ++j) {
-                        load(sA + j * p.a_box_rows * 128, &p.a_maps[c], k0, li, a_bar);
-                        li += p.a_box_rows;
-                        if (li >= p.m_local && c < p.num_a_maps - 1) li -= p.m_local, ++c;
-                    }
-                } else if (p.a_mode == A_KINTERLEAVE) {
-                    // permuted column k0 = kc * k_local + kl lives in chunk kc (k_local % kBK == 0)
-                    load(sA, &p.a_maps[kc], kl, m0, a_bar);
-                    if constexpr (kRS) {
-                        // ... and so does the B slice: rank kc's weight shard at column kl
-                        const CUtensorMap *bm = &p.b_rank_maps[kc];
-                        if (p.b_mn_major) {
-#pragma unroll
-                            for (int j = 0; j < Cfg::kBRows / 64; ++j)
-                                load(sB + j * (kBK * 128), bm, n0 + 64 * j, kl, b_bar);
-                        } else {
-                            load(sB, bm, kl, n0, b_bar);
-                        }
-                    }
-                    kl += kBK;
-                    if (kl >= p.k_local) kl = 0, ++kc;
-                } else if (p.a_mode == A_SINGLE_MN) {
-                    // M-major A: 64-wide M slabs of the (k, m) matrix, like an N-major B
-#pragma unroll
-                    for (int j = 0; j < kBM / 64; ++j) load(sA + j * (kBK * 128), &p.a_maps[0], m0 + 64 * j, k0, a_bar);
-                } else {
-                    load(sA, &p.a_maps[0], k0, m0, a_bar);
-                }
-                if constexpr (!kRS) {
-                    if (p.b_mn_major) {
-#pragma unroll
-                        for (int j = 0; j < Cfg::kBRows / 64; ++j)
-                            load(sB + j * (kBK * 128), &p.b_map, n0 + 64 * j, k0, b_bar);
-                    } else {
-                        load(sB, &p.b_map, k0, n0, b_bar);
-                    }
-                }
-                ++iters;
-                if (++stage == S) stage = 0, phase ^= 1u;
+            using I0 = std::integral_constant<int, 0>;
+            using I1 = std::integral_constant<int, 1>;
+            using I2 = std::integral_constant<int, 2>;
+            auto with_b = [&](auto a_c) {
+                if (b_mode == 0)
+                    k_loop(a_c, I0{}, kt_begin, kt_end, m0, n0, a_chunk0, a_row0, a_nbox, kc, kl);
+                else if (b_mode == 2)
+                    k_loop(a_c, I2{}, kt_begin, kt_end, m0, n0, a_chunk0, a_row0, a_nbox, kc, kl);
+                else
+                    k_loop(a_c, I1{}, kt_begin, kt_end, m0, n0, a_chunk0, a_row0, a_nbox, kc, kl);
+            };
+            switch (a_form) {
+                case 4: with_b(std::integral_constant<int, 4>{}); break;
+                case A_MCONCAT: with_b(std::integral_constant<int, A_MCONCAT>{}); break;
+                case A_KINTERLEAVE: with_b(std::integral_constant<int, A_KINTERLEAVE>{}); break;
+                case A_SINGLE_MN: with_b(std::integral_constant<int, A_SINGLE_MN>{}); break;
+                default: with_b(std::integral_constant<int, A_SINGLE>{}); break;
             }
         }
         if (!ok) {

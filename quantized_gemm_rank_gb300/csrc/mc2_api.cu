@@ -61,6 +61,26 @@ bool make_map16(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer
     return r == CUDA_SUCCESS;
 }
 
+// N-major B (outer = k rows, inner = n columns, 16-bit) as a 3-D map
+// [inner / 64][outer][64] (strides inner * 2 and 128 bytes), so one copy of box
+// {64, box_outer, groups} brings `groups` 64-column slices, slice j landing
+// 8 KiB after slice j - 1 (the layout of that many 2-D boxes).  Only for
+// inner % 64 == 0: a partial last group would read into the next row.
+bool make_map16_nmajor3d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, uint32_t box_outer,
+                         uint32_t groups) {
+    if (inner % 64 != 0) return false;
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {64, outer, inner / 64};
+    cuuint64_t strides[2] = {inner * 2, 128};
+    cuuint32_t box[3] = {64, box_outer, groups};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 struct DeviceInfo {
     int device = -1;
     int num_sms = 0;
@@ -230,7 +250,9 @@ int mc2_all_gather_mm(const void *const *x_chunks, int world_size, int64_t m_loc
             return fail(MC2_ERR_CUDA, "cuTensorMapEncodeTiled failed for x2 (n, k)");
         p.b_mn_major = 0;
     } else {
-        if (!make_map16(&p.b_map, x2, n, k, 64, mc2::kBK))
+        if (make_map16_nmajor3d(&p.b_map, x2, n, k, mc2::kBK, (mc2::kBN / group) / 64))
+            p.b_3d = 1;
+        else if (!make_map16(&p.b_map, x2, n, k, 64, mc2::kBK))
             return fail(MC2_ERR_CUDA, "cuTensorMapEncodeTiled failed for x2 (k, n)");
         p.b_mn_major = 1;
     }
@@ -344,7 +366,11 @@ int mc2_matmul_weight_grad(const void *dy, int64_t m, int64_t n, const void *x, 
     mc2::GemmParams p;
     memset(&p, 0, sizeof(p));
     if (!make_map16(&p.a_maps[0], dy, n, m, 64, mc2::kBK)) return fail(MC2_ERR_CUDA, "cuTensorMapEncodeTiled failed for dy");
-    if (!make_map16(&p.b_map, x, k, m, 64, mc2::kBK)) return fail(MC2_ERR_CUDA, "cuTensorMapEncodeTiled failed for x");
+    const int wgroup = mc2::gemm_group_for(static_cast<int>(n));
+    if (make_map16_nmajor3d(&p.b_map, x, k, m, mc2::kBK, (mc2::kBN / wgroup) / 64))
+        p.b_3d = 1;
+    else if (!make_map16(&p.b_map, x, k, m, 64, mc2::kBK))
+        return fail(MC2_ERR_CUDA, "cuTensorMapEncodeTiled failed for x");
     p.num_a_maps = 1;
     p.a_mode = mc2::A_SINGLE_MN;
     p.b_mn_major = 1;
@@ -499,7 +525,9 @@ int mc2_alltoall_quant_mm(const void *const *chunks, int rank_size, int64_t bs_l
     } else if (!make_map16(&p.a_maps[0], ah, K, bs_local, mc2::kBK, mc2::kBM)) {
         return fail(MC2_ERR_CUDA, "cuTensorMapEncodeTiled failed for the quantised activations");
     }
-    if (!make_map16(&p.b_map, x2h, n, K, 64, mc2::kBK))
+    if (make_map16_nmajor3d(&p.b_map, x2h, n, K, mc2::kBK, (mc2::kBN / group) / 64))
+        p.b_3d = 1;
+    else if (!make_map16(&p.b_map, x2h, n, K, 64, mc2::kBK))
         return fail(MC2_ERR_CUDA, "cuTensorMapEncodeTiled failed for x2");
     p.num_a_maps = a_by_chunk ? rank_size : 1;
     p.a_mode = a_by_chunk ? mc2::A_KINTERLEAVE : mc2::A_SINGLE;

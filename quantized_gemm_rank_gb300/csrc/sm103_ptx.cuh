@@ -158,6 +158,26 @@ __device__ __forceinline__ void bulk_load_1d(uint32_t dst, const void *src, uint
 // initialisation) visible to the async proxy (the bulk copies).
 __device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
+// 3-D tiled load for a CTA pair (see tma_load_2d_pair).
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap *m, int32_t c0, int32_t c1,
+                                                 int32_t c2, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+        "%3, %4}], [%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+        : "memory");
+}
+
+// 3-D tiled load global -> shared (one CTA).
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *m, int32_t c0, int32_t c1, int32_t c2,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(
+            dst),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+        : "memory");
+}
+
 // 2-D tiled store shared -> global (bulk async-group completion).
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap *m, int32_t c0, int32_t c1, uint32_t src) {
     asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
