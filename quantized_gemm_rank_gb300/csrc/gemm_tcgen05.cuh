@@ -364,7 +364,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
             constexpr int AF = decltype(a_c)::value;
             constexpr int BF = decltype(b_c)::value;
             for (int kt = kt_begin; kt < kt_end; ++kt) {
-                if (!wait_or_abort<kPair>(empty0 + 8u * stage, phase ^ 1u, p, abort_flag)) {
+                // (CTA scope: the stage is released by the MMA's tcgen05.commit)
+                if (!wait_or_abort<false>(empty0 + 8u * stage, phase ^ 1u, p, abort_flag)) {
                     ok = false;
                     break;
                 }
@@ -520,7 +521,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
                     ptx::tc_fence_after();
                     d_tmem = tmem_base + b * kBN;
                 }
-                if (!wait_or_abort<kPair>(full0 + 8u * stage, phase, p, abort_flag)) {
+                // (CTA scope: the stage is completed by the copies' transaction bytes)
+                if (!wait_or_abort<false>(full0 + 8u * stage, phase, p, abort_flag)) {
                     ok = false;
                     break;
                 }
