@@ -92,3 +92,24 @@ def test_repeat_calls_are_deterministic():
     a, _ = run_gpu(inp, shape)
     b, _ = run_gpu(inp, shape)
     assert_bits_equal(a, b, "repeat")
+
+
+# The largest contraction the page allows (k < 65535, here 65528 = 1024 K blocks
+# of 64), on one-CTA tiles (m = 16) and on CTA-pair tiles (m = 272), with the
+# x2 (k, n) layout read as one 3-D box per stage (n % 64 == 0) and as 64-column
+# boxes (n % 64 != 0).
+MAX_K_CASES = {
+    "maxk-one-cta-3d": mc2_inputs.AGShape(world_size=2, m_local=8, k=65528, n=64),
+    "maxk-pair-2d-bias": mc2_inputs.AGShape(world_size=2, m_local=136, k=65528, n=72, bias=True),
+    "maxk-pair-nk": mc2_inputs.AGShape(world_size=2, m_local=136, k=65528, n=128, x2_is_nk=True),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MAX_K_CASES))
+def test_largest_k(name):
+    shape = MAX_K_CASES[name]
+    inp = mc2_inputs.ag_inputs(shape, seed=9)
+    out, gathered = run_gpu(inp, shape)
+    ref, ref_g = oracle.all_gather_mm(inp["chunks"], inp["x2"], x2_is_nk=shape.x2_is_nk, bias=inp["bias"])
+    assert_close_16(out, ref, f"{name}: out")
+    assert_bits_equal(gathered, ref_g, f"{name}: gathered")

@@ -231,3 +231,23 @@ def test_stream_k_all_127_bound():
     assert torch.all(got["acc"] == -8192 * 16129)
     ref = run_oracle(inp, shape, rows=[0, 1, 1023, 2047])
     compare(got, ref, "stream-K all-127", rows=[0, 1, 1023, 2047])
+
+
+# rank_size * H at the top of the page's range (<= 35000, a multiple of 16):
+# 8 x 4368 = 34944 (the per-token quant kernel and the permuted int8 widening,
+# the rows being too long for the fused prologue) and 8 x 4096 = 32768 (the
+# fused prologue at its largest row, 64 KiB in shared memory).
+MAX_K_CASES = {
+    "dyn-maxk-34944": A2A(rank_size=8, bs_local=136, h=4368, n=64, quant_mode=7),
+    "dyn-maxk-32768-prologue": A2A(rank_size=8, bs_local=136, h=4096, n=64, quant_mode=7),
+    "full-maxk-34944": A2A(rank_size=8, bs_local=136, h=4368, n=64, quant_mode=3),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MAX_K_CASES))
+def test_largest_rank_h(name):
+    shape = MAX_K_CASES[name]
+    inp = mc2_inputs.a2a_inputs(shape, seed=14)
+    got = run_gpu(inp, shape)
+    ref = run_oracle(inp, shape)
+    compare(got, ref, name)
