@@ -50,7 +50,7 @@ FLUSH_BYTES = 512 << 20
 # (GEMM_SOURCES) the capture was taken with: the figure is reported only
 # while they match.
 AG_GEMM_TRAFFIC = 293.78e6          # dram__bytes_read.sum 182.75 MB + dram__bytes_write.sum 111.02 MB
-AG_GEMM_TRAFFIC_SRC_HASH = "11c291409b284c81"
+AG_GEMM_TRAFFIC_SRC_HASH = "43c65d2a85af4a28"
 
 
 def parse_args():

@@ -29,7 +29,10 @@
 // tile) overlaps the MMAs of the next.
 //
 // Warp roles (384 threads per CTA):
-//   warp 0      TMA producer (one lane)
+//   warp 0      TMA producer (one lane).  Its instruction path per stage bounds
+//               the load pipeline, so it issues one copy for A and one for B
+//               (N-major B through a 3-D map when n % 64 == 0), with the copy
+//               forms fixed at compile time for its k-tile loop.
 //   warp 1      TMEM allocator; MMA issuer (one lane; the leader CTA for kG = 2)
 //   warp 2      gathered-output TMA store (one lane; AllGather with gather only).
 //               On n-tile-0 tiles the MMA commits each stage to a "consumed"
@@ -38,7 +41,10 @@
 //               the store never delays the MMAs.
 //   warp 3      idle
 //   warps 4-11  epilogue: warp w reads TMEM lanes 32*(w%4)..+31 (its rows) and
-//               half (w-4)/4 of the 256 accumulator columns.
+//               half (w-4)/4 of the 256 accumulator columns.  The float path
+//               stores its rounded outputs through a swizzled shared slab and a
+//               TMA tensor store; the integer path and the reduce-scatter store
+//               from registers.
 #pragma once
 
 #include <cuda_bf16.h>
