@@ -15,11 +15,13 @@ int concurrent_pairs(int num_sms) {
     using Cfg = TileCfg<2, !kRS && !kIntPath>;
     static int cached[64] = {0};
     int dev = 0;
-    cudaGetDevice(&dev);
+    if (cudaGetDevice(&dev) != cudaSuccess) return num_sms / 2;
     int clusters = dev < 64 ? cached[dev] : 0;
     if (clusters == 0) {
         auto kern = mc2_gemm_kernel<2, kBF16, kIntPath, kRS>;
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
+        // without the opt-in the occupancy query below fails and the fallback applies
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes) != cudaSuccess)
+            return num_sms / 2;
         cudaLaunchConfig_t cfg = {};
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;

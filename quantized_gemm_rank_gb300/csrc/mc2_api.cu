@@ -96,8 +96,9 @@ int current_device(DeviceInfo *info) {
         e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return fail(MC2_ERR_CUDA, "cudaDeviceGetAttribute: %s", cudaGetErrorString(e));
         int major = 0, minor = 0;
-        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        if (e != cudaSuccess) return fail(MC2_ERR_CUDA, "cudaDeviceGetAttribute: %s", cudaGetErrorString(e));
         if (major != 10 || minor != 3)
             return fail(MC2_ERR_UNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a only", dev,
                         major, minor);
