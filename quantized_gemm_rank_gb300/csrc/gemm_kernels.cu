@@ -1,4 +1,5 @@
 // gemm_kernels.cu -- instantiations and launch of the fused MC2 GEMM.
+#include <atomic>
 #include "gemm_tcgen05.cuh"
 #include "internal.h"
 
@@ -13,10 +14,10 @@ namespace {
 template <bool kBF16, bool kIntPath, bool kRS = false>
 int concurrent_pairs(int num_sms) {
     using Cfg = TileCfg<2, !kRS && !kIntPath>;
-    static int cached[64] = {0};
+    static std::atomic<int> cached[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return num_sms / 2;
-    int clusters = dev < 64 ? cached[dev] : 0;
+    int clusters = dev < 64 ? cached[dev].load(std::memory_order_relaxed) : 0;
     if (clusters == 0) {
         auto kern = mc2_gemm_kernel<2, kBF16, kIntPath, kRS>;
         // without the opt-in the occupancy query below fails and the fallback applies
@@ -35,7 +36,7 @@ int concurrent_pairs(int num_sms) {
         cfg.gridDim = dim3(2 * (num_sms / 2), 1, 1);
         if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess || clusters < 1)
             clusters = num_sms / 2;
-        if (dev < 64) cached[dev] = clusters;
+        if (dev < 64) cached[dev].store(clusters, std::memory_order_relaxed);
     }
     return clusters;
 }
@@ -46,18 +47,19 @@ cudaError_t launch_one(const GemmParams &p_in, int num_sms, cudaStream_t stream)
     auto kern = mc2_gemm_kernel<kG, kBF16, kIntPath, kRS>;
     GemmParams p = p_in;
     // per device, once: the status word's address and the shared-memory opt-in
-    static int *status_addr[64] = {nullptr};
+    static std::atomic<int *> status_addr[64];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev >= 64 || status_addr[dev] == nullptr) {
+    int *cached_status = dev < 64 ? status_addr[dev].load(std::memory_order_relaxed) : nullptr;
+    if (cached_status == nullptr) {
         e = cudaGetSymbolAddress(reinterpret_cast<void **>(&p.status), g_gemm_status);
         if (e != cudaSuccess) return e;
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
         if (e != cudaSuccess) return e;
-        if (dev < 64) status_addr[dev] = p.status;
+        if (dev < 64) status_addr[dev].store(p.status, std::memory_order_relaxed);
     } else {
-        p.status = status_addr[dev];
+        p.status = cached_status;
     }
     const int num_tiles = ((p.m + Cfg::kTileM - 1) / Cfg::kTileM) * ((p.n + kBN - 1) / kBN);
 
@@ -128,13 +130,15 @@ cudaError_t launch_gemm(GemmKind kind, int group, const GemmParams &p, int num_s
 }
 
 int *device_status_word() {
-    static int *addr[64] = {nullptr};
+    static std::atomic<int *> addr[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
-    if (dev < 64 && addr[dev]) return addr[dev];
+    if (dev < 64) {
+        if (int *c = addr[dev].load(std::memory_order_relaxed)) return c;
+    }
     int *p = nullptr;
     if (cudaGetSymbolAddress(reinterpret_cast<void **>(&p), g_gemm_status) != cudaSuccess) return nullptr;
-    if (dev < 64) addr[dev] = p;
+    if (dev < 64) addr[dev].store(p, std::memory_order_relaxed);
     return p;
 }
 

@@ -2,6 +2,7 @@
 // validation (constraints of "torch_npu.npu_all_gather_base_mm" 约束说明 and
 // "aclnnAlltoAllQuantMatmul" 约束说明, plus this kernel's alignment needs),
 // TMA tensor-map encoding, workspace carving and stream-ordered launches.
+#include <atomic>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -33,16 +34,19 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_
                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
 EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    if (!fn) {
+    static std::atomic<EncodeTiledFn> fn{nullptr};
+    EncodeTiledFn f = fn.load(std::memory_order_relaxed);
+    if (!f) {
         void *p = nullptr;
         cudaDriverEntryPointQueryResult q;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
                 cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(p);
+            q == cudaDriverEntryPointSuccess) {
+            f = reinterpret_cast<EncodeTiledFn>(p);
+            fn.store(f, std::memory_order_relaxed);
+        }
     }
-    return fn;
+    return f;
 }
 
 // 2-D map over a row-major (outer, inner) matrix with 16-bit elements and a
@@ -90,8 +94,8 @@ int current_device(DeviceInfo *info) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return fail(MC2_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
-    static int sms_cache[64] = {0};
-    int sms = dev < 64 ? sms_cache[dev] : 0;
+    static std::atomic<int> sms_cache[64];
+    int sms = dev < 64 ? sms_cache[dev].load(std::memory_order_relaxed) : 0;
     if (sms == 0) {
         e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return fail(MC2_ERR_CUDA, "cudaDeviceGetAttribute: %s", cudaGetErrorString(e));
@@ -102,7 +106,7 @@ int current_device(DeviceInfo *info) {
         if (major != 10 || minor != 3)
             return fail(MC2_ERR_UNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a only", dev,
                         major, minor);
-        if (dev < 64) sms_cache[dev] = sms;
+        if (dev < 64) sms_cache[dev].store(sms, std::memory_order_relaxed);
     }
     info->device = dev;
     info->num_sms = sms;

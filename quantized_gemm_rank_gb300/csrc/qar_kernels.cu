@@ -15,6 +15,7 @@
 // two per rank in flight per thread), the output written once.  Because G divides H,
 // the scale of flat element e is scales_r[e / G] whatever the row, so the
 // kernel runs over the flat (bs * H) range with no row arithmetic.
+#include <atomic>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
@@ -159,13 +160,15 @@ template <int kX, int kS, int kOut, int kR>
 cudaError_t launch_one(const QarPtrs &p, int64_t nvec, void *out, int num_sms, cudaStream_t stream) {
     // Persistent grid: as many CTAs as fit on the device at once (the
     // occupancy of this instantiation, looked up once per process).
-    static int per_sm = 0;
+    static std::atomic<int> per_sm_cache{0};
+    int per_sm = per_sm_cache.load(std::memory_order_relaxed);
     if (per_sm == 0) {
         int b = 0;
         cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
             &b, quant_all_reduce_kernel<kX, kS, kOut, kR>, kThreads, 0);
         if (e != cudaSuccess) return e;
         per_sm = b > 0 ? b : 1;
+        per_sm_cache.store(per_sm, std::memory_order_relaxed);
     }
     const int64_t need = (nvec + kThreads - 1) / kThreads;
     const int64_t full = static_cast<int64_t>(num_sms) * per_sm;

@@ -9,6 +9,7 @@
 //   * the optional alltoAllOut output (commOut, the rank_size received blocks
 //     stacked as (rank_size, bs_local, h) in x1's dtype), stored from the same
 //     registers that read the chunks.
+#include <atomic>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -492,11 +493,11 @@ cudaError_t launch_a2a_prologue(const ChunkPtrs &chunks, int rank_size, int64_t 
     const uint16_t *sm = static_cast<const uint16_t *>(smooth);
     auto kern = bf16 ? a2a_prologue_kernel<true> : a2a_prologue_kernel<false>;
     // rows above 48 KiB need the opt-in (raised once per process and type)
-    static size_t opted[2] = {48 * 1024, 48 * 1024};
-    if (smem > opted[bf16 ? 1 : 0]) {
+    static std::atomic<bool> opted[2];
+    if (smem > 48 * 1024 && !opted[bf16 ? 1 : 0].load(std::memory_order_relaxed)) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024 + 16);
         if (e != cudaSuccess) return e;
-        opted[bf16 ? 1 : 0] = 64 * 1024 + 16;
+        opted[bf16 ? 1 : 0].store(true, std::memory_order_relaxed);
     }
     kern<<<static_cast<unsigned>(grid), threads, smem, stream>>>(chunks, h, bs_local, rank_size, sm, qh, q_out,
                                                                  scale_out, x2, x2h, x2_vecs, widen_ctas, zero_words,
