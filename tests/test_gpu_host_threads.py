@@ -18,7 +18,7 @@ import quantized_gemm_rank_gb300 as mc2
 pytestmark = pytest.mark.gpu
 
 AG = mc2_inputs.AGShape(world_size=4, m_local=200, k=640, n=392, x2_is_nk=True, bias=True)
-A2A = mc2_inputs.A2AShape(rank_size=4, bs_local=300, h=256, n=520, quant_mode=7)
+A2A = mc2_inputs.A2AShape(rank_size=4, bs_local=300, h=256, n=528, quant_mode=7)
 THREADS = 6
 REPEATS = 4
 
