@@ -49,8 +49,8 @@ FLUSH_BYTES = 512 << 20
 # profiles/gemm_bf16_ag-8x1024.md, and the hash of the GEMM's sources
 # (GEMM_SOURCES) the capture was taken with: the figure is reported only
 # while they match.
-AG_GEMM_TRAFFIC = 295.55e6          # dram__bytes_read.sum 184.71 MB + dram__bytes_write.sum 110.83 MB
-AG_GEMM_TRAFFIC_SRC_HASH = "3d2d410b9d9d8ef8"
+AG_GEMM_TRAFFIC = 296.67e6          # dram__bytes_read.sum 185.51 MB + dram__bytes_write.sum 111.16 MB
+AG_GEMM_TRAFFIC_SRC_HASH = "5322e5f13293157c"
 
 
 def parse_args():
