@@ -355,7 +355,29 @@ def oracle_baseline(ag_s, a2a_s, host, target_s=10.0, max_reps=3):
         reps += 1
     return {"value": fl_tot / t_tot / 1e12, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
             "sample": f"{reps} whole step(s) of {WORKLOAD} (all {ag_s.m} + {a2a_s.bs_local} output rows), "
-                      f"{t_tot:.1f} s"}
+                      f"{t_tot:.1f} s",
+            "single_thread": oracle_single_thread()}
+
+
+def oracle_single_thread(rows=32, timeout_s=300):
+    """The oracle on one host thread: a child process (fork + exec, so no CUDA
+    state is inherited) with OMP_NUM_THREADS=1, on `rows` seeded rows of each
+    op's output.  None if the child fails or runs out of time."""
+    code = ("import json, bench, mc2_inputs\n"
+            "ag, a2a = mc2_inputs.WORKLOADS[bench.AG_NAME], mc2_inputs.WORKLOADS[bench.A2A_NAME]\n"
+            "host = {'ag': mc2_inputs.ag_inputs(ag, seed=0), 'a2a': mc2_inputs.a2a_inputs(a2a, seed=0)}\n"
+            "bench.oracle_sample(1, 1, ag, a2a, host)\n"
+            f"dt, fl = bench.oracle_sample({rows}, {rows}, ag, a2a, host)\n"
+            "print(json.dumps({'dt': dt, 'fl': fl}))\n")
+    env = dict(os.environ, OMP_NUM_THREADS="1")
+    try:
+        r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True, text=True,
+                           timeout=timeout_s)
+        d = json.loads(r.stdout.strip().splitlines()[-1])
+    except Exception:
+        return None
+    return {"value": d["fl"] / d["dt"] / 1e12, "unit": UNIT, "threads": 1,
+            "sample": f"{rows} seeded rows of each op's output, {d['dt']:.1f} s"}
 
 
 def run_reference(args):

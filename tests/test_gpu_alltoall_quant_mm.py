@@ -120,6 +120,17 @@ def test_full_size_dynamic_sampled_rows():
     assert_bits_equal(got["x1_scale"], s, "a2a-dyn: all scales")
 
 
+def test_literal_small_config_every_row():
+    """The dynamic-quant config read literally (8 chunks of (512, 1024) -> a
+    (512, 8192) permuted matrix), small enough for the oracle to check every
+    output: one wave of tiles, each over all eight K blocks."""
+    shape = mc2_inputs.WORKLOADS["a2a-dyn-small"]
+    inp = mc2_inputs.a2a_inputs(shape, seed=0)
+    got = run_gpu(inp, shape)
+    ref = run_oracle(inp, shape)
+    compare(got, ref, "a2a-dyn-small")
+
+
 def test_full_size_full_quant_subset():
     """The full-quant workload; the oracle checks a seeded 1024-row subset."""
     shape = mc2_inputs.WORKLOADS["a2a-full"]
