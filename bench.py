@@ -472,7 +472,39 @@ def extra_table(dev, flush, stream, steps, hbm_peak):
             res[name] = {"us": round(t * 1e3, 2), "tflops": round(work / (t * 1e-3) / 1e12, 1)}
         del fn
         torch.cuda.empty_cache()
+    res["int8_context"] = int8_context(dev, flush, stream, steps)
     return res
+
+
+def int8_context(dev, flush, stream, steps):
+    """Context for the integer path's route (int8 as exact fp16 through tcgen05):
+    the legacy mma.sync int8 and fp16 rates of this GPU (register operands, all
+    SMs busy), and torch._int_mm (the library int8 GEMM) on the a2a-dyn shape."""
+    import quantized_gemm_rank_gb300 as mc2
+    out = {}
+    blocks = 4 * torch.cuda.get_device_properties(dev).multi_processor_count
+    sink = torch.empty(blocks * 256, dtype=torch.int32, device=dev)
+    for kind, key in ((0, "mma_sync_s8_tops"), (1, "mma_sync_f16_tflops")):
+        ops = [0.0]
+
+        def fn(kind=kind):
+            ops[0] = mc2.mc2_calib_mma_sync(kind, 2048, blocks, sink, stream=stream)
+
+        t = statistics.median(time_device(fn, steps, 3, flush, stream))
+        out[key] = round(ops[0] / (t * 1e-3) / 1e12, 1)
+    s = mc2_inputs.WORKLOADS[A2A_NAME]
+    a = torch.randint(-127, 128, (s.bs_local, s.k), dtype=torch.int8, device=dev)
+    b = torch.randint(-127, 128, (s.n, s.k), dtype=torch.int8, device=dev).t()   # (k, n), column-major
+    try:
+        t = statistics.median(time_device(lambda: torch._int_mm(a, b), steps, 3, flush, stream))
+        out["torch_int_mm_tops"] = round(s.ops / (t * 1e-3) / 1e12, 1)
+    except RuntimeError as e:
+        out["torch_int_mm_tops"] = None
+        out["torch_int_mm_error"] = str(e).splitlines()[0][:120]
+    out["torch_int_mm_shape"] = f"({s.bs_local}, {s.k}) @ ({s.k}, {s.n}) int8 -> int32"
+    del a, b, sink
+    torch.cuda.empty_cache()
+    return out
 
 
 def profile_workload(name, args):

@@ -268,6 +268,19 @@ int mc2_alltoall_quant_mm_no_alloc(const void *const *chunks, int rank_size, int
                                    void *out, void *alltoall_out, int8_t *q_out, float *x1_scale_out,
                                    int32_t *acc_out, void *stream);
 
+/*
+ * Calibration (not part of the operations): launches `blocks` CTAs of 256
+ * threads on `stream`, each warp running `iters` rounds of 8 independent
+ * legacy warp-level tensor-core MMAs (mma.sync) on register operands:
+ * kind 0 = int8 x int8 -> int32 (m16n8k32), kind 1 = fp16 x fp16 -> fp32
+ * (m16n8k16).  `sink` (device, blocks * 256 int32, caller-owned) receives one
+ * word per thread so that the work stays live.  *ops receives the operations
+ * (2 per multiply-add) one launch performs; time the launch with events on
+ * `stream` for the rate.  Returns MC2_ERR_NULL / MC2_ERR_SHAPE on bad
+ * arguments, MC2_ERR_CUDA if the launch fails.
+ */
+int mc2_calib_mma_sync(int kind, int64_t iters, int blocks, int32_t *sink, void *stream, double *ops);
+
 /* Name of a status code (static string). */
 const char *mc2_status_str(int status);
 

@@ -79,6 +79,8 @@ def lib() -> ctypes.CDLL:
         L.mc2_last_error.restype = ctypes.c_char_p
         L.mc2_device_status.argtypes = []
         L.mc2_device_status.restype = _INT
+        L.mc2_calib_mma_sync.argtypes = [_INT, _I64, _INT, _P, _P, ctypes.POINTER(ctypes.c_double)]
+        L.mc2_calib_mma_sync.restype = _INT
         _lib = L
     return _lib
 
@@ -305,12 +307,23 @@ def mc2_device_status() -> int:
     return int(lib().mc2_device_status())
 
 
+def mc2_calib_mma_sync(kind: int, iters: int, blocks: int, sink: torch.Tensor, stream=None) -> float:
+    """Launch the legacy mma.sync rate kernel (kind 0: int8 -> int32, 1: fp16 ->
+    fp32) on `stream`; returns the operations the launch performs.  `sink` is a
+    device int32 tensor of at least blocks * 256 elements."""
+    if sink.dtype != torch.int32 or sink.numel() < blocks * 256:
+        raise ValueError("sink must be a device int32 tensor of blocks * 256 elements")
+    ops = ctypes.c_double(0.0)
+    _check(lib().mc2_calib_mma_sync(kind, iters, blocks, _dev(sink, "sink"), _stream(stream), ctypes.byref(ops)))
+    return ops.value
+
+
 __all__ = [
     "Mc2Error", "lib", "library_path", "status_str", "last_error", "mc2_all_gather_mm",
     "mc2_matmul_reduce_scatter", "mc2_matmul_weight_grad", "mc2_quant_all_reduce",
     "mc2_alltoall_quant_mm_workspace", "mc2_alltoall_quant_mm",
     "mc2_alltoall_quant_mm_no_alloc",
-    "NO_ALLOC_SCRATCH_BYTES", "mc2_device_status",
+    "NO_ALLOC_SCRATCH_BYTES", "mc2_device_status", "mc2_calib_mma_sync",
     "MC2_OK", "MC2_ERR_NULL", "MC2_ERR_SHAPE", "MC2_ERR_DTYPE", "MC2_ERR_UNSUPPORTED", "MC2_ERR_WORKSPACE",
     "MC2_ERR_CUDA", "MC2_ERR_TIMEOUT", "MC2_F16", "MC2_BF16", "MC2_F32", "MC2_I8",
     "MC2_F8E4M3", "MC2_F8E5M2", "MC2_E8M0",

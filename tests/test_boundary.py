@@ -42,6 +42,19 @@ def test_library_exports_every_declared_symbol():
         assert hasattr(L, name), name
 
 
+def test_calibration_rejects_before_launch():
+    import ctypes
+    L = mc2.lib()
+    ops = ctypes.c_double(-1.0)
+    fake = ctypes.c_void_p(256)   # never dereferenced: validation fails first
+    assert L.mc2_calib_mma_sync(0, 16, 4, None, None, ctypes.byref(ops)) == mc2.MC2_ERR_NULL
+    assert L.mc2_calib_mma_sync(0, 16, 4, fake, None, None) == mc2.MC2_ERR_NULL
+    assert L.mc2_calib_mma_sync(2, 16, 4, fake, None, ctypes.byref(ops)) == mc2.MC2_ERR_SHAPE
+    assert L.mc2_calib_mma_sync(0, 0, 4, fake, None, ctypes.byref(ops)) == mc2.MC2_ERR_SHAPE
+    assert L.mc2_calib_mma_sync(1, 16, 0, fake, None, ctypes.byref(ops)) == mc2.MC2_ERR_SHAPE
+    assert ops.value == -1.0
+
+
 def test_status_strings():
     assert mc2.status_str(0) == "MC2_OK"
     assert mc2.status_str(mc2.MC2_ERR_TIMEOUT) == "MC2_ERR_TIMEOUT"
