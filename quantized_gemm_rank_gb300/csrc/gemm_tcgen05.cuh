@@ -342,6 +342,10 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
     // The set-up above may overlap the previous kernel of the stream; nothing in
     // global memory is touched before it has completed.
     ptx::grid_dependency_wait();
+    // The next kernel of the stream may be scheduled from now on: its CTAs take
+    // the SMs this grid leaves, and it waits for this grid to complete before
+    // it touches global memory.
+    ptx::allow_dependent_launch();
 
     if (warp == 0 && lane == 0) {
         // ------------------------------------------------------------ TMA producer

@@ -223,6 +223,9 @@ __global__ void __launch_bounds__(kPrologueThreads) a2a_prologue_kernel(
     int64_t widen_ctas, int *__restrict__ zero_words, int n_zero, uint16_t *__restrict__ comm_out, int *status,
     uint64_t wait_limit_ns) {
     extern __shared__ __align__(128) uint8_t prow[];   // the permuted row (K bf16/fp16), then its mbarrier
+    // launched as a programmatic dependent of the stream's previous kernel:
+    // nothing in global memory is touched before that kernel has completed
+    ptx::grid_dependency_wait();
     const int64_t b = blockIdx.x;
     // the GEMM's stream-K counters start at zero (it runs after this kernel)
     if (b == gridDim.x - 1)
@@ -499,9 +502,20 @@ cudaError_t launch_a2a_prologue(const ChunkPtrs &chunks, int rank_size, int64_t 
         if (e != cudaSuccess) return e;
         opted[bf16 ? 1 : 0].store(true, std::memory_order_relaxed);
     }
-    kern<<<static_cast<unsigned>(grid), threads, smem, stream>>>(chunks, h, bs_local, rank_size, sm, qh, q_out,
-                                                                 scale_out, x2, x2h, x2_vecs, widen_ctas, zero_words,
-                                                                 n_zero, co, status, wait_limit_ns);
+    // its CTAs may be scheduled before the previous kernel ends (they wait for it)
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(threads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, chunks, h, bs_local, rank_size, sm, qh, q_out, scale_out, x2, x2h,
+                                       x2_vecs, widen_ctas, zero_words, n_zero, co, status, wait_limit_ns);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
