@@ -13,7 +13,7 @@ namespace {
 // occupancy calculator (cached per device).
 template <bool kBF16, bool kIntPath, bool kRS = false>
 int concurrent_pairs(int num_sms) {
-    using Cfg = TileCfg<2, !kRS && !kIntPath>;
+    using Cfg = TileCfg<2, !kRS>;
     static std::atomic<int> cached[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return num_sms / 2;
@@ -43,7 +43,7 @@ int concurrent_pairs(int num_sms) {
 
 template <int kG, bool kBF16, bool kIntPath, bool kRS = false>
 cudaError_t launch_one(const GemmParams &p_in, int num_sms, cudaStream_t stream) {
-    using Cfg = TileCfg<kG, !kRS && !kIntPath>;
+    using Cfg = TileCfg<kG, !kRS>;
     auto kern = mc2_gemm_kernel<kG, kBF16, kIntPath, kRS>;
     GemmParams p = p_in;
     // per device, once: the status word's address and the shared-memory opt-in
@@ -81,11 +81,10 @@ cudaError_t launch_one(const GemmParams &p_in, int num_sms, cudaStream_t stream)
         attr[1].val.clusterDim.z = 1;
         cfg.numAttrs = 2;
         const int clusters = concurrent_pairs<kBF16, kIntPath, kRS>(num_sms);
-        // with a stream-K tail every co-resident pair takes part
-        const int grid_clusters = (p.sk_tiles > 0 || num_tiles >= clusters) ? clusters : num_tiles;
+        const int grid_clusters = num_tiles >= clusters ? clusters : num_tiles;
         cfg.gridDim = dim3(2 * grid_clusters, 1, 1);
     } else {
-        const int units = p.sk_tiles > 0 ? num_sms : (num_tiles < num_sms ? num_tiles : num_sms);
+        const int units = num_tiles < num_sms ? num_tiles : num_sms;
         cfg.gridDim = dim3(units, 1, 1);
     }
     e = cudaLaunchKernelEx(&cfg, kern, p);
@@ -96,17 +95,6 @@ cudaError_t launch_one(const GemmParams &p_in, int num_sms, cudaStream_t stream)
 }  // namespace
 
 int gemm_group_for(int m) { return m > kBM ? 2 : 1; }
-
-int gemm_units(GemmKind kind, int group, int num_sms) {
-    if (group == 1) return num_sms;
-    switch (kind) {
-        case GEMM_F16: return concurrent_pairs<false, false>(num_sms);
-        case GEMM_BF16: return concurrent_pairs<true, false>(num_sms);
-        case GEMM_RS_F16: return concurrent_pairs<false, false, true>(num_sms);
-        case GEMM_RS_BF16: return concurrent_pairs<true, false, true>(num_sms);
-        default: return concurrent_pairs<false, true>(num_sms);
-    }
-}
 
 cudaError_t launch_gemm(GemmKind kind, int group, const GemmParams &p, int num_sms, cudaStream_t stream) {
     if (group == 2) {

@@ -109,12 +109,9 @@ struct GemmParams {
     const void *bias16;             // float path: (n) in the operand dtype, or null
     const float *x1_scale;          // integer path: (m)
     const float *x2_scale;          // integer path: (n)
-    const void *bias_q;             // integer path: (n) fp32 or bf16, or null
+    const void *bias_q;             // integer path: (n) fp32 or bf16 (required), 16-byte aligned
     int bias_q_bf16;
     int32_t *acc_out;               // integer path: optional (m, n)
-    int sk_tiles;                   // integer path: tiles of the stream-K tail (0: all data-parallel)
-    int32_t *sk_partials;           // stream-K partial sums: slot (unit * 2 + cta) of 128 x 256 int32
-    int *sk_flags;                  // stream-K: partial parts written, per (tile, cta); zero at launch
     int *status;                    // device word set to -7 when a bounded wait gives up
     uint64_t wait_limit_ns;
     // reduce-scatter instantiation only (kRS): B is rank r's weight shard for the
@@ -126,79 +123,26 @@ struct GemmParams {
 };
 
 // ---------------------------------------------------------------------------
-// Work schedule of one cluster (identical in every role of every CTA of it).
-// Tiles [0, num_tiles - sk_tiles) are data-parallel: cluster c takes tiles
-// c, c + U, ... whole.  The K blocks of the last sk_tiles tiles are laid end to
-// end and cut into U equal ranges, one per cluster; a range shorter than a
-// tile covers at most two parts: the end of one tile and the start of the next.
-// A part that does not end at its tile's end is a WRITE part (its int32 sums
-// go to the cluster's partial slot); a part that ends there but starts inside
-// the tile is a FINISH part (it adds the WRITE parts of the earlier clusters);
-// WRITE parts are scheduled first, so a FINISH part never waits on a cluster
-// that is itself waiting.
-enum WorkKind : int { WORK_FULL = 0, WORK_WRITE = 1, WORK_FINISH = 2 };
-
+// Work schedule of one cluster (identical in every role of every CTA of it):
+// cluster c takes tiles c, c + U, c + 2U, ... whole (U clusters in the grid),
+// each over all its K blocks.
 struct Work {
-    int tile, kb0, kb1, kind;
+    int tile, kb0, kb1;
 };
 
 struct Schedule {
-    int c, U, nkb, dp_tiles, n_dp, n_sk;
-    long long total;  // K blocks in the stream-K region
-    Work sk[2];
+    int c, U, nkb, n;
 
-    __device__ __forceinline__ long long range_start(int u) const { return static_cast<long long>(u) * total / U; }
-
-    __device__ __forceinline__ void init(int cluster, int units, int num_tiles, int sk_tiles, int nkb_) {
+    __device__ __forceinline__ void init(int cluster, int units, int num_tiles, int nkb_) {
         c = cluster;
         U = units;
         nkb = nkb_;
-        dp_tiles = num_tiles - sk_tiles;
-        n_dp = c < dp_tiles ? (dp_tiles - c + U - 1) / U : 0;
-        total = static_cast<long long>(sk_tiles) * nkb;
-        n_sk = 0;
-        if (sk_tiles == 0) return;
-        const long long s0 = range_start(c), e0 = range_start(c + 1);
-        if (s0 == e0) return;
-        const int t0 = static_cast<int>(s0 / nkb);
-        const int kb0 = static_cast<int>(s0 - static_cast<long long>(t0) * nkb);
-        const int kb1 = static_cast<int>(min(static_cast<long long>(nkb), kb0 + (e0 - s0)));
-        Work a{dp_tiles + t0, kb0, kb1, kb1 < nkb ? WORK_WRITE : (kb0 > 0 ? WORK_FINISH : WORK_FULL)};
-        if (e0 > static_cast<long long>(t0 + 1) * nkb) {
-            // the range continues into the next tile: that start part is a WRITE part, done first
-            Work b{dp_tiles + t0 + 1, 0, static_cast<int>(e0 - static_cast<long long>(t0 + 1) * nkb), WORK_WRITE};
-            sk[0] = b;
-            sk[1] = a;
-            n_sk = 2;
-        } else {
-            sk[0] = a;
-            n_sk = 1;
-        }
+        n = c < num_tiles ? (num_tiles - c + U - 1) / U : 0;
     }
 
-    __device__ __forceinline__ int count() const { return n_dp + n_sk; }
+    __device__ __forceinline__ int count() const { return n; }
 
-    __device__ __forceinline__ Work get(int i) const {
-        if (i < n_dp) return Work{c + i * U, 0, nkb, WORK_FULL};
-        return sk[i - n_dp];
-    }
-
-    // Clusters u < c whose non-empty range reaches into `tile` (the WRITE parts a
-    // FINISH part of that tile adds), visited in descending u.
-    template <class F>
-    __device__ __forceinline__ int for_each_writer(int tile, F f) const {
-        const long long g0 = static_cast<long long>(tile - dp_tiles) * nkb;
-        int n = 0;
-        for (int u = c - 1; u >= 0; --u) {
-            const long long su = range_start(u), eu = range_start(u + 1);
-            if (eu <= g0) break;
-            if (su < eu) {
-                f(u);
-                ++n;
-            }
-        }
-        return n;
-    }
+    __device__ __forceinline__ Work get(int i) const { return Work{c + i * U, 0, nkb}; }
 };
 
 // Raster order of the tiles: groups of gm m-tiles, each walked m-fastest
@@ -285,7 +229,7 @@ __device__ __forceinline__ void store_row32_16(uint16_t *row_ptr, int n, int col
 
 template <int kG, bool kBF16, bool kIntPath, bool kRS = false>
 __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_constant__ GemmParams p) {
-    constexpr bool kTmaOut = !kRS && !kIntPath;  // epilogue stores through shared slabs and TMA
+    constexpr bool kTmaOut = !kRS;  // epilogue stores through shared slabs and TMA
     using Cfg = TileCfg<kG, kTmaOut>;
     constexpr bool kPair = kG == 2;
     constexpr int S = Cfg::kStages;
@@ -315,7 +259,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
     const int num_clusters = gridDim.x / kG;
     const int nkb = (num_k + p.kblock_tiles - 1) / p.kblock_tiles;  // K blocks per tile
     Schedule sched;
-    sched.init(cluster_id, num_clusters, num_tiles, p.sk_tiles, nkb);
+    sched.init(cluster_id, num_clusters, num_tiles, nkb);
 
     if (threadIdx.x == 0) {
         abort_flag_s = 0;
@@ -656,64 +600,15 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
                 ++acc_iter;
             }
             if (!ok) break;
-            if constexpr (kIntPath) {
-                // stream-K: this thread's 128 sums of row (32q + lane) in slot (unit, cta)
-                const int r_in = 32 * q + lane;
-                if (w.kind == WORK_WRITE) {
-                    int32_t *slot = p.sk_partials + (static_cast<size_t>(cluster_id * 2 + cr) * kBM + r_in) * kBN +
-                                    half * 128;
-#pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        __stcg(reinterpret_cast<int4 *>(slot) + j,
-                               make_int4(sum[4 * j], sum[4 * j + 1], sum[4 * j + 2], sum[4 * j + 3]));
-                    __threadfence();
-                    __syncwarp();
-                    if (lane == 0) atomicAdd(&p.sk_flags[w.tile * 2 + cr], 1);
-                    continue;
-                }
-                if (w.kind == WORK_FINISH) {
-                    // wait until every epilogue warp of every earlier part has published
-                    const int need = kNumEpiWarps * sched.for_each_writer(w.tile, [](int) {});
-                    volatile int *flag = p.sk_flags + w.tile * 2 + cr;
-                    if (*flag < need) {
-                        const uint64_t start = ptx::globaltimer_ns();
-                        while (*flag < need) {
-                            if (*abort_flag || ptx::globaltimer_ns() - start > p.wait_limit_ns) {
-                                *abort_flag = 1;
-                                if (p.status) atomicExch(p.status, -7);
-                                ok = false;
-                                break;
-                            }
-                            ptx::nanosleep(64);
-                        }
-                    }
-                    if (!ok) break;
-                    __threadfence();
-                    sched.for_each_writer(w.tile, [&](int u) {
-                        const int32_t *slot = p.sk_partials + (static_cast<size_t>(u * 2 + cr) * kBM + r_in) * kBN +
-                                              half * 128;
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            const int4 v = __ldcg(reinterpret_cast<const int4 *>(slot) + j);
-                            sum[4 * j] += v.x;
-                            sum[4 * j + 1] += v.y;
-                            sum[4 * j + 2] += v.z;
-                            sum[4 * j + 3] += v.w;
-                        }
-                    });
-                }
-            }
             const bool row_ok = row < p.m;
-            if constexpr (kRS || kIntPath) {
-                if (!row_ok) continue;   // no warp-wide steps below on these paths
+            if constexpr (kRS) {
+                if (!row_ok) continue;   // no warp-wide steps below on this path
             }
-            // Float path: this warp's 32 rows x 128 columns leave as two 64-column
-            // slabs: rounded 16-bit values go to its shared staging slab (128-byte
-            // rows, chunk j of row r at ((j ^ (r % 8)) * 16)), then one TMA store per
+            // This warp's 32 rows x 128 columns leave as two 64-column slabs:
+            // rounded 16-bit values go to its shared staging slab (128-byte rows,
+            // chunk j of row r at ((j ^ (r % 8)) * 16)), then one TMA store per
             // slab; rows and columns past the output are clipped by the TMA unit.
-            // The reduce-scatter writes rows straight to the ranks' outputs, and the
-            // integer path (whose dequant leaves fewer registers) straight from its
-            // registers.
+            // The reduce-scatter writes rows straight to the ranks' outputs.
             uint8_t *slab = reinterpret_cast<uint8_t *>(epi_stage) + (warp - 4) * kEpiSlabBytes;
             const int slab_row0 = mb * Cfg::kTileM + kBM * static_cast<int>(cr) + 32 * q;
             auto put = [&](int c, const uint32_t (&pk)[16]) {
@@ -772,23 +667,75 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
                 for (int c = 0; c < 4; ++c) {
                     const int col0 = colh + c * 32;
                     uint32_t pk[16];
+                    if (col0 + 32 <= p.n) {
+                        // a whole chunk: its column scales and biases by 16-byte read-only
+                        // loads (16-byte aligned: col0 % 32 == 0), 16 columns at a time,
+                        // issued together before the arithmetic
 #pragma unroll
-                    for (int i = 0; i < 32; i += 2) {
-                        float o[2];
+                        for (int h = 0; h < 2; ++h) {
+                            const int cg = col0 + 16 * h;
+                            float sc[16], bs[16];
 #pragma unroll
-                        for (int e = 0; e < 2; ++e) {
-                            const int col = min(col0 + i + e, p.n - 1);
-                            float v = __int2float_rn(sum[c * 32 + i + e]);
-                            v = __fmul_rn(v, s1);
-                            v = __fmul_rn(v, p.x2_scale[col]);
-                            if (p.bias_q != nullptr) {
-                                const float bv = p.bias_q_bf16 ? load16<true>(p.bias_q, col)
-                                                               : reinterpret_cast<const float *>(p.bias_q)[col];
-                                v = __fadd_rn(v, bv);
+                            for (int q4 = 0; q4 < 4; ++q4) {
+                                const float4 t = __ldg(reinterpret_cast<const float4 *>(p.x2_scale + cg) + q4);
+                                sc[4 * q4] = t.x;
+                                sc[4 * q4 + 1] = t.y;
+                                sc[4 * q4 + 2] = t.z;
+                                sc[4 * q4 + 3] = t.w;
                             }
-                            o[e] = v;
+                            if (p.bias_q_bf16) {
+#pragma unroll
+                                for (int q8 = 0; q8 < 2; ++q8) {
+                                    const uint4 t = __ldg(
+                                        reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(p.bias_q) + cg) + q8);
+                                    const uint32_t w[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+                                    for (int e = 0; e < 4; ++e) {
+                                        bs[8 * q8 + 2 * e] = __uint_as_float(w[e] << 16);
+                                        bs[8 * q8 + 2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
+                                    }
+                                }
+                            } else {
+#pragma unroll
+                                for (int q4 = 0; q4 < 4; ++q4) {
+                                    const float4 t =
+                                        __ldg(reinterpret_cast<const float4 *>(static_cast<const float *>(p.bias_q) + cg) + q4);
+                                    bs[4 * q4] = t.x;
+                                    bs[4 * q4 + 1] = t.y;
+                                    bs[4 * q4 + 2] = t.z;
+                                    bs[4 * q4 + 3] = t.w;
+                                }
+                            }
+#pragma unroll
+                            for (int i = 0; i < 16; i += 2) {
+                                float o[2];
+#pragma unroll
+                                for (int e = 0; e < 2; ++e) {
+                                    float v = __int2float_rn(sum[c * 32 + 16 * h + i + e]);
+                                    v = __fmul_rn(v, s1);
+                                    v = __fmul_rn(v, sc[i + e]);
+                                    o[e] = __fadd_rn(v, bs[i + e]);
+                                }
+                                pk[8 * h + (i >> 1)] = pack2<true>(o[0], o[1]);
+                            }
                         }
-                        pk[i >> 1] = pack2<true>(o[0], o[1]);
+                    } else {
+                        // the ragged last chunk: columns clamped to the output
+#pragma unroll
+                        for (int i = 0; i < 32; i += 2) {
+                            float o[2];
+#pragma unroll
+                            for (int e = 0; e < 2; ++e) {
+                                const int col = min(col0 + i + e, p.n - 1);
+                                float v = __int2float_rn(sum[c * 32 + i + e]);
+                                v = __fmul_rn(v, s1);
+                                v = __fmul_rn(v, p.x2_scale[col]);
+                                const float bv = p.bias_q_bf16 ? load16<true>(p.bias_q, col)
+                                                               : static_cast<const float *>(p.bias_q)[col];
+                                o[e] = __fadd_rn(v, bv);
+                            }
+                            pk[i >> 1] = pack2<true>(o[0], o[1]);
+                        }
                     }
                     put(c, pk);
                     if (p.acc_out != nullptr && row_ok && col0 < p.n) {
@@ -809,7 +756,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
             }
         }
         // every output store has completed before the CTA can exit
-        if constexpr (!kRS && !kIntPath) {
+        if constexpr (kTmaOut) {
             if (lane == 0) ptx::bulk_wait_group<0>();
             __syncwarp();
         }

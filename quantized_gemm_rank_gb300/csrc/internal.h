@@ -21,11 +21,6 @@ struct GemmParams;
 enum GemmKind : int { GEMM_F16 = 0, GEMM_BF16 = 1, GEMM_INT_AS_F16 = 2, GEMM_RS_F16 = 3, GEMM_RS_BF16 = 4 };
 // group: 1 = one CTA per 128 x 256 tile, 2 = a CTA pair per 256 x 256 tile.
 int gemm_group_for(int m);
-// Work units (CTAs for group 1, CTA pairs for group 2) co-resident on the device;
-// the persistent grid launches this many when a stream-K tail is used.
-int gemm_units(GemmKind kind, int group, int num_sms);
-// Stream-K partial slots reserved in the workspace: at most this many work units.
-constexpr int kSkMaxUnits = 76;
 cudaError_t launch_gemm(GemmKind kind, int group, const GemmParams &p, int num_sms, cudaStream_t stream);
 int read_and_clear_gemm_status(int *status);
 // Device address of the status word that bounded waits set to -7 (cached per device).
@@ -38,16 +33,13 @@ cudaError_t launch_quant_pertoken(const ChunkPtrs &chunks, int rank_size, int64_
                                   const void *smooth, __half *qh, int8_t *q_out, float *scale_out, void *comm_out,
                                   int num_sms, cudaStream_t stream);
 // One launch doing both the per-token dynamic quant and the x2 widening
-// (h % 8 == 0 and rank_size*h <= 32768, see a2a_prologue_fits).  Also sets
-// zero_words[0, n_zero) to 0.
+// (h % 8 == 0 and rank_size*h <= 32768, see a2a_prologue_fits).
 bool a2a_prologue_fits(int rank_size, int64_t bs_local, int h);
 cudaError_t launch_a2a_prologue(const ChunkPtrs &chunks, int rank_size, int64_t bs_local, int h, bool bf16,
                                 const void *smooth, __half *qh, int8_t *q_out, float *scale_out, const int8_t *x2,
-                                __half *x2h, int64_t x2_count, int *zero_words, int n_zero, void *comm_out,
-                                int *status, uint64_t wait_limit_ns, cudaStream_t stream);
-// Also sets zero_words[0, n_zero) to 0 (the GEMM's stream-K counters).
-cudaError_t launch_widen_i8(const int8_t *src, __half *dst, int64_t count, int num_sms, int *zero_words, int n_zero,
-                            cudaStream_t stream);
+                                __half *x2h, int64_t x2_count, void *comm_out, int *status, uint64_t wait_limit_ns,
+                                cudaStream_t stream);
+cudaError_t launch_widen_i8(const int8_t *src, __half *dst, int64_t count, int num_sms, cudaStream_t stream);
 // Widens each rank's int8 chunk to fp16 in its own layout at dst + r*bs_local*h
 // (h % 16 == 0); q_out (optional) receives the permuted int8 matrix.
 cudaError_t launch_widen_chunks_i8(const ChunkPtrs &chunks, int rank_size, int64_t bs_local, int h, __half *dst,

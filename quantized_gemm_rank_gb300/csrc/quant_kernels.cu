@@ -220,16 +220,13 @@ __global__ void __launch_bounds__(kPrologueThreads) a2a_prologue_kernel(
     const __grid_constant__ ChunkPtrs chunks, int h, int64_t bs_local, int rank_size,
     const uint16_t *__restrict__ smooth, __half *__restrict__ qh, int8_t *__restrict__ q_out,
     float *__restrict__ scale_out, const int8_t *__restrict__ x2, __half *__restrict__ x2h, int64_t x2_vecs,
-    int64_t widen_ctas, int *__restrict__ zero_words, int n_zero, uint16_t *__restrict__ comm_out, int *status,
+    int64_t widen_ctas, uint16_t *__restrict__ comm_out, int *status,
     uint64_t wait_limit_ns) {
     extern __shared__ __align__(128) uint8_t prow[];   // the permuted row (K bf16/fp16), then its mbarrier
     // launched as a programmatic dependent of the stream's previous kernel:
     // nothing in global memory is touched before that kernel has completed
     ptx::grid_dependency_wait();
     const int64_t b = blockIdx.x;
-    // the GEMM's stream-K counters start at zero (it runs after this kernel)
-    if (b == gridDim.x - 1)
-        for (int i = threadIdx.x; i < n_zero; i += blockDim.x) zero_words[i] = 0;
     const int64_t G = gridDim.x;
     const int64_t before = b * widen_ctas / G;  // widen CTAs among [0, b)
     if ((b + 1) * widen_ctas / G > before) {
@@ -356,10 +353,7 @@ __global__ void __launch_bounds__(kPrologueThreads) a2a_prologue_kernel(
 
 // int8 -> fp16, exact, 16 elements per thread-iteration.
 __global__ void __launch_bounds__(256) widen_i8_kernel(const int8_t *__restrict__ src, __half *__restrict__ dst,
-                                                       int64_t count, int *__restrict__ zero_words, int n_zero) {
-    // the GEMM's stream-K counters start at zero (it runs after this kernel)
-    if (blockIdx.x == 0)
-        for (int i = threadIdx.x; i < n_zero; i += blockDim.x) zero_words[i] = 0;
+                                                       int64_t count) {
     const int64_t nvec = count / 16;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < nvec; i += stride) {
@@ -480,7 +474,7 @@ bool a2a_prologue_fits(int rank_size, int64_t bs_local, int h) {
 
 cudaError_t launch_a2a_prologue(const ChunkPtrs &chunks, int rank_size, int64_t bs_local, int h, bool bf16,
                                 const void *smooth, __half *qh, int8_t *q_out, float *scale_out, const int8_t *x2,
-                                __half *x2h, int64_t x2_count, int *zero_words, int n_zero, void *comm_out,
+                                __half *x2h, int64_t x2_count, void *comm_out,
                                 int *status, uint64_t wait_limit_ns, cudaStream_t stream) {
     uint16_t *co = static_cast<uint16_t *>(comm_out);
     const int K = rank_size * h;
@@ -514,14 +508,13 @@ cudaError_t launch_a2a_prologue(const ChunkPtrs &chunks, int rank_size, int64_t 
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     cudaError_t e = cudaLaunchKernelEx(&cfg, kern, chunks, h, bs_local, rank_size, sm, qh, q_out, scale_out, x2, x2h,
-                                       x2_vecs, widen_ctas, zero_words, n_zero, co, status, wait_limit_ns);
+                                       x2_vecs, widen_ctas, co, status, wait_limit_ns);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
-cudaError_t launch_widen_i8(const int8_t *src, __half *dst, int64_t count, int num_sms, int *zero_words, int n_zero,
-                            cudaStream_t stream) {
-    widen_i8_kernel<<<grid_for(count / 16 + 1, 256, num_sms), 256, 0, stream>>>(src, dst, count, zero_words, n_zero);
+cudaError_t launch_widen_i8(const int8_t *src, __half *dst, int64_t count, int num_sms, cudaStream_t stream) {
+    widen_i8_kernel<<<grid_for(count / 16 + 1, 256, num_sms), 256, 0, stream>>>(src, dst, count);
     return cudaGetLastError();
 }
 

@@ -113,3 +113,38 @@ def test_largest_k(name):
     ref, ref_g = oracle.all_gather_mm(inp["chunks"], inp["x2"], x2_is_nk=shape.x2_is_nk, bias=inp["bias"])
     assert_close_16(out, ref, f"{name}: out")
     assert_bits_equal(gathered, ref_g, f"{name}: gathered")
+
+
+# Several K blocks of 1024 per tile (the fp32 block sums added in order),
+# fewer pair tiles than co-resident CTA pairs, a ragged last K block and
+# n-tile: every output row against the oracle.
+KBLOCK_CASES = {
+    "kblocks-bf16-kn-bias": mc2_inputs.AGShape(world_size=2, m_local=1280, k=3072, n=1024, bias=True),
+    "kblocks-fp16-nk-ragged": mc2_inputs.AGShape(world_size=4, m_local=520, k=2112, n=1000, dtype=torch.float16,
+                                                 x2_is_nk=True),
+}
+
+
+@pytest.mark.parametrize("name", sorted(KBLOCK_CASES))
+def test_several_k_blocks_every_row(name):
+    shape = KBLOCK_CASES[name]
+    inp = mc2_inputs.ag_inputs(shape, seed=21)
+    out, gathered = run_gpu(inp, shape)
+    ref, ref_g = oracle.all_gather_mm(inp["chunks"], inp["x2"], x2_is_nk=shape.x2_is_nk, bias=inp["bias"])
+    assert_close_16(out, ref, f"{name}: out")
+    assert_bits_equal(gathered, ref_g, f"{name}: gathered")
+
+
+@pytest.mark.parametrize("x2_is_nk", [False, True])
+def test_several_k_blocks_integer_valued_bit_exact(x2_is_nk):
+    """Small-integer operands over four K blocks (the last one ragged): every
+    block sum is exact, so a block added twice or missed changes the bits."""
+    g = torch.Generator().manual_seed(9)
+    R, ml, k, n = 2, 1280, 3136, 776
+    chunks = [torch.randint(-3, 4, (ml, k), generator=g).to(torch.bfloat16) for _ in range(R)]
+    x2 = torch.randint(-3, 4, (n, k) if x2_is_nk else (k, n), generator=g).to(torch.bfloat16)
+    dev = torch.device("cuda")
+    out, gathered = mc2.mc2_all_gather_mm([c.to(dev) for c in chunks], x2.to(dev), x2_is_nk=x2_is_nk)
+    ref, ref_g = oracle.all_gather_mm(chunks, x2, x2_is_nk=x2_is_nk)
+    assert_bits_equal(out, ref, "out")
+    assert_bits_equal(gathered, ref_g, "gathered")

@@ -220,20 +220,20 @@ def test_quant_ties_and_near_ties_on_gpu():
 
 
 @pytest.mark.parametrize("n,mode", [(2560, 3), (4352, 7), (4352, 3)])
-def test_stream_k_tail_exact(n, mode):
-    """Shapes whose tile count is not a multiple of the co-resident CTA pairs,
-    so the leftover tiles are split by K blocks across pairs (stream-K) and
-    their int32 partial sums combined: every output element bit for bit."""
+def test_partial_last_wave_exact(n, mode):
+    """Shapes whose tile count is not a multiple of the co-resident CTA pairs
+    (a partial last wave), four K blocks of exact int32 sums per tile: every
+    output element bit for bit."""
     shape = A2A(rank_size=8, bs_local=2048, h=512, n=n, quant_mode=mode)   # 8 x (n/256) tiles, 4 K blocks each
     inp = mc2_inputs.a2a_inputs(shape, seed=31)
     got = run_gpu(inp, shape)
     ref = run_oracle(inp, shape)
-    compare(got, ref, f"stream-K n={n} mode={mode}")
+    compare(got, ref, f"partial wave n={n} mode={mode}")
 
 
-def test_stream_k_all_127_bound():
-    """All-127 operands through the stream-K tail: exact int32 partials at the
-    accumulator bound (8192 * 16129 = 132128768)."""
+def test_all_127_bound_over_k_blocks():
+    """All-127 operands over eight K blocks: the exact int32 block sums reach
+    the accumulator bound (8192 * 16129 = 132128768)."""
     shape = A2A(rank_size=8, bs_local=2048, h=1024, n=2560, quant_mode=3)
     inp = mc2_inputs.a2a_inputs(shape, seed=2)
     inp["chunks"] = [torch.full_like(c, -127) for c in inp["chunks"]]
@@ -241,7 +241,7 @@ def test_stream_k_all_127_bound():
     got = run_gpu(inp, shape)
     assert torch.all(got["acc"] == -8192 * 16129)
     ref = run_oracle(inp, shape, rows=[0, 1, 1023, 2047])
-    compare(got, ref, "stream-K all-127", rows=[0, 1, 1023, 2047])
+    compare(got, ref, "all-127", rows=[0, 1, 1023, 2047])
 
 
 # rank_size * H at the top of the page's range (<= 35000, a multiple of 16):
