@@ -1,5 +1,6 @@
 // gemm_kernels.cu -- instantiations and launch of the fused MC2 GEMM.
 #include <atomic>
+#include <chrono>
 #include "gemm_tcgen05.cuh"
 #include "internal.h"
 
@@ -41,6 +42,26 @@ int concurrent_pairs(int num_sms) {
     return clusters;
 }
 
+// Epochs of the stream-K flags: consecutive per launch from a per-process
+// starting point (clock and address mixed), in [2^20, 2^40), far from the
+// small integers a fresh buffer may hold and from another process's epochs.
+unsigned long long sk_epoch_seed() {
+    static int anchor;
+    unsigned long long x = static_cast<unsigned long long>(
+                               std::chrono::steady_clock::now().time_since_epoch().count()) ^
+                           reinterpret_cast<uintptr_t>(&anchor);
+    x ^= x >> 33;
+    x *= 0xff51afd7ed558ccdull;
+    x ^= x >> 33;
+    return x;
+}
+
+unsigned long long next_sk_epoch() {
+    static std::atomic<unsigned long long> counter{sk_epoch_seed()};
+    constexpr unsigned long long kLo = 1ull << 20, kSpan = (1ull << 40) - (1ull << 20);
+    return kLo + counter.fetch_add(1, std::memory_order_relaxed) % kSpan;
+}
+
 template <int kG, bool kBF16, bool kIntPath, bool kRS = false>
 cudaError_t launch_one(const GemmParams &p_in, int num_sms, cudaStream_t stream) {
     using Cfg = TileCfg<kG, !kRS>;
@@ -62,6 +83,8 @@ cudaError_t launch_one(const GemmParams &p_in, int num_sms, cudaStream_t stream)
         p.status = cached_status;
     }
     const int num_tiles = ((p.m + Cfg::kTileM - 1) / Cfg::kTileM) * ((p.n + kBN - 1) / kBN);
+    // stream-K flags carry the launch's epoch, so they never need zeroing
+    p.sk_epoch = next_sk_epoch();
 
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[2];
@@ -81,10 +104,11 @@ cudaError_t launch_one(const GemmParams &p_in, int num_sms, cudaStream_t stream)
         attr[1].val.clusterDim.z = 1;
         cfg.numAttrs = 2;
         const int clusters = concurrent_pairs<kBF16, kIntPath, kRS>(num_sms);
-        const int grid_clusters = num_tiles >= clusters ? clusters : num_tiles;
+        // with a stream-K tail every co-resident pair takes part
+        const int grid_clusters = (p.sk_tiles > 0 || num_tiles >= clusters) ? clusters : num_tiles;
         cfg.gridDim = dim3(2 * grid_clusters, 1, 1);
     } else {
-        const int units = num_tiles < num_sms ? num_tiles : num_sms;
+        const int units = p.sk_tiles > 0 ? num_sms : (num_tiles < num_sms ? num_tiles : num_sms);
         cfg.gridDim = dim3(units, 1, 1);
     }
     e = cudaLaunchKernelEx(&cfg, kern, p);
@@ -95,6 +119,17 @@ cudaError_t launch_one(const GemmParams &p_in, int num_sms, cudaStream_t stream)
 }  // namespace
 
 int gemm_group_for(int m) { return m > kBM ? 2 : 1; }
+
+int gemm_units(GemmKind kind, int group, int num_sms) {
+    if (group == 1) return num_sms;
+    switch (kind) {
+        case GEMM_F16: return concurrent_pairs<false, false>(num_sms);
+        case GEMM_BF16: return concurrent_pairs<true, false>(num_sms);
+        case GEMM_RS_F16: return concurrent_pairs<false, false, true>(num_sms);
+        case GEMM_RS_BF16: return concurrent_pairs<true, false, true>(num_sms);
+        default: return concurrent_pairs<false, true>(num_sms);
+    }
+}
 
 cudaError_t launch_gemm(GemmKind kind, int group, const GemmParams &p, int num_sms, cudaStream_t stream) {
     if (group == 2) {

@@ -112,6 +112,12 @@ struct GemmParams {
     const void *bias_q;             // integer path: (n) fp32 or bf16 (required), 16-byte aligned
     int bias_q_bf16;
     int32_t *acc_out;               // integer path: optional (m, n)
+    int sk_tiles;                   // integer path: tiles of the stream-K tail (0: whole tiles only)
+    int32_t *sk_partials;           // stream-K partial int32 sums: slot (unit * 2 + cta) of 128 x 256,
+                                    // lane-contiguous (see the epilogue)
+    unsigned long long *sk_flags;   // stream-K, per (tile, cta): (epoch << 24) | parts published; any
+                                    // value at launch (a stale epoch counts as none)
+    unsigned long long sk_epoch;    // this launch's epoch: unique per launch, in [2^20, 2^40)
     int *status;                    // device word set to -7 when a bounded wait gives up
     uint64_t wait_limit_ns;
     // reduce-scatter instantiation only (kRS): B is rank r's weight shard for the
@@ -123,26 +129,79 @@ struct GemmParams {
 };
 
 // ---------------------------------------------------------------------------
-// Work schedule of one cluster (identical in every role of every CTA of it):
-// cluster c takes tiles c, c + U, c + 2U, ... whole (U clusters in the grid),
-// each over all its K blocks.
+// Work schedule of one cluster (identical in every role of every CTA of it).
+// Tiles [0, num_tiles - sk_tiles) are data-parallel: cluster c takes tiles
+// c, c + U, ... whole.  The K blocks of the last sk_tiles tiles are laid end to
+// end and cut into U equal ranges, one per cluster; a range shorter than a
+// tile covers at most two parts: the end of one tile and the start of the next.
+// A part that does not end at its tile's end is a WRITE part (its int32 sums
+// go to the cluster's partial slot); a part that ends there but starts inside
+// the tile is a FINISH part (it adds the WRITE parts of the earlier clusters);
+// WRITE parts are scheduled first, so a FINISH part never waits on a cluster
+// that is itself waiting.
+enum WorkKind : int { WORK_FULL = 0, WORK_WRITE = 1, WORK_FINISH = 2 };
+
 struct Work {
-    int tile, kb0, kb1;
+    int tile, kb0, kb1, kind;
 };
 
 struct Schedule {
-    int c, U, nkb, n;
+    int c, U, nkb, dp_tiles, n_dp, n_sk;
+    long long total;  // K blocks in the stream-K region
+    Work sk[2];
 
-    __device__ __forceinline__ void init(int cluster, int units, int num_tiles, int nkb_) {
+    __device__ __forceinline__ long long range_start(int u) const { return static_cast<long long>(u) * total / U; }
+
+    __device__ __forceinline__ void init(int cluster, int units, int num_tiles, int sk_tiles, int nkb_) {
         c = cluster;
         U = units;
         nkb = nkb_;
-        n = c < num_tiles ? (num_tiles - c + U - 1) / U : 0;
+        dp_tiles = num_tiles - sk_tiles;
+        n_dp = c < dp_tiles ? (dp_tiles - c + U - 1) / U : 0;
+        total = static_cast<long long>(sk_tiles) * nkb;
+        n_sk = 0;
+        if (sk_tiles == 0) return;
+        const long long s0 = range_start(c), e0 = range_start(c + 1);
+        if (s0 == e0) return;
+        const int t0 = static_cast<int>(s0 / nkb);
+        const int kb0 = static_cast<int>(s0 - static_cast<long long>(t0) * nkb);
+        const int kb1 = static_cast<int>(min(static_cast<long long>(nkb), kb0 + (e0 - s0)));
+        Work a{dp_tiles + t0, kb0, kb1, kb1 < nkb ? WORK_WRITE : (kb0 > 0 ? WORK_FINISH : WORK_FULL)};
+        if (e0 > static_cast<long long>(t0 + 1) * nkb) {
+            // the range continues into the next tile: that start part is a WRITE part, done first
+            Work b{dp_tiles + t0 + 1, 0, static_cast<int>(e0 - static_cast<long long>(t0 + 1) * nkb), WORK_WRITE};
+            sk[0] = b;
+            sk[1] = a;
+            n_sk = 2;
+        } else {
+            sk[0] = a;
+            n_sk = 1;
+        }
     }
 
-    __device__ __forceinline__ int count() const { return n; }
+    __device__ __forceinline__ int count() const { return n_dp + n_sk; }
 
-    __device__ __forceinline__ Work get(int i) const { return Work{c + i * U, 0, nkb}; }
+    __device__ __forceinline__ Work get(int i) const {
+        if (i < n_dp) return Work{c + i * U, 0, nkb, WORK_FULL};
+        return sk[i - n_dp];
+    }
+
+    // Clusters u < c whose non-empty range reaches into `tile` (the WRITE parts a
+    // FINISH part of that tile adds), visited in descending u.
+    template <class F>
+    __device__ __forceinline__ int for_each_writer(int tile, F f) const {
+        const long long g0 = static_cast<long long>(tile - dp_tiles) * nkb;
+        int n = 0;
+        for (int u = c - 1; u >= 0; --u) {
+            const long long su = range_start(u), eu = range_start(u + 1);
+            if (eu <= g0) break;
+            if (su < eu) {
+                f(u);
+                ++n;
+            }
+        }
+        return n;
+    }
 };
 
 // Raster order of the tiles: groups of gm m-tiles, each walked m-fastest
@@ -161,6 +220,21 @@ __device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int 
     const int r = tile - g * span;
     mb = first_m + r % gsz;
     nb = r / gsz;
+}
+
+// Stream-K publication: one more part of this launch (epoch) written for the
+// (tile, cta) flag.  The first publisher of a launch replaces whatever an
+// earlier launch left; the CAS loop only retries while other publishers of
+// the same flag win, so its bound is never reached in practice.
+__device__ __forceinline__ bool sk_publish(unsigned long long *flag, unsigned long long epoch) {
+    unsigned long long cur = *reinterpret_cast<volatile unsigned long long *>(flag);
+    for (int it = 0; it < (1 << 20); ++it) {
+        const unsigned long long want = (cur >> 24) == epoch ? cur + 1 : ((epoch << 24) | 1ull);
+        const unsigned long long prev = atomicCAS(flag, cur, want);
+        if (prev == cur) return true;
+        cur = prev;
+    }
+    return false;
 }
 
 // Slow path of a barrier wait: poll with a wall-clock limit and the CTA's
@@ -259,7 +333,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
     const int num_clusters = gridDim.x / kG;
     const int nkb = (num_k + p.kblock_tiles - 1) / p.kblock_tiles;  // K blocks per tile
     Schedule sched;
-    sched.init(cluster_id, num_clusters, num_tiles, nkb);
+    sched.init(cluster_id, num_clusters, num_tiles, p.sk_tiles, nkb);
 
     if (threadIdx.x == 0) {
         abort_flag_s = 0;
@@ -600,6 +674,62 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
                 ++acc_iter;
             }
             if (!ok) break;
+            if constexpr (kIntPath) {
+                if (w.kind != WORK_FULL) {
+                    // stream-K: this thread's 128 int32 sums in slot (unit, cta), laid out
+                    // lane-contiguous (vector j of epilogue warp e, lane l at int4 index
+                    // (e * 32 + j) * 32 + l), so a warp's store or load is 512 contiguous bytes
+                    const size_t lane_off = static_cast<size_t>(warp - 4) * 32 * 32 + lane;
+                    if (w.kind == WORK_WRITE) {
+                        int4 *slot = reinterpret_cast<int4 *>(p.sk_partials +
+                                                              static_cast<size_t>(cluster_id * 2 + cr) * kBM * kBN) +
+                                     lane_off;
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            __stcg(slot + j * 32, make_int4(sum[4 * j], sum[4 * j + 1], sum[4 * j + 2], sum[4 * j + 3]));
+                        __threadfence();
+                        __syncwarp();
+                        if (lane == 0 && !sk_publish(p.sk_flags + w.tile * 2 + cr, p.sk_epoch)) {
+                            *abort_flag = 1;
+                            if (p.status) atomicExch(p.status, -7);
+                        }
+                        continue;
+                    }
+                    // FINISH: wait until every epilogue warp of every earlier part has published
+                    const unsigned long long want =
+                        (p.sk_epoch << 24) |
+                        static_cast<unsigned long long>(kNumEpiWarps * sched.for_each_writer(w.tile, [](int) {}));
+                    volatile unsigned long long *flag = p.sk_flags + w.tile * 2 + cr;
+                    if (*flag != want) {
+                        const uint64_t start = ptx::globaltimer_ns();
+                        while (*flag != want) {
+                            if (*abort_flag || ptx::globaltimer_ns() - start > p.wait_limit_ns) {
+                                *abort_flag = 1;
+                                if (p.status) atomicExch(p.status, -7);
+                                ok = false;
+                                break;
+                            }
+                            ptx::nanosleep(64);
+                        }
+                    }
+                    if (!ok) break;
+                    __threadfence();
+                    // the earlier parts' sums (exact int32: the order does not matter)
+                    sched.for_each_writer(w.tile, [&](int u) {
+                        const int4 *slot =
+                            reinterpret_cast<const int4 *>(p.sk_partials + static_cast<size_t>(u * 2 + cr) * kBM * kBN) +
+                            lane_off;
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            const int4 v = __ldcg(slot + j * 32);
+                            sum[4 * j] += v.x;
+                            sum[4 * j + 1] += v.y;
+                            sum[4 * j + 2] += v.z;
+                            sum[4 * j + 3] += v.w;
+                        }
+                    });
+                }
+            }
             const bool row_ok = row < p.m;
             if constexpr (kRS) {
                 if (!row_ok) continue;   // no warp-wide steps below on this path

@@ -21,6 +21,11 @@ struct GemmParams;
 enum GemmKind : int { GEMM_F16 = 0, GEMM_BF16 = 1, GEMM_INT_AS_F16 = 2, GEMM_RS_F16 = 3, GEMM_RS_BF16 = 4 };
 // group: 1 = one CTA per 128 x 256 tile, 2 = a CTA pair per 256 x 256 tile.
 int gemm_group_for(int m);
+// Work units (CTAs for group 1, CTA pairs for group 2) co-resident on the device;
+// the persistent grid launches this many when a stream-K tail is used.
+int gemm_units(GemmKind kind, int group, int num_sms);
+// Stream-K partial slots reserved in the workspace: at most this many work units.
+constexpr int kSkMaxUnits = 76;
 cudaError_t launch_gemm(GemmKind kind, int group, const GemmParams &p, int num_sms, cudaStream_t stream);
 int read_and_clear_gemm_status(int *status);
 // Device address of the status word that bounded waits set to -7 (cached per device).

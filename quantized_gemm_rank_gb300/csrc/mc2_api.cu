@@ -119,17 +119,31 @@ constexpr int kKBlockTiles = 1024 / mc2::kBK;      // k-tiles per exact fp32 K b
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 struct A2AWorkspace {
-    size_t x2h = 0, ah = 0, scale = 0, total = 0;
+    size_t x2h = 0, ah = 0, scale = 0, sk_partials = 0, sk_flags = 0, total = 0;
+    int num_tiles = 0, nkb = 0, sk_slots = 0;
 };
 
-// Workspace: x2 widened (K, N) fp16 | activations as fp16 (BS/R, K) | scales.
+// Workspace: x2 widened (K, N) fp16 | activations as fp16 (BS/R, K) | scales |
+// stream-K partial slots (2 x 128 x 256 int32 each) | stream-K flags (2 per tile,
+// 8 bytes each, never zeroed: they carry the launch's epoch).
 A2AWorkspace a2a_layout(int rank_size, int64_t bs_local, int64_t h, int64_t n) {
     A2AWorkspace w;
     const size_t K = static_cast<size_t>(rank_size) * static_cast<size_t>(h);
+    const int group = mc2::gemm_group_for(static_cast<int>(bs_local));
+    const int64_t tile_m = static_cast<int64_t>(mc2::kBM) * group;
+    w.num_tiles = static_cast<int>(((bs_local + tile_m - 1) / tile_m) * ((n + mc2::kBN - 1) / mc2::kBN));
+    const int64_t num_k = (static_cast<int64_t>(K) + mc2::kBK - 1) / mc2::kBK;
+    w.nkb = static_cast<int>((num_k + kKBlockTiles - 1) / kKBlockTiles);
+    const int64_t blocks = static_cast<int64_t>(w.num_tiles) * w.nkb;
+    // a writer uses the slot of its work unit, so a tail needs one slot per unit
+    // (kSkMaxUnits on GB300); problems with fewer K blocks than that reserve none
+    w.sk_slots = blocks >= mc2::kSkMaxUnits ? mc2::kSkMaxUnits : 0;
     w.x2h = 0;
     w.ah = align_up(w.x2h + K * static_cast<size_t>(n) * 2, 256);
     w.scale = align_up(w.ah + static_cast<size_t>(bs_local) * K * 2, 256);
-    w.total = align_up(w.scale + static_cast<size_t>(bs_local) * 4, 256);
+    w.sk_partials = align_up(w.scale + static_cast<size_t>(bs_local) * 4, 256);
+    w.sk_flags = align_up(w.sk_partials + static_cast<size_t>(w.sk_slots) * 2 * mc2::kBM * mc2::kBN * 4, 256);
+    w.total = align_up(w.sk_flags + static_cast<size_t>(w.num_tiles) * 2 * 8, 256);
     return w;
 }
 
@@ -473,7 +487,12 @@ int mc2_alltoall_quant_mm(const void *const *chunks, int rank_size, int64_t bs_l
     // GEMM reads the permuted matrix through one tensor map per chunk (a k-tile
     // never straddles two chunks); otherwise the widening writes it permuted.
     const bool a_by_chunk = x1_quant_mode == MC2_QUANT_PERTOKEN && h % mc2::kBK == 0;
+    // stream-K tail: the tiles left over after whole waves of the co-resident pairs
+    // (or CTAs) are split by K blocks over all of them (needs >= 2 K blocks a tile)
     const int group = mc2::gemm_group_for(static_cast<int>(bs_local));
+    const int units = mc2::gemm_units(mc2::GEMM_INT_AS_F16, group, dev.num_sms);
+    int sk_tiles = 0;
+    if (ws.nkb >= 2 && units <= ws.sk_slots && ws.num_tiles % units != 0) sk_tiles = ws.num_tiles % units;
     cudaError_t e = cudaSuccess;
     bool x2_done = false;
     if (x1_quant_mode == MC2_QUANT_PERTOKEN_DYNAMIC && mc2::a2a_prologue_fits(rank_size, bs_local, static_cast<int>(h))) {
@@ -529,6 +548,9 @@ int mc2_alltoall_quant_mm(const void *const *chunks, int rank_size, int64_t bs_l
     p.bias_q = bias;
     p.bias_q_bf16 = bias_dtype == MC2_BF16;
     p.acc_out = acc_out;
+    p.sk_tiles = sk_tiles;
+    p.sk_partials = reinterpret_cast<int32_t *>(wsb + ws.sk_partials);
+    p.sk_flags = reinterpret_cast<unsigned long long *>(wsb + ws.sk_flags);
     p.wait_limit_ns = kWaitLimitNs;
     e = mc2::launch_gemm(mc2::GEMM_INT_AS_F16, group, p, dev.num_sms, s);
     if (e != cudaSuccess) return fail(MC2_ERR_CUDA, "GEMM launch: %s", cudaGetErrorString(e));

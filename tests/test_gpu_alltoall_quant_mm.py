@@ -221,9 +221,10 @@ def test_quant_ties_and_near_ties_on_gpu():
 
 @pytest.mark.parametrize("n,mode", [(2560, 3), (4352, 7), (4352, 3)])
 def test_partial_last_wave_exact(n, mode):
-    """Shapes whose tile count is not a multiple of the co-resident CTA pairs
-    (a partial last wave), four K blocks of exact int32 sums per tile: every
-    output element bit for bit."""
+    """Shapes whose tile count is not a multiple of the co-resident CTA pairs:
+    the last partial wave's tiles are split by K blocks across all pairs
+    (stream-K) and their int32 partial sums combined; every output element bit
+    for bit."""
     shape = A2A(rank_size=8, bs_local=2048, h=512, n=n, quant_mode=mode)   # 8 x (n/256) tiles, 4 K blocks each
     inp = mc2_inputs.a2a_inputs(shape, seed=31)
     got = run_gpu(inp, shape)
@@ -232,8 +233,9 @@ def test_partial_last_wave_exact(n, mode):
 
 
 def test_all_127_bound_over_k_blocks():
-    """All-127 operands over eight K blocks: the exact int32 block sums reach
-    the accumulator bound (8192 * 16129 = 132128768)."""
+    """All-127 operands over eight K blocks, through the stream-K tail: the
+    exact int32 partials reach the accumulator bound (8192 * 16129 =
+    132128768)."""
     shape = A2A(rank_size=8, bs_local=2048, h=1024, n=2560, quant_mode=3)
     inp = mc2_inputs.a2a_inputs(shape, seed=2)
     inp["chunks"] = [torch.full_like(c, -127) for c in inp["chunks"]]
