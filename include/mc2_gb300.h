@@ -224,7 +224,10 @@ int mc2_alltoall_quant_mm_workspace(int rank_size, int64_t bs_local, int64_t h, 
  *   q_out           NULL or int8 (bs_local, rank_size*h): the quantised activations (mode 7)
  *   x1_scale_out    NULL or fp32 (bs_local): the per-token scales (mode 7)
  *   acc_out         NULL or int32 (bs_local, n): the exact accumulators (debug)
- *   workspace       device scratch of at least the bytes the query returns
+ *   workspace       device scratch of at least the bytes the query returns, 16-byte
+ *                   aligned; it needs no initialisation (the stream-K flags in it
+ *                   carry a per-launch epoch) and may be reused by calls ordered
+ *                   on one stream; concurrent calls need their own
  *
  * Returns MC2_OK or a negative mc2_status; nothing is launched on error.
  */
