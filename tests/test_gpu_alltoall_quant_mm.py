@@ -264,3 +264,34 @@ def test_largest_rank_h(name):
     got = run_gpu(inp, shape)
     ref = run_oracle(inp, shape)
     compare(got, ref, name)
+
+
+def test_stream_k_workspace_needs_no_zeroing():
+    """The stream-K flags in the workspace carry a per-launch epoch: a workspace
+    full of arbitrary bytes, or holding the flags an earlier launch left, gives
+    the same exact result (136 tiles: the 60 after one whole wave are split by
+    K blocks over the 76 pairs)."""
+    shape = A2A(rank_size=8, bs_local=2048, h=512, n=4352, quant_mode=7)
+    inp = mc2_inputs.a2a_inputs(shape, seed=33)
+    dev = torch.device("cuda")
+    chunks = [c.to(dev) for c in inp["chunks"]]
+    args = (chunks, inp["x2"].to(dev), inp["x2_scale"].to(dev), inp["bias"].to(dev))
+    nbytes = mc2.mc2_alltoall_quant_mm_workspace(shape.rank_size, shape.bs_local, shape.h, shape.n, 7,
+                                                 chunks[0].dtype)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    rows = mc2_inputs.sample_rows(shape.bs_local, 64, seed=5)
+    ref = run_oracle(inp, shape, rows=rows)
+    outs = []
+    for fill in (0x00, 0xA5, 0xFF, None, None):   # None: the previous launch's flags stay
+        if fill is not None:
+            ws.fill_(fill)
+        acc = torch.empty((shape.bs_local, shape.n), dtype=torch.int32, device=dev)
+        res = mc2.mc2_alltoall_quant_mm(*args, x1_quant_mode=7, x1_scale=inp["x1_scale"].to(dev), acc_out=acc,
+                                        workspace=ws)
+        torch.cuda.synchronize()
+        assert mc2.mc2_device_status() == mc2.MC2_OK
+        assert_bits_equal(acc.cpu()[rows], ref["acc"], f"fill {fill}: acc")
+        assert_bits_equal(res["out"].cpu()[rows], ref["out"], f"fill {fill}: out")
+        outs.append(res["out"].cpu())
+    for o in outs[1:]:
+        assert_bits_equal(o, outs[0], "every launch identical")
