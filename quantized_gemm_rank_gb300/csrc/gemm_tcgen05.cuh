@@ -205,14 +205,20 @@ struct Schedule {
 };
 
 // Raster order of the tiles: groups of gm m-tiles, each walked m-fastest
-// across all n-tiles.  gm is 8 in general; with at most 16 n-tiles (n <= 4096)
-// it is 2, which measured 1-4% faster on each such all-gather shape tried
-// (m 8192-16384, k 4096-8192) and no different on the integer path, while on
-// 28-32 n-tiles a group of 8 measured 2-5% faster than 2.
-__device__ __forceinline__ int raster_group(int num_n) { return num_n <= 16 ? kGroupMNarrow : kGroupM; }
+// across all n-tiles.  gm is 8 in general.  On the float path with at most 16
+// n-tiles (n <= 4096) it is 2, which measured 1-4% faster on each such
+// all-gather shape tried (m 8192-16384, k 4096-8192), while on 28-32 n-tiles
+// a group of 8 measured 2-5% faster than 2.  The integer path keeps 8 as a
+// compile-time constant, which measured 1-2% faster there than either rule.
+template <bool kIntPath>
+__device__ __forceinline__ int raster_group(int num_n) {
+    if constexpr (kIntPath) return kGroupM;
+    return num_n <= 16 ? kGroupMNarrow : kGroupM;
+}
 
+template <bool kIntPath>
 __device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int &mb, int &nb) {
-    const int gm = raster_group(num_n);
+    const int gm = raster_group<kIntPath>(num_n);
     const int span = gm * num_n;
     const int g = tile / span;
     const int first_m = g * gm;
@@ -467,7 +473,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
             const Work w = sched.get(wi);
             const int kt_begin = w.kb0 * p.kblock_tiles, kt_end = min(num_k, w.kb1 * p.kblock_tiles);
             int mb, nb;
-            tile_coords(w.tile, num_m, num_n, mb, nb);
+            tile_coords<kIntPath>(w.tile, num_m, num_n, mb, nb);
             const int m0 = mb * Cfg::kTileM + kBM * static_cast<int>(cr);
             const int n0 = nb * kBN + Cfg::kBRows * static_cast<int>(cr);
             // first A box of this tile: chunk and row inside it (rows past m stay in the
@@ -543,7 +549,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
             const Work w = sched.get(wi);
             const int kt_begin = w.kb0 * kblock, kt_end = min(num_k, w.kb1 * kblock);
             int mb, nb;
-            tile_coords(w.tile, num_m, num_n, mb, nb);
+            tile_coords<kIntPath>(w.tile, num_m, num_n, mb, nb);
             // stages of gathered tiles go to the gathered-store warp before being freed
             const uint32_t release0 = (p.gather && nb == 0) ? consumed0 : empty0;
             int kin = 0;  // k-tile index inside the current K block
@@ -596,7 +602,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
             const Work w = sched.get(wi);
             const int kt_begin = w.kb0 * p.kblock_tiles, kt_end = min(num_k, w.kb1 * p.kblock_tiles);
             int mb, nb;
-            tile_coords(w.tile, num_m, num_n, mb, nb);
+            tile_coords<kIntPath>(w.tile, num_m, num_n, mb, nb);
             if (nb != 0) {  // not a gathered tile: its stages are freed by the MMA directly
                 stage = (stage + (kt_end - kt_begin)) % S;
                 continue;
@@ -631,7 +637,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
         for (int wi = 0; wi < sched.count(); ++wi) {
             const Work w = sched.get(wi);
             int mb, nb;
-            tile_coords(w.tile, num_m, num_n, mb, nb);
+            tile_coords<kIntPath>(w.tile, num_m, num_n, mb, nb);
             const int row = mb * Cfg::kTileM + kBM * static_cast<int>(cr) + 32 * q + lane;
             const int colh = nb * kBN + half * 128;
             bool ok = true;
