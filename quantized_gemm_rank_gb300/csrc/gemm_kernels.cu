@@ -14,7 +14,7 @@ namespace {
 // occupancy calculator (cached per device).
 template <bool kBF16, bool kIntPath, bool kRS = false>
 int concurrent_pairs(int num_sms) {
-    using Cfg = TileCfg<2, !kRS>;
+    using Cfg = TileCfg<2, true>;
     static std::atomic<int> cached[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return num_sms / 2;
@@ -64,7 +64,7 @@ unsigned long long next_sk_epoch() {
 
 template <int kG, bool kBF16, bool kIntPath, bool kRS = false>
 cudaError_t launch_one(const GemmParams &p_in, int num_sms, cudaStream_t stream) {
-    using Cfg = TileCfg<kG, !kRS>;
+    using Cfg = TileCfg<kG, true>;
     auto kern = mc2_gemm_kernel<kG, kBF16, kIntPath, kRS>;
     GemmParams p = p_in;
     // per device, once: the status word's address and the shared-memory opt-in

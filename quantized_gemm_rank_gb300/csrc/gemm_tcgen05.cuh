@@ -71,9 +71,8 @@ constexpr int kGroupMNarrow = 2;                 // ... and when the output is a
 constexpr uint32_t kEpiSlabBytes = 32 * 128;
 constexpr uint32_t kEpiStageBytes = kNumEpiWarps * kEpiSlabBytes;
 
-// kTmaOut: the epilogue stores through shared staging slabs (the float path);
-// only then is the staging area reserved, leaving the rest of the SM's
-// shared/L1 space to the L1 cache that the integer epilogue's loads use.
+// kTmaOut: reserve the epilogue's shared staging slabs (8 x 4 KiB) after the
+// stage ring; every instantiation of the GEMM stores its outputs through them.
 template <int kG, bool kTmaOut = false>
 struct TileCfg {
     static constexpr int kTileM = kBM * kG;               // rows per tile
@@ -126,6 +125,10 @@ struct GemmParams {
     CUtensorMap b_rank_maps[kMaxAMaps];
     void *out_chunks[kMaxAMaps];
     int out_rows;
+    // rank r's output (out_rows, n) 16-bit, box 64 columns x 32 rows, 128-byte
+    // swizzle; used when rs_tma (out_rows % 32 == 0: a warp's 32 rows are one rank's)
+    CUtensorMap out_rank_maps[kMaxAMaps];
+    int rs_tma;
 };
 
 // ---------------------------------------------------------------------------
@@ -309,7 +312,7 @@ __device__ __forceinline__ void store_row32_16(uint16_t *row_ptr, int n, int col
 
 template <int kG, bool kBF16, bool kIntPath, bool kRS = false>
 __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_constant__ GemmParams p) {
-    constexpr bool kTmaOut = !kRS;  // epilogue stores through shared slabs and TMA
+    constexpr bool kTmaOut = true;  // epilogue stores through shared slabs and TMA (see the epilogue)
     using Cfg = TileCfg<kG, kTmaOut>;
     constexpr bool kPair = kG == 2;
     constexpr int S = Cfg::kStages;
@@ -737,25 +740,32 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
                 }
             }
             const bool row_ok = row < p.m;
-            if constexpr (kRS) {
-                if (!row_ok) continue;   // no warp-wide steps below on this path
-            }
+            // the reduce-scatter with out_rows % 32 != 0 writes rows straight from
+            // registers (a warp's rows may belong to two ranks)
+            const bool rs_direct = kRS && !p.rs_tma;
+            if (rs_direct && !row_ok) continue;   // no warp-wide steps below in that mode
             // This warp's 32 rows x 128 columns leave as two 64-column slabs:
             // rounded 16-bit values go to its shared staging slab (128-byte rows,
             // chunk j of row r at ((j ^ (r % 8)) * 16)), then one TMA store per
             // slab; rows and columns past the output are clipped by the TMA unit.
-            // The reduce-scatter writes rows straight to the ranks' outputs.
+            // The reduce-scatter stores through the map of the rank that owns the
+            // warp's rows, at the rows' place in that rank's output.
             uint8_t *slab = reinterpret_cast<uint8_t *>(epi_stage) + (warp - 4) * kEpiSlabBytes;
             const int slab_row0 = mb * Cfg::kTileM + kBM * static_cast<int>(cr) + 32 * q;
+            const CUtensorMap *omap = &p.out_map;
+            int orow0 = slab_row0;
+            bool ostore = true;
+            if constexpr (kRS) {
+                const int rank = min(slab_row0 / p.out_rows, p.num_a_maps - 1);
+                omap = &p.out_rank_maps[rank];
+                orow0 = slab_row0 - rank * p.out_rows;
+                ostore = slab_row0 < p.m;   // warp-uniform: out_rows % 32 == 0 in this mode
+            }
             auto put = [&](int c, const uint32_t (&pk)[16]) {
-                if constexpr (kRS) {
+                if (rs_direct) {
                     uint16_t *orow = reinterpret_cast<uint16_t *>(p.out_chunks[row / p.out_rows]) +
                                      static_cast<int64_t>(row % p.out_rows) * p.n;
                     store_row32_16(orow, p.n, colh + c * 32, pk);
-                } else if constexpr (!kTmaOut) {
-                    if (row_ok && colh + c * 32 < p.n)
-                        store_row32_16(reinterpret_cast<uint16_t *>(p.out) + static_cast<int64_t>(row) * p.n, p.n,
-                                       colh + c * 32, pk);
                 } else {
                     if ((c & 1) == 0) {
                         // the slab's previous store has finished reading it
@@ -772,8 +782,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
                         ptx::fence_proxy_async_smem();
                         __syncwarp();
                         const int scol = colh + (c >> 1) * 64;
-                        if (lane == 0 && scol < p.n) {
-                            ptx::tma_store_2d(&p.out_map, scol, slab_row0, ptx::smem_u32(slab));
+                        if (lane == 0 && ostore && scol < p.n) {
+                            ptx::tma_store_2d(omap, scol, orow0, ptx::smem_u32(slab));
                             ptx::bulk_commit_group();
                         }
                     }
@@ -783,7 +793,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     const int col0 = colh + c * 32;
-                    if (kRS && col0 >= p.n) continue;
+                    if (rs_direct && col0 >= p.n) continue;
                     float v[32];
 #pragma unroll
                     for (int i = 0; i < 32; ++i) v[i] = sum[c * 32 + i];

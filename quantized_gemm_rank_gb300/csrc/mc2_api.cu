@@ -331,6 +331,15 @@ int mc2_matmul_reduce_scatter(const void *const *x_chunks, const void *const *w_
     p.k_local = static_cast<int>(k_local);
     p.b_mn_major = w_is_nk ? 0 : 1;
     p.out_rows = static_cast<int>(m / world_size);
+    // a warp's 32 output rows belong to one rank when out_rows % 32 == 0: the
+    // epilogue then stores through one tensor map per rank's output
+    if (p.out_rows % 32 == 0) {
+        for (int r = 0; r < world_size; ++r)
+            if (!make_map16(&p.out_rank_maps[r], out_chunks[r], static_cast<uint64_t>(n),
+                            static_cast<uint64_t>(p.out_rows), 64, 32))
+                return fail(MC2_ERR_CUDA, "cuTensorMapEncodeTiled failed for out_chunks[%d]", r);
+        p.rs_tma = 1;
+    }
     p.m = static_cast<int>(m);
     p.n = static_cast<int>(n);
     p.k = static_cast<int>(k_local * world_size);
