@@ -50,7 +50,7 @@ FLUSH_BYTES = 512 << 20
 # (GEMM_SOURCES) the capture was taken with: the figure is reported only
 # while they match.
 AG_GEMM_TRAFFIC = 272.30e6          # dram__bytes_read.sum 159.53 MB + dram__bytes_write.sum 112.77 MB
-AG_GEMM_TRAFFIC_SRC_HASH = "55531a2342388564"
+AG_GEMM_TRAFFIC_SRC_HASH = "473c18471fd6cec7"
 
 
 def parse_args():

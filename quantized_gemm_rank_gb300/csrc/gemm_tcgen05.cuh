@@ -65,7 +65,8 @@ constexpr int kNumThreads = 128 + kNumEpiWarps * 32;
 constexpr uint32_t kATileBytes = kBM * kBK * 2;  // 16 KiB
 constexpr uint32_t kTmemCols = 512;              // two 256-column fp32 accumulators
 constexpr int kGroupM = 8;                       // m-tiles per raster group (L2 reuse of B) ...
-constexpr int kGroupMNarrow = 2;                 // ... and when the output is at most 16 tiles wide
+constexpr int kGroupMNarrow = 2;                 // ... and on the float path when the output is at
+                                                 // most 16 tiles wide
 // Output staging for the TMA-store epilogue: per epilogue warp one 32-row x
 // 64-column 16-bit slab (128-byte rows, 128-byte swizzle).
 constexpr uint32_t kEpiSlabBytes = 32 * 128;
