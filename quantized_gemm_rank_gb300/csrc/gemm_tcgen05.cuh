@@ -118,6 +118,8 @@ struct GemmParams {
     unsigned long long *sk_flags;   // stream-K, per (tile, cta): (epoch << 24) | parts published; any
                                     // value at launch (a stale epoch counts as none)
     unsigned long long sk_epoch;    // this launch's epoch: unique per launch, in [2^20, 2^40)
+    int sk_extra_writers;           // test hook: WRITE parts a FINISH part expects beyond the real ones
+                                    // (0 in normal use; > 0 makes every FINISH wait run out)
     int *status;                    // device word set to -7 when a bounded wait gives up
     uint64_t wait_limit_ns;
     // reduce-scatter instantiation only (kRS): B is rank r's weight shard for the
@@ -326,6 +328,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
     uint64_t *tfull_bar = bars + 3 * S;       // accumulator buffer ready
     uint64_t *tempty_bar = bars + 3 * S + 2;  // accumulator buffer drained (the leader's counts both CTAs)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 3 * S + 4);
+    uint64_t *drain_bar = bars + 3 * S + 5;   // every MMA this CTA issued has completed
     // the epilogue's output slabs, after the 1 KiB barrier area (1024-byte aligned)
     uint8_t *epi_stage = smem + S * Cfg::kStageBytes + 1024;
     __shared__ int abort_flag_s;
@@ -356,6 +359,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
             ptx::mbar_init(ptx::smem_u32(&tfull_bar[b]), 1);
             ptx::mbar_init(ptx::smem_u32(&tempty_bar[b]), kNumEpiWarps * kG);
         }
+        ptx::mbar_init(ptx::smem_u32(drain_bar), 1);
         ptx::fence_mbar_init();
     }
     if (warp == 1) {
@@ -595,6 +599,16 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
                 }
             }
         }
+        // Drain: whether the loop ended or gave up, wait (bounded) until every MMA
+        // issued above has completed, so that no MMA can still write TMEM (in
+        // either CTA of a pair) when the CTAs pass the final barrier and free it.
+        // On the normal path they have all completed already (the epilogue waited
+        // for their accumulators) and this returns at once.
+        ptx::mma_commit_local<kG>(ptx::smem_u32(drain_bar));
+        if (!ptx::mbar_wait(ptx::smem_u32(drain_bar), 0u, p.wait_limit_ns)) {
+            *abort_flag = 1;
+            if (p.status) atomicExch(p.status, -7);
+        }
     } else if (warp == 2 && lane == 0 && p.gather) {
         // ------------------------------------------------------------ gathered store
         ptx::prefetch_tmap(&p.g_map);
@@ -653,7 +667,10 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
             for (int i = 0; i < 128; ++i) sum[i] = acc_t(0);
             for (int kb = w.kb0; kb < w.kb1; ++kb) {
                 const uint32_t b = acc_iter & 1u;
-                if (!wait_or_abort<kPair>(ptx::smem_u32(&tfull_bar[b]), (acc_iter >> 1) & 1u, p, abort_flag)) {
+                // every lane waits (bounded); the warp goes on only if all of them saw the
+                // buffer ready, so no lane reaches the warp-wide TMEM load alone
+                const bool got = wait_or_abort<kPair>(ptx::smem_u32(&tfull_bar[b]), (acc_iter >> 1) & 1u, p, abort_flag);
+                if (!__all_sync(0xffffffffu, got)) {
                     ok = false;
                     break;
                 }
@@ -705,24 +722,31 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
                         }
                         continue;
                     }
-                    // FINISH: wait until every epilogue warp of every earlier part has published
+                    // FINISH: wait until every epilogue warp of every earlier part has published.
+                    // Lane 0 polls (bounded) and tells the warp, so the warp decides as one.
+                    const int writers = sched.for_each_writer(w.tile, [](int) {}) + p.sk_extra_writers;
                     const unsigned long long want =
-                        (p.sk_epoch << 24) |
-                        static_cast<unsigned long long>(kNumEpiWarps * sched.for_each_writer(w.tile, [](int) {}));
-                    volatile unsigned long long *flag = p.sk_flags + w.tile * 2 + cr;
-                    if (*flag != want) {
-                        const uint64_t start = ptx::globaltimer_ns();
-                        while (*flag != want) {
-                            if (*abort_flag || ptx::globaltimer_ns() - start > p.wait_limit_ns) {
-                                *abort_flag = 1;
-                                if (p.status) atomicExch(p.status, -7);
-                                ok = false;
-                                break;
+                        (p.sk_epoch << 24) | static_cast<unsigned long long>(kNumEpiWarps * writers);
+                    int seen = 1;
+                    if (lane == 0) {
+                        volatile unsigned long long *flag = p.sk_flags + w.tile * 2 + cr;
+                        if (*flag != want) {
+                            const uint64_t start = ptx::globaltimer_ns();
+                            while (*flag != want) {
+                                if (*abort_flag || ptx::globaltimer_ns() - start > p.wait_limit_ns) {
+                                    *abort_flag = 1;
+                                    if (p.status) atomicExch(p.status, -7);
+                                    seen = 0;
+                                    break;
+                                }
+                                ptx::nanosleep(64);
                             }
-                            ptx::nanosleep(64);
                         }
                     }
-                    if (!ok) break;
+                    if (__shfl_sync(0xffffffffu, seen, 0) == 0) {
+                        ok = false;
+                        break;
+                    }
                     __threadfence();
                     // the earlier parts' sums (exact int32: the order does not matter)
                     sched.for_each_writer(w.tile, [&](int u) {

@@ -270,6 +270,19 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
             : "memory");
 }
 
+// Arrive on this CTA's own `bar` once all previously issued tcgen05 ops of
+// this thread complete (no multicast: with kG = 2 only the issuing CTA's
+// barrier receives the arrival).
+template <int kG>
+__device__ __forceinline__ void mma_commit_local(uint32_t bar) {
+    if constexpr (kG == 1)
+        asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                     : "memory");
+    else
+        asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                     : "memory");
+}
+
 // 32 lanes x 32 consecutive 32-bit columns: thread i gets lane (base + i).
 __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile(
