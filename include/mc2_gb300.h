@@ -20,7 +20,14 @@
  *   - Arguments are validated before anything is launched.  A violated
  *     constraint returns a negative mc2_status and launches nothing;
  *     mc2_last_error() then describes which argument failed (thread-local).
- *   - Outputs are deterministic: no atomics, no split-K.
+ *   - Outputs are deterministic: the same inputs give the same bits on every
+ *     call.  The float paths compute each output tile whole in one CTA pair.
+ *     The integer GEMM of mc2_alltoall_quant_mm splits the tiles of its last
+ *     partial wave by K blocks ("stream-K"): the parts that do not end a tile
+ *     write exact int32 partial sums to the workspace and publish them on
+ *     per-tile flags with atomic compare-and-swap, and the part that ends the
+ *     tile adds them.  Integer sums are exact in any order, so the result is
+ *     bit-identical to whole tiles.
  *   - Pointers must be 16-byte aligned and row pitches multiples of 16 bytes
  *     (the tensor-memory-accelerator copies need it); otherwise
  *     MC2_ERR_UNSUPPORTED.
@@ -255,8 +262,14 @@ int mc2_alltoall_quant_mm(const void *const *chunks, int rank_size, int64_t bs_l
  *     exceeds that are refused with MC2_ERR_WORKSPACE before anything is
  *     launched.
  *   - The call never calls cudaMalloc, cudaFree or any allocating routine.
- *   - The first call on each device looks up the scratch's device address,
- *     with that device current; make that first call before any stream capture.
+ *   - Every call looks up the scratch's device address on the current device
+ *     (a lookup, no allocation and no synchronisation), so a device reset
+ *     between calls is harmless.  With CUDA's lazy module loading (the default)
+ *     the library's device code, this array included, is loaded on a device
+ *     the first time it is used there: that first call (of this or any other
+ *     entry point) maps the 32 MiB.  A caller that must never see device
+ *     memory grow mid-run makes one warm-up call at start-up, and makes its
+ *     first call before any stream capture.
  *   - All calls share the one scratch array, and it keeps whatever the last
  *     call wrote (nothing in it needs to start at zero).  Calls whose work can
  *     overlap on the GPU (other streams, other host threads) race on it and
@@ -271,19 +284,6 @@ int mc2_alltoall_quant_mm_no_alloc(const void *const *chunks, int rank_size, int
                                    void *out, void *alltoall_out, int8_t *q_out, float *x1_scale_out,
                                    int32_t *acc_out, void *stream);
 
-/*
- * Calibration (not part of the operations): launches `blocks` CTAs of 256
- * threads on `stream`, each warp running `iters` rounds of 8 independent
- * legacy warp-level tensor-core MMAs (mma.sync) on register operands:
- * kind 0 = int8 x int8 -> int32 (m16n8k32), kind 1 = fp16 x fp16 -> fp32
- * (m16n8k16).  `sink` (device, blocks * 256 int32, caller-owned) receives one
- * word per thread so that the work stays live.  *ops receives the operations
- * (2 per multiply-add) one launch performs; time the launch with events on
- * `stream` for the rate.  Returns MC2_ERR_NULL / MC2_ERR_SHAPE on bad
- * arguments, MC2_ERR_CUDA if the launch fails.
- */
-int mc2_calib_mma_sync(int kind, int64_t iters, int blocks, int32_t *sink, void *stream, double *ops);
-
 /* Name of a status code (static string). */
 const char *mc2_status_str(int status);
 
@@ -297,6 +297,46 @@ const char *mc2_last_error(void);
  * and clears the flag.
  */
 int mc2_device_status(void);
+
+/*
+ * Measurement aid (not one of the operations): lets a caller time each kernel
+ * of a call on the call's own stream.  `events` is a host array of `count`
+ * cudaEvent_t handles (as void*) created by the caller; count 0 turns it off.
+ * While set, every call on this host thread records events[0] on its stream
+ * just before its first kernel launch and events[i] just after its i-th
+ * launch, for i < count (launches beyond count - 1 record nothing).  So
+ * cudaEventElapsedTime(events[i], events[i+1]) is the device time of launch i.
+ * The calls launch, in order:
+ *   mc2_all_gather_mm, mc2_matmul_reduce_scatter   1: the GEMM
+ *   mc2_matmul_weight_grad     2: the bias-gradient sums (only with db), the GEMM
+ *   mc2_quant_all_reduce       1: the reduction
+ *   mc2_alltoall_quant_mm      x1_quant_mode 7: 2 (the fused quant and x2
+ *                              widening, the GEMM), or 3 when rank_size*h > 32768
+ *                              or h % 8 != 0 (the quant, the x2 widening, the
+ *                              GEMM); x1_quant_mode 3: 3 (the activations'
+ *                              widening, the x2 widening, the GEMM)
+ * An event between two launches also keeps the second from starting early
+ * (programmatic dependent launch), which can add a few microseconds to a
+ * call.  The setting is per host thread and stays until changed; the caller
+ * keeps the events alive while it is set.
+ * Returns MC2_OK, MC2_ERR_SHAPE (count outside [0, 8]) or MC2_ERR_NULL.
+ */
+int mc2_set_launch_events(void *const *events, int count);
+
+/*
+ * Test hook for the bounded waits (not one of the operations).  Arms a fault
+ * for the next mc2_alltoall_quant_mm (or _no_alloc) call on this host thread
+ * only: in that call's GEMM, every stream-K finishing part expects one more
+ * partial sum than any part writes, so its wait on the tile's flag cannot
+ * succeed and gives up after `wait_limit_ns` (instead of the usual 2 s).  The
+ * kernel then skips those tiles' epilogues (their outputs are left as they
+ * were) and raises the device status word: mc2_device_status() afterwards
+ * returns MC2_ERR_TIMEOUT and clears it, and the device stays usable.  The
+ * hook is consumed by that one call even when its GEMM has no stream-K tail
+ * (then nothing waits and nothing is raised).
+ * Returns MC2_OK, or MC2_ERR_SHAPE if wait_limit_ns is 0 or above 2 s.
+ */
+int mc2_test_expire_next_flag_waits(uint64_t wait_limit_ns);
 
 #ifdef __cplusplus
 }

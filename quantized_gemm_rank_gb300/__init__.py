@@ -79,8 +79,10 @@ def lib() -> ctypes.CDLL:
         L.mc2_last_error.restype = ctypes.c_char_p
         L.mc2_device_status.argtypes = []
         L.mc2_device_status.restype = _INT
-        L.mc2_calib_mma_sync.argtypes = [_INT, _I64, _INT, _P, _P, ctypes.POINTER(ctypes.c_double)]
-        L.mc2_calib_mma_sync.restype = _INT
+        L.mc2_set_launch_events.argtypes = [_P, _INT]
+        L.mc2_set_launch_events.restype = _INT
+        L.mc2_test_expire_next_flag_waits.argtypes = [ctypes.c_uint64]
+        L.mc2_test_expire_next_flag_waits.restype = _INT
         _lib = L
     return _lib
 
@@ -307,15 +309,25 @@ def mc2_device_status() -> int:
     return int(lib().mc2_device_status())
 
 
-def mc2_calib_mma_sync(kind: int, iters: int, blocks: int, sink: torch.Tensor, stream=None) -> float:
-    """Launch the legacy mma.sync rate kernel (kind 0: int8 -> int32, 1: fp16 ->
-    fp32) on `stream`; returns the operations the launch performs.  `sink` is a
-    device int32 tensor of at least blocks * 256 elements."""
-    if sink.dtype != torch.int32 or sink.numel() < blocks * 256:
-        raise ValueError("sink must be a device int32 tensor of blocks * 256 elements")
-    ops = ctypes.c_double(0.0)
-    _check(lib().mc2_calib_mma_sync(kind, iters, blocks, _dev(sink, "sink"), _stream(stream), ctypes.byref(ops)))
-    return ops.value
+def mc2_set_launch_events(events: Optional[Sequence["torch.cuda.Event"]]) -> None:
+    """Record the given CUDA events around the kernel launches of the next calls
+    on this host thread: events[0] before a call's first launch, events[i]
+    after its i-th (see the header for each call's launches).  None or [] turns
+    it off.  The events must be created with timing enabled and stay alive
+    while set."""
+    evs = list(events or [])
+    handles = [e.cuda_event for e in evs]
+    if any(h == 0 for h in handles):
+        raise ValueError("record each event once (or create it) before installing it")
+    arr = (ctypes.c_void_p * max(1, len(handles)))(*handles) if handles else None
+    _check(lib().mc2_set_launch_events(arr, len(handles)))
+
+
+def mc2_test_expire_next_flag_waits(wait_limit_ns: int) -> None:
+    """Test hook: the next AlltoAllQuantMatmul call on this host thread runs its
+    GEMM with every stream-K finishing wait set to run out after
+    ``wait_limit_ns`` (see the header)."""
+    _check(lib().mc2_test_expire_next_flag_waits(int(wait_limit_ns)))
 
 
 __all__ = [
@@ -323,7 +335,7 @@ __all__ = [
     "mc2_matmul_reduce_scatter", "mc2_matmul_weight_grad", "mc2_quant_all_reduce",
     "mc2_alltoall_quant_mm_workspace", "mc2_alltoall_quant_mm",
     "mc2_alltoall_quant_mm_no_alloc",
-    "NO_ALLOC_SCRATCH_BYTES", "mc2_device_status", "mc2_calib_mma_sync",
+    "NO_ALLOC_SCRATCH_BYTES", "mc2_device_status", "mc2_set_launch_events", "mc2_test_expire_next_flag_waits",
     "MC2_OK", "MC2_ERR_NULL", "MC2_ERR_SHAPE", "MC2_ERR_DTYPE", "MC2_ERR_UNSUPPORTED", "MC2_ERR_WORKSPACE",
     "MC2_ERR_CUDA", "MC2_ERR_TIMEOUT", "MC2_F16", "MC2_BF16", "MC2_F32", "MC2_I8",
     "MC2_F8E4M3", "MC2_F8E5M2", "MC2_E8M0",

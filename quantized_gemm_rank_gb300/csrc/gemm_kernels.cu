@@ -8,6 +8,32 @@ namespace mc2 {
 
 __device__ int g_gemm_status = 0;
 
+unsigned long long current_context_id() {
+    using GetCurrentFn = CUresult (*)(CUcontext *);
+    using GetIdFn = CUresult (*)(CUcontext, unsigned long long *);
+    static std::atomic<GetCurrentFn> get_current{nullptr};
+    static std::atomic<GetIdFn> get_id{nullptr};
+    GetCurrentFn gc = get_current.load(std::memory_order_relaxed);
+    GetIdFn gi = get_id.load(std::memory_order_relaxed);
+    if (!gc || !gi) {
+        void *a = nullptr, *b = nullptr;
+        cudaDriverEntryPointQueryResult qa, qb;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &a, 12000, cudaEnableDefault, &qa) != cudaSuccess ||
+            qa != cudaDriverEntryPointSuccess ||
+            cudaGetDriverEntryPointByVersion("cuCtxGetId", &b, 12000, cudaEnableDefault, &qb) != cudaSuccess ||
+            qb != cudaDriverEntryPointSuccess)
+            return 0;
+        gc = reinterpret_cast<GetCurrentFn>(a);
+        gi = reinterpret_cast<GetIdFn>(b);
+        get_current.store(gc, std::memory_order_relaxed);
+        get_id.store(gi, std::memory_order_relaxed);
+    }
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (gc(&ctx) != CUDA_SUCCESS || ctx == nullptr || gi(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
+
 namespace {
 
 // CTA pairs of this instantiation that fit on the device at once, from the
@@ -67,21 +93,20 @@ cudaError_t launch_one(const GemmParams &p_in, int num_sms, cudaStream_t stream)
     using Cfg = TileCfg<kG, true>;
     auto kern = mc2_gemm_kernel<kG, kBF16, kIntPath, kRS>;
     GemmParams p = p_in;
-    // per device, once: the status word's address and the shared-memory opt-in
-    static std::atomic<int *> status_addr[64];
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    int *cached_status = dev < 64 ? status_addr[dev].load(std::memory_order_relaxed) : nullptr;
-    if (cached_status == nullptr) {
-        e = cudaGetSymbolAddress(reinterpret_cast<void **>(&p.status), g_gemm_status);
+    // once per host thread and context (a device switch or reset makes a new
+    // context): the status word's address and the shared-memory opt-in
+    thread_local unsigned long long ready_ctx = 0;
+    thread_local int *status_word = nullptr;
+    const unsigned long long ctx = current_context_id();
+    cudaError_t e = cudaSuccess;
+    if (ctx == 0 || ctx != ready_ctx) {
+        e = cudaGetSymbolAddress(reinterpret_cast<void **>(&status_word), g_gemm_status);
         if (e != cudaSuccess) return e;
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
         if (e != cudaSuccess) return e;
-        if (dev < 64) status_addr[dev].store(p.status, std::memory_order_relaxed);
-    } else {
-        p.status = cached_status;
+        ready_ctx = ctx;
     }
+    p.status = status_word;
     const int num_tiles = ((p.m + Cfg::kTileM - 1) / Cfg::kTileM) * ((p.n + kBN - 1) / kBN);
     // stream-K flags carry the launch's epoch, so they never need zeroing
     p.sk_epoch = next_sk_epoch();
@@ -153,16 +178,14 @@ cudaError_t launch_gemm(GemmKind kind, int group, const GemmParams &p, int num_s
 }
 
 int *device_status_word() {
-    static std::atomic<int *> addr[64];
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
-    if (dev < 64) {
-        if (int *c = addr[dev].load(std::memory_order_relaxed)) return c;
+    thread_local unsigned long long ready_ctx = 0;
+    thread_local int *addr = nullptr;
+    const unsigned long long ctx = current_context_id();
+    if (ctx == 0 || ctx != ready_ctx) {
+        if (cudaGetSymbolAddress(reinterpret_cast<void **>(&addr), g_gemm_status) != cudaSuccess) return nullptr;
+        ready_ctx = ctx;
     }
-    int *p = nullptr;
-    if (cudaGetSymbolAddress(reinterpret_cast<void **>(&p), g_gemm_status) != cudaSuccess) return nullptr;
-    if (dev < 64) addr[dev].store(p, std::memory_order_relaxed);
-    return p;
+    return addr;
 }
 
 int read_and_clear_gemm_status(int *status) {

@@ -31,6 +31,13 @@ int read_and_clear_gemm_status(int *status);
 // Device address of the status word that bounded waits set to -7 (cached per device).
 int *device_status_word();
 
+// Id of the CUDA context current on this thread (cuCtxGetId: unique for the
+// life of the process, so a context created after a device reset gets a new
+// one), or 0 when there is none or it cannot be read.  Host-side state that
+// belongs to a context (symbol addresses, function attributes) is cached
+// under this id and looked up again when it changes; id 0 is never cached.
+unsigned long long current_context_id();
+
 // Records `msg` as this thread's mc2_last_error() text and returns `status`.
 int record_error(int status, const char *msg);
 

@@ -28,6 +28,34 @@ int fail(int status, const char *fmt, ...) {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// ------------------------------------------------------------------ launch events
+// The caller's events that mc2_set_launch_events installed on this thread:
+// events[0] is recorded before a call's first kernel launch, events[i] after
+// its i-th, on the call's stream.
+constexpr int kMaxLaunchEvents = 8;
+thread_local cudaEvent_t g_launch_events[kMaxLaunchEvents];
+thread_local int g_num_launch_events = 0;
+
+// Records the installed events of one call, in launch order.
+class LaunchMarks {
+  public:
+    explicit LaunchMarks(cudaStream_t s) : s_(s) { mark(); }
+    // after each kernel launch of the call
+    void launched() { mark(); }
+
+  private:
+    void mark() {
+        if (next_ < g_num_launch_events) cudaEventRecord(g_launch_events[next_], s_);
+        ++next_;
+    }
+    cudaStream_t s_;
+    int next_ = 0;
+};
+
+// One-shot test hook (mc2_test_expire_next_flag_waits): the wait limit the next
+// AlltoAllQuantMatmul GEMM on this thread runs with, 0 when not armed.
+thread_local uint64_t g_expire_next_flag_waits_ns = 0;
+
 // ------------------------------------------------------------------ driver entry point
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                    const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
@@ -203,6 +231,27 @@ int mc2_device_status(void) {
     return MC2_OK;
 }
 
+int mc2_set_launch_events(void *const *events, int count) {
+    g_last_error[0] = '\0';
+    if (count < 0 || count > kMaxLaunchEvents)
+        return fail(MC2_ERR_SHAPE, "count must be in [0, %d] (got %d)", kMaxLaunchEvents, count);
+    if (count > 0 && !events) return fail(MC2_ERR_NULL, "events is NULL");
+    for (int i = 0; i < count; ++i)
+        if (!events[i]) return fail(MC2_ERR_NULL, "events[%d] is NULL", i);
+    for (int i = 0; i < count; ++i) g_launch_events[i] = static_cast<cudaEvent_t>(events[i]);
+    g_num_launch_events = count;
+    return MC2_OK;
+}
+
+int mc2_test_expire_next_flag_waits(uint64_t wait_limit_ns) {
+    g_last_error[0] = '\0';
+    if (wait_limit_ns == 0 || wait_limit_ns > kWaitLimitNs)
+        return fail(MC2_ERR_SHAPE, "wait_limit_ns must be in [1, %llu] (got %llu)", (unsigned long long)kWaitLimitNs,
+                    (unsigned long long)wait_limit_ns);
+    g_expire_next_flag_waits_ns = wait_limit_ns;
+    return MC2_OK;
+}
+
 int mc2_all_gather_mm(const void *const *x_chunks, int world_size, int64_t m_local, int64_t k, const void *x2,
                       int64_t n, int x2_is_nk, const void *bias, int dtype, int gather_output, void *out,
                       void *gathered, void *stream) {
@@ -277,8 +326,10 @@ int mc2_all_gather_mm(const void *const *x_chunks, int world_size, int64_t m_loc
     p.bias16 = bias;
     p.wait_limit_ns = kWaitLimitNs;
     const mc2::GemmKind kind = dtype == MC2_BF16 ? mc2::GEMM_BF16 : mc2::GEMM_F16;
+    LaunchMarks marks(static_cast<cudaStream_t>(stream));
     cudaError_t e = mc2::launch_gemm(kind, group, p, dev.num_sms, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail(MC2_ERR_CUDA, "GEMM launch: %s", cudaGetErrorString(e));
+    marks.launched();
     return MC2_OK;
 }
 
@@ -346,9 +397,11 @@ int mc2_matmul_reduce_scatter(const void *const *x_chunks, const void *const *w_
     p.kblock_tiles = kKBlockTiles;
     p.bias16 = bias;
     p.wait_limit_ns = kWaitLimitNs;
+    LaunchMarks marks(static_cast<cudaStream_t>(stream));
     cudaError_t e = mc2::launch_gemm(dtype == MC2_BF16 ? mc2::GEMM_RS_BF16 : mc2::GEMM_RS_F16, group, p, dev.num_sms,
                                      static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail(MC2_ERR_CUDA, "GEMM launch: %s", cudaGetErrorString(e));
+    marks.launched();
     return MC2_OK;
 }
 
@@ -372,9 +425,11 @@ int mc2_matmul_weight_grad(const void *dy, int64_t m, int64_t n, const void *x, 
     if (int st = current_device(&dev)) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaSuccess;
+    LaunchMarks marks(s);
     if (db) {
         e = mc2::launch_colsum16(dy, m, static_cast<int>(n), dtype == MC2_BF16, db, s);
         if (e != cudaSuccess) return fail(MC2_ERR_CUDA, "bias-gradient launch: %s", cudaGetErrorString(e));
+        marks.launched();
     }
     // dW (n, k) = dY^T @ X: A = dY^T read M-major from dY (m, n), B = X (m, k) N-major,
     // the contraction runs down the m rows of both
@@ -400,6 +455,7 @@ int mc2_matmul_weight_grad(const void *dy, int64_t m, int64_t n, const void *x, 
     const int group = mc2::gemm_group_for(static_cast<int>(n));
     e = mc2::launch_gemm(dtype == MC2_BF16 ? mc2::GEMM_BF16 : mc2::GEMM_F16, group, p, dev.num_sms, s);
     if (e != cudaSuccess) return fail(MC2_ERR_CUDA, "GEMM launch: %s", cudaGetErrorString(e));
+    marks.launched();
     return MC2_OK;
 }
 
@@ -432,10 +488,12 @@ int mc2_quant_all_reduce(const void *const *x_chunks, const void *const *scale_c
     if (int st = current_device(&dev)) return st;
     const int x_kind = x_dtype == MC2_I8 ? 0 : (x_dtype == MC2_F8E4M3 ? 1 : 2);
     const int out_kind = out_dtype == MC2_F32 ? 0 : (out_dtype == MC2_F16 ? 1 : 2);
+    LaunchMarks marks(static_cast<cudaStream_t>(stream));
     cudaError_t e = mc2::launch_quant_all_reduce(x_chunks, scale_chunks, world_size, bs * h, x_kind,
                                                  scale_dtype == MC2_E8M0 ? 1 : 0, out_kind, out, dev.num_sms,
                                                  static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail(MC2_ERR_CUDA, "QuantAllReduce launch: %s", cudaGetErrorString(e));
+    marks.launched();
     return MC2_OK;
 }
 
@@ -504,6 +562,12 @@ int mc2_alltoall_quant_mm(const void *const *chunks, int rank_size, int64_t bs_l
     if (ws.nkb >= 2 && units <= ws.sk_slots && ws.num_tiles % units != 0) sk_tiles = ws.num_tiles % units;
     cudaError_t e = cudaSuccess;
     bool x2_done = false;
+    if (x1_quant_mode == MC2_QUANT_PERTOKEN && x1_scale_out) {
+        // mode 3: the per-token scales are the caller's; x1_scale_out receives a copy
+        e = cudaMemcpyAsync(x1_scale_out, x1_scale, static_cast<size_t>(bs_local) * 4, cudaMemcpyDeviceToDevice, s);
+        if (e != cudaSuccess) return fail(MC2_ERR_CUDA, "x1 scale copy: %s", cudaGetErrorString(e));
+    }
+    LaunchMarks marks(s);
     if (x1_quant_mode == MC2_QUANT_PERTOKEN_DYNAMIC && mc2::a2a_prologue_fits(rank_size, bs_local, static_cast<int>(h))) {
         e = mc2::launch_a2a_prologue(cp, rank_size, bs_local, static_cast<int>(h), x1_dtype == MC2_BF16, x1_scale, ah,
                                      q_out, scale, x2, x2h, K * n, alltoall_out,
@@ -520,13 +584,15 @@ int mc2_alltoall_quant_mm(const void *const *chunks, int rank_size, int64_t bs_l
         else
             e = mc2::launch_permute_widen_i8(cp, rank_size, bs_local, static_cast<int>(h), ah, q_out,
                                              static_cast<int8_t *>(alltoall_out), dev.num_sms, s);
-        if (e == cudaSuccess && x1_scale_out)
-            e = cudaMemcpyAsync(x1_scale_out, x1_scale, static_cast<size_t>(bs_local) * 4, cudaMemcpyDeviceToDevice, s);
         scale = const_cast<float *>(static_cast<const float *>(x1_scale));
     }
     if (e != cudaSuccess) return fail(MC2_ERR_CUDA, "prologue launch: %s", cudaGetErrorString(e));
-    if (!x2_done) e = mc2::launch_widen_i8(x2, x2h, K * n, dev.num_sms, s);
-    if (e != cudaSuccess) return fail(MC2_ERR_CUDA, "x2 widening launch: %s", cudaGetErrorString(e));
+    marks.launched();
+    if (!x2_done) {
+        e = mc2::launch_widen_i8(x2, x2h, K * n, dev.num_sms, s);
+        if (e != cudaSuccess) return fail(MC2_ERR_CUDA, "x2 widening launch: %s", cudaGetErrorString(e));
+        marks.launched();
+    }
 
     mc2::GemmParams p;
     memset(&p, 0, sizeof(p));
@@ -561,8 +627,15 @@ int mc2_alltoall_quant_mm(const void *const *chunks, int rank_size, int64_t bs_l
     p.sk_partials = reinterpret_cast<int32_t *>(wsb + ws.sk_partials);
     p.sk_flags = reinterpret_cast<unsigned long long *>(wsb + ws.sk_flags);
     p.wait_limit_ns = kWaitLimitNs;
+    if (g_expire_next_flag_waits_ns != 0) {
+        // the test hook: this launch's FINISH parts expect one writer too many
+        p.wait_limit_ns = g_expire_next_flag_waits_ns;
+        p.sk_extra_writers = 1;
+        g_expire_next_flag_waits_ns = 0;
+    }
     e = mc2::launch_gemm(mc2::GEMM_INT_AS_F16, group, p, dev.num_sms, s);
     if (e != cudaSuccess) return fail(MC2_ERR_CUDA, "GEMM launch: %s", cudaGetErrorString(e));
+    marks.launched();
     return MC2_OK;
 }
 

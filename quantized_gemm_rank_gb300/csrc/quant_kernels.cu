@@ -489,12 +489,15 @@ cudaError_t launch_a2a_prologue(const ChunkPtrs &chunks, int rank_size, int64_t 
     const int64_t grid = bs_local + widen_ctas;
     const uint16_t *sm = static_cast<const uint16_t *>(smooth);
     auto kern = bf16 ? a2a_prologue_kernel<true> : a2a_prologue_kernel<false>;
-    // rows above 48 KiB need the opt-in (raised once per process and type)
-    static std::atomic<bool> opted[2];
-    if (smem > 48 * 1024 && !opted[bf16 ? 1 : 0].load(std::memory_order_relaxed)) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024 + 16);
-        if (e != cudaSuccess) return e;
-        opted[bf16 ? 1 : 0].store(true, std::memory_order_relaxed);
+    // rows above 48 KiB need the opt-in (raised once per host thread, context and type)
+    thread_local unsigned long long opted_ctx[2] = {0, 0};
+    if (smem > 48 * 1024) {
+        const unsigned long long ctx = current_context_id();
+        if (ctx == 0 || ctx != opted_ctx[bf16 ? 1 : 0]) {
+            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024 + 16);
+            if (e != cudaSuccess) return e;
+            opted_ctx[bf16 ? 1 : 0] = ctx;
+        }
     }
     // its CTAs may be scheduled before the previous kernel ends (they wait for it)
     cudaLaunchConfig_t cfg = {};
