@@ -13,15 +13,19 @@
 //
 // Costs and rules of that array:
 //   - It is kMaxScratchBytes (32 MiB) on every GPU that loads this library, and
-//     stays allocated until the process exits.
+//     stays allocated until the process exits.  Under CUDA's lazy module
+//     loading (the default) the library's device code, this array with it, is
+//     loaded on a device the first time the library is used there, so the
+//     first call on a device maps the 32 MiB; a caller that must not see
+//     device memory grow mid-run makes one warm-up call at start-up.
 //   - Every call shares it, so calls whose work overlaps on the GPU (different
 //     streams, or different host threads) race on it.  Serialise them.
 //   - It keeps whatever the last call left there.  Nothing in it has to start at
-//     zero: every byte the kernels read is written earlier in the same call.
+//     zero: every byte the kernels read is written earlier in the same call
+//     (the stream-K flags carry a per-launch epoch, so stale ones count as none).
 #include <cuda_runtime.h>
 
 #include <cstdio>
-#include <mutex>
 
 #include "internal.h"
 #include "mc2_gb300.h"
@@ -32,36 +36,20 @@ constexpr size_t kMaxScratchBytes = MC2_NO_ALLOC_SCRATCH_BYTES;
 
 static __device__ __align__(256) unsigned char g_no_alloc_scratch[kMaxScratchBytes];
 
-// Device address of g_no_alloc_scratch, one per device.  In host code the
-// array's name is only a host-side stand-in, so the real address is looked up
-// with that device current, once, the first time the device is used here.
-constexpr int kMaxDevices = 64;
-void *g_scratch_ptr[kMaxDevices] = {nullptr};
-std::mutex g_scratch_mutex;
-
+// Device address of g_no_alloc_scratch on the current device.  In host code
+// the array's name is only a host-side stand-in, so the real address is looked
+// up with the device current.  It is looked up on every call: the lookup
+// neither allocates nor synchronises, and an address kept from before a
+// device reset would point into a context that no longer exists.
 int scratch_for_current_device(void **ptr) {
     char msg[160];
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) {
-        snprintf(msg, sizeof(msg), "cudaGetDevice: %s", cudaGetErrorString(e));
+    void *p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_no_alloc_scratch);
+    if (e != cudaSuccess || p == nullptr) {
+        snprintf(msg, sizeof(msg), "cudaGetSymbolAddress of the scratch failed: %s", cudaGetErrorString(e));
         return mc2::record_error(MC2_ERR_CUDA, msg);
     }
-    if (dev < 0 || dev >= kMaxDevices) {
-        snprintf(msg, sizeof(msg), "device %d is beyond the %d this entry point serves", dev, kMaxDevices);
-        return mc2::record_error(MC2_ERR_UNSUPPORTED, msg);
-    }
-    std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    if (g_scratch_ptr[dev] == nullptr) {
-        void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_no_alloc_scratch);
-        if (e != cudaSuccess || p == nullptr) {
-            snprintf(msg, sizeof(msg), "cudaGetSymbolAddress of the scratch failed: %s", cudaGetErrorString(e));
-            return mc2::record_error(MC2_ERR_CUDA, msg);
-        }
-        g_scratch_ptr[dev] = p;
-    }
-    *ptr = g_scratch_ptr[dev];
+    *ptr = p;
     return MC2_OK;
 }
 
