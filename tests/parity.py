@@ -44,3 +44,16 @@ def assert_bits_equal(got: torch.Tensor, ref: torch.Tensor, what: str):
         bad = (g != r).nonzero()
         raise AssertionError(f"{what}: {bad.shape[0]} of {g.numel()} elements differ; first at {bad[0].tolist()}: "
                              f"got {g[tuple(bad[0])].item()} want {r[tuple(bad[0])].item()}")
+
+
+def rows_per_block(total: int, block: int, seed: int, extra=()) -> torch.Tensor:
+    """Sorted row indices: one seeded row inside every `block`-row block of
+    [0, total) (block 32 = the rows one epilogue warp of a CTA writes), plus the
+    rows in `extra` (chunk edges).  Used where the oracle cannot afford every
+    output row of a full-size workload."""
+    g = torch.Generator().manual_seed(seed)
+    starts = torch.arange(0, total, block)
+    span = torch.clamp(total - starts, max=block)
+    offs = (torch.rand(starts.numel(), generator=g) * span).long()
+    rows = torch.cat([starts + offs, torch.tensor(list(extra), dtype=torch.long)])
+    return torch.unique(rows[(rows >= 0) & (rows < total)])

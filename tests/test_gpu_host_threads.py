@@ -5,7 +5,10 @@ driver's tensor-map entry point) that the first calls fill; calls that race to
 fill them must still launch correctly.  Every thread runs both hot-path calls
 (AllGatherMatmul and the dynamic-quant AlltoAllQuantMatmul) on its own stream
 and its own buffers, and every result must equal, bit for bit, the result of
-the same call made alone (the kernels are deterministic: no split-K atomics).
+the same call made alone.  The kernels are deterministic: the float GEMMs
+compute every tile whole, and the integer GEMM's stream-K tail, which meets
+its partial sums through workspace flags and atomics, adds exact int32 values,
+so the order in which the parts finish does not change the bits.
 """
 import threading
 

@@ -13,7 +13,7 @@ import torch
 import mc2_inputs
 import oracle
 import quantized_gemm_rank_gb300 as mc2
-from parity import assert_bits_equal, assert_close_16
+from parity import assert_bits_equal, assert_close_16, rows_per_block
 
 pytestmark = pytest.mark.gpu
 
@@ -84,10 +84,15 @@ def test_each_rank_contributes_its_own_term():
         assert_bits_equal(run_gpu(cur, shape), run_oracle(cur, shape), f"rank {dead} zeroed")
 
 
-def test_full_size_sampled_rows():
+def test_full_size_row_of_every_warp_block():
+    """mmrs-4x2048 at full size (64 x 32 tiles over the co-resident CTA pairs):
+    one seeded row from every 32-row block, the first and last row of each
+    rank's output, and all outputs finite."""
     shape = mc2_inputs.WORKLOADS["mmrs-4x2048"]
     inp = mc2_inputs.mmrs_inputs(shape, seed=0)
     got = run_gpu(inp, shape)
-    rows = mc2_inputs.sample_rows(shape.m, 64, seed=1)
-    assert_close_16(got[rows], run_oracle(inp, shape, rows=rows), "mmrs-4x2048 sampled rows")
+    per = shape.m // shape.world_size
+    edges = [e for r in range(shape.world_size) for e in (r * per, (r + 1) * per - 1)]
+    rows = rows_per_block(shape.m, 32, seed=1, extra=edges)
+    assert_close_16(got[rows], run_oracle(inp, shape, rows=rows), "mmrs-4x2048 rows")
     assert torch.isfinite(got.float()).all()

@@ -13,7 +13,7 @@ import torch
 import mc2_inputs
 import oracle
 import quantized_gemm_rank_gb300 as mc2
-from parity import assert_bits_equal, assert_close_16
+from parity import assert_bits_equal, assert_close_16, rows_per_block
 
 pytestmark = pytest.mark.gpu
 
@@ -84,12 +84,15 @@ def test_all_gather_layer_backward_end_to_end():
     assert_close_16(db.cpu(), ref_b, "AG backward db")
 
 
-def test_full_size_sampled_rows():
+def test_full_size_row_of_every_warp_block():
+    """wgrad-ag-4x4096 at full size (dW is 7168 x 8192: 28 x 32 tiles): one
+    seeded row of dW from every 32-row block plus the first and last, every
+    element of dB, and all outputs finite."""
     shape = mc2_inputs.WORKLOADS["wgrad-ag-4x4096"]
     inp = mc2_inputs.wgrad_inputs(shape, seed=0)
     dw, db = run_gpu(inp)
-    rows = mc2_inputs.sample_rows(shape.n, 12, seed=1)
+    rows = rows_per_block(shape.n, 32, seed=1, extra=(0, shape.n - 1))
     ref_w, ref_b = oracle.matmul_weight_grad(inp["dy"], inp["x"], rows=rows)
-    assert_close_16(dw[rows], ref_w, "wgrad-ag-4x4096 sampled rows")
+    assert_close_16(dw[rows], ref_w, "wgrad-ag-4x4096 rows")
     assert_close_16(db, ref_b, "wgrad-ag-4x4096 db")
     assert torch.isfinite(dw.float()).all()
