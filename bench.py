@@ -1,15 +1,21 @@
 #!/usr/bin/env python
 """Benchmark of the MC2 fused-linear hot path on GB300.
 
-One step = one pass of the whole hot path over one batch of synthetic input:
-  * mc2_all_gather_mm on "ag-8x1024": 8 rank chunks (1024, 4096) bf16, x2 (4096,
-    4096), gathered output on -> chunk addressing, gathered store, bf16 GEMM;
-  * mc2_alltoall_quant_mm on "a2a-dyn": 8 received chunks (4096, 1024) bf16 with
-    the smooth scale, per-token dynamic quant (mode 7), int8 GEMM with exact
-    int32 accumulation, per-token x per-channel dequant + bias, bf16 out.
+One step = one pass of the whole hot path over one batch of synthetic input,
+on the two largest configurations:
+  * mc2_all_gather_mm on "ag-4x4096": 4 rank chunks (4096, 8192) bf16, the
+    nn.Linear weight w (7168, 8192) passed as x2 = w^T, bias, gathered output on
+    -> chunk addressing, gathered store, bf16 GEMM, bias epilogue;
+  * mc2_alltoall_quant_mm on "a2a-full": 8 received int8 chunks (16384, 4096)
+    with per-token fp32 scales (quant mode 3) -> permute addressing, int8 GEMM
+    with exact int32 accumulation, per-token x per-channel dequant + bias, bf16
+    out.
 value = (2*m*n*k of both GEMMs) / device time per step, in TFLOP/s (bf16 FLOPs
 plus int8 OPs).  L2 (129 MB) is flushed between timed steps by writing a
-512 MiB buffer outside the timed events.
+512 MiB buffer outside the timed events (the step's inputs are far larger than
+L2 as well).  Every kernel of the step is timed between its own CUDA events on
+the launching stream (mc2_set_launch_events), and the roofline is reported for
+the kernel with the largest share of the step.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
@@ -21,6 +27,7 @@ collective) and value is the sum over ranks divided by the slowest rank's time.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import hashlib
 import json
 import os
@@ -39,24 +46,33 @@ import mc2_inputs  # noqa: E402
 
 METRIC = "fused MC2 GEMM TFLOP/s (bf16) & TOP/s (int8) on 1 GB300, % of tensor peak"
 UNIT = "TFLOP/s"
-AG_NAME = "ag-8x1024"
-A2A_NAME = "a2a-dyn"
+AG_NAME = "ag-4x4096"
+A2A_NAME = "a2a-full"
 WORKLOAD = f"{AG_NAME}+{A2A_NAME}"
 FLUSH_BYTES = 512 << 20
 
-# DRAM bytes (read + write) per launch of the bf16 all-gather GEMM on the
-# ag-8x1024 workload, from the ncu capture summarised in
-# profiles/gemm_bf16_ag-8x1024.md, and the hash of the GEMM's sources
-# (GEMM_SOURCES) the capture was taken with: the figure is reported only
-# while they match.
-AG_GEMM_TRAFFIC = 272.30e6          # dram__bytes_read.sum 159.53 MB + dram__bytes_write.sum 112.77 MB
-AG_GEMM_TRAFFIC_SRC_HASH = "473c18471fd6cec7"
+# The step's kernels in launch order: (key, description, kind).  kind "tensor"
+# is a contraction measured in FLOP/s, "hbm" a format conversion in bytes/s.
+STEP_KERNELS = (
+    ("ag_gemm", "mc2_gemm_kernel<bf16> (all-gather GEMM, ag-4x4096)", "tensor"),
+    ("a2a_widen_a", "widen_chunks_i8_kernel (a2a-full activations int8 -> fp16)", "hbm"),
+    ("a2a_widen_b", "widen_i8_kernel (a2a-full x2 int8 -> fp16)", "hbm"),
+    ("a2a_gemm", "mc2_gemm_kernel<int8 as fp16> (a2a-full GEMM)", "tensor"),
+)
+
+# DRAM bytes (read + write) per launch of the step's dominant kernel, from an
+# ncu capture (dram__bytes_read.sum + dram__bytes_write.sum) of that kernel on
+# this workload, and the hash of the GEMM sources (GEMM_SOURCES) it was taken
+# with: the figure is reported only while they match.
+DOMINANT_TRAFFIC = None
+DOMINANT_TRAFFIC_KERNEL = "a2a_gemm"
+DOMINANT_TRAFFIC_SRC_HASH = None
 
 
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--no-extra", action="store_true", help="skip the per-workload table")
@@ -174,6 +190,15 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------------- workloads
+def _ag_host_tensors(ag):
+    return list(ag["chunks"]) + [ag["x2"]] + ([ag["bias"]] if ag["bias"] is not None else [])
+
+
+def _a2a_host_tensors(a2):
+    return list(a2["chunks"]) + [a2["x2"], a2["x2_scale"], a2["bias"]] + \
+        ([a2["x1_scale"]] if a2["x1_scale"] is not None else [])
+
+
 class Step:
     """Device-resident inputs and outputs for one step of the hot path."""
 
@@ -183,23 +208,35 @@ class Step:
         self.ag_s, self.a2a_s = ag_shape, a2a_shape
         if host is None:
             host = {"ag": mc2_inputs.ag_inputs(ag_shape, seed=seed), "a2a": mc2_inputs.a2a_inputs(a2a_shape, seed=seed)}
-        ag, a2 = host["ag"], host["a2a"]
         self.host = host
-        self.ag_chunks = [c.to(dev) for c in ag["chunks"]]
-        self.ag_x2 = ag["x2"].to(dev)
-        self.ag_bias = None if ag["bias"] is None else ag["bias"].to(dev)
+        self.set_inputs([t.to(dev) for t in _ag_host_tensors(host["ag"])],
+                        [t.to(dev) for t in _a2a_host_tensors(host["a2a"])])
         m, n, k = ag_shape.m, ag_shape.n, ag_shape.k
         self.ag_out = torch.empty((m, n), dtype=ag_shape.dtype, device=dev)
         self.ag_gathered = torch.empty((m, k), dtype=ag_shape.dtype, device=dev) if ag_shape.gather_output else None
-        self.a_chunks = [c.to(dev) for c in a2["chunks"]]
-        self.a_x1s = None if a2["x1_scale"] is None else a2["x1_scale"].to(dev)
-        self.a_x2 = a2["x2"].to(dev)
-        self.a_x2s = a2["x2_scale"].to(dev)
-        self.a_bias = a2["bias"].to(dev)
         self.a_out = torch.empty((a2a_shape.bs_local, a2a_shape.n), dtype=torch.bfloat16, device=dev)
         ws = mc2.mc2_alltoall_quant_mm_workspace(a2a_shape.rank_size, a2a_shape.bs_local, a2a_shape.h, a2a_shape.n,
                                                  a2a_shape.quant_mode, self.a_chunks[0].dtype)
         self.ws = torch.empty(ws, dtype=torch.uint8, device=dev)
+
+    def set_inputs(self, ag_t, a2a_t):
+        """Point the step at device tensors laid out as _ag/_a2a_host_tensors."""
+        R = self.ag_s.world_size
+        self.ag_chunks, self.ag_x2 = ag_t[:R], ag_t[R]
+        self.ag_bias = ag_t[R + 1] if self.host["ag"]["bias"] is not None else None
+        Q = self.a2a_s.rank_size
+        self.a_chunks = a2a_t[:Q]
+        self.a_x2, self.a_x2s, self.a_bias = a2a_t[Q], a2a_t[Q + 1], a2a_t[Q + 2]
+        self.a_x1s = a2a_t[Q + 3] if self.host["a2a"]["x1_scale"] is not None else None
+
+    def outputs(self):
+        return [self.ag_out] + ([self.ag_gathered] if self.ag_gathered is not None else []) + [self.a_out]
+
+    def set_outputs(self, outs):
+        self.ag_out = outs[0]
+        if self.ag_gathered is not None:
+            self.ag_gathered = outs[1]
+        self.a_out = outs[-1]
 
     def run_ag(self):
         self.mc2.mc2_all_gather_mm(self.ag_chunks, self.ag_x2, x2_is_nk=self.ag_s.x2_is_nk, bias=self.ag_bias,
@@ -215,11 +252,20 @@ class Step:
         self.run_ag()
         self.run_a2a()
 
-    launches_per_step = 3  # ag: GEMM; a2a (mode 7): fused quant + x2-widening prologue, GEMM
+    # ag: the GEMM; a2a (mode 3): activations widened, x2 widened, the GEMM
+    launches_per_step = 4
 
     @property
     def flops(self):
         return self.ag_s.flops + self.a2a_s.ops
+
+
+def new_events(n, stream):
+    """n timing events, each recorded once so that its CUDA handle exists."""
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    for e in evs:
+        e.record(stream)
+    return evs
 
 
 def time_device(fn, steps, warmup, flush, stream):
@@ -238,6 +284,29 @@ def time_device(fn, steps, warmup, flush, stream):
         b.synchronize()
         times.append(a.elapsed_time(b))
     return times
+
+
+def time_launches(fn, nlaunch, steps, warmup, flush, stream):
+    """Per-launch device times (ms) of a call's kernels, from the library's
+    launch events on `stream` (L2 flushed before each call, outside the events):
+    a list per launch, in launch order."""
+    import quantized_gemm_rank_gb300 as mc2
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    evs = new_events(nlaunch + 1, stream)
+    per = [[] for _ in range(nlaunch)]
+    for _ in range(steps):
+        flush.zero_()
+        mc2.mc2_set_launch_events(evs)
+        try:
+            fn()
+        finally:
+            mc2.mc2_set_launch_events(None)
+        evs[-1].synchronize()
+        for i in range(nlaunch):
+            per[i].append(evs[i].elapsed_time(evs[i + 1]))
+    return per
 
 
 def _arena(tensors, device):
@@ -263,32 +332,22 @@ def time_e2e(step: Step, steps, warmup, dev):
     each direction is one copy per step.  Three device buffer sets and three
     streams (upload, compute, download) ordered by events let step i+1's upload
     and step i-1's download run while step i computes."""
-    ag, a2 = step.host["ag"], step.host["a2a"]
-    host_in = list(ag["chunks"]) + [ag["x2"]] + list(a2["chunks"]) + [a2["x2"], a2["x2_scale"], a2["bias"]]
-    if a2["x1_scale"] is not None:
-        host_in.append(a2["x1_scale"])
+    ag_t, a2a_t = _ag_host_tensors(step.host["ag"]), _a2a_host_tensors(step.host["a2a"])
+    host_in = ag_t + a2a_t
     h_in_buf, h_in = _arena(host_in, torch.device("cpu"))
     for v, t in zip(h_in, host_in):
         v.copy_(t)
     nsets = 3
     sets = [step] + [Step(dev, step.ag_s, step.a2a_s, host=step.host) for _ in range(nsets - 1)]
-    R = len(ag["chunks"])
     d_in_bufs, d_out_bufs, h_out_bufs = [], [], []
     for st in sets:
         buf, v = _arena(host_in, dev)
-        st.ag_chunks, st.ag_x2 = v[:R], v[R]
-        st.a_chunks = v[R + 1:2 * R + 1]
-        st.a_x2, st.a_x2s, st.a_bias = v[2 * R + 1], v[2 * R + 2], v[2 * R + 3]
-        st.a_x1s = v[2 * R + 4] if a2["x1_scale"] is not None else None
+        st.set_inputs(v[:len(ag_t)], v[len(ag_t):])
         d_in_bufs.append(buf)
-        outs = [st.ag_out] + ([st.ag_gathered] if st.ag_gathered is not None else []) + [st.a_out]
-        obuf, ov = _arena(outs, dev)
-        st.ag_out = ov[0]
-        if st.ag_gathered is not None:
-            st.ag_gathered = ov[1]
-        st.a_out = ov[-1]
+        obuf, ov = _arena(st.outputs(), dev)
+        st.set_outputs(ov)
         d_out_bufs.append(obuf)
-        h_out_bufs.append(_arena(outs, torch.device("cpu"))[0])
+        h_out_bufs.append(_arena(st.outputs(), torch.device("cpu"))[0])
     h2d = h_in_buf.numel()
     d2h = h_out_bufs[0].numel()
     up, comp, down = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
@@ -323,15 +382,18 @@ def time_e2e(step: Step, steps, warmup, dev):
         up.wait_stream(s_)
     t1.record(up)
     t1.synchronize()
-    return t0.elapsed_time(t1) / steps, h2d, d2h
+    ms = t0.elapsed_time(t1) / steps
+    del sets, d_in_bufs, d_out_bufs, h_out_bufs
+    torch.cuda.empty_cache()
+    return ms, h2d, d2h
 
 
 # ----------------------------------------------------------------------------- CPU oracle
-def oracle_sample(rows_ag: int, rows_a2a: int, ag_s, a2a_s, host):
+def oracle_sample(rows_ag: int, rows_a2a: int, ag_s, a2a_s, host, seed=11):
     """Oracle on a bounded row sample of the step's workload; returns (seconds, flops)."""
     import oracle
-    ra = mc2_inputs.sample_rows(ag_s.m, rows_ag, seed=11)
-    rb = mc2_inputs.sample_rows(a2a_s.bs_local, rows_a2a, seed=12)
+    ra = mc2_inputs.sample_rows(ag_s.m, rows_ag, seed=seed)
+    rb = mc2_inputs.sample_rows(a2a_s.bs_local, rows_a2a, seed=seed + 1)
     t0 = time.perf_counter()
     oracle.all_gather_mm(host["ag"]["chunks"], host["ag"]["x2"], x2_is_nk=ag_s.x2_is_nk, bias=host["ag"]["bias"],
                          rows=ra, gather_output=False)
@@ -343,23 +405,24 @@ def oracle_sample(rows_ag: int, rows_a2a: int, ag_s, a2a_s, host):
     return dt, flops
 
 
-def oracle_baseline(ag_s, a2a_s, host, target_s=10.0, max_reps=3):
-    """Time the oracle as it stands on whole steps of the workload (every output
-    row of both ops), repeated until ~target_s seconds of CPU work."""
+def oracle_baseline(ag_s, a2a_s, host, rows=256, target_s=12.0, max_reps=6):
+    """Time the oracle as it stands on row samples of the step's workload
+    (`rows` seeded output rows of each op per sample, a new sample each time),
+    repeated until ~target_s seconds of CPU work."""
     import oracle
     t_tot, fl_tot, reps = 0.0, 0.0, 0
     while reps < max_reps and t_tot < target_s:
-        dt, fl = oracle_sample(ag_s.m, a2a_s.bs_local, ag_s, a2a_s, host)
+        dt, fl = oracle_sample(rows, rows, ag_s, a2a_s, host, seed=11 + 2 * reps)
         t_tot += dt
         fl_tot += fl
         reps += 1
     return {"value": fl_tot / t_tot / 1e12, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": f"{reps} whole step(s) of {WORKLOAD} (all {ag_s.m} + {a2a_s.bs_local} output rows), "
-                      f"{t_tot:.1f} s",
+            "sample": f"{reps} sample(s) of {rows} seeded output rows of each op of {WORKLOAD} "
+                      f"(of {ag_s.m} and {a2a_s.bs_local}), {t_tot:.1f} s",
             "single_thread": oracle_single_thread()}
 
 
-def oracle_single_thread(rows=32, timeout_s=300):
+def oracle_single_thread(rows=8, timeout_s=300):
     """The oracle on one host thread: a child process (fork + exec, so no CUDA
     state is inherited) with OMP_NUM_THREADS=1, on `rows` seeded rows of each
     op's output.  None if the child fails or runs out of time."""
@@ -387,13 +450,13 @@ def run_reference(args):
     ag_s, a2a_s = mc2_inputs.WORKLOADS[AG_NAME], mc2_inputs.WORKLOADS[A2A_NAME]
     host = {"ag": mc2_inputs.ag_inputs(ag_s, seed=0), "a2a": mc2_inputs.a2a_inputs(a2a_s, seed=0)}
     import oracle
-    rows = 16   # ~0.1 s of oracle work per step on 16 cores, so K steps end within minutes
+    rows = 16   # about a second of oracle work per step on 16 cores, so K steps end within minutes
     for _ in range(args.warmup):
         oracle_sample(rows, rows, ag_s, a2a_s, host)
     t0 = time.perf_counter()
     tot_fl = 0.0
-    for _ in range(args.steps):
-        _, fl = oracle_sample(rows, rows, ag_s, a2a_s, host)
+    for i in range(args.steps):
+        _, fl = oracle_sample(rows, rows, ag_s, a2a_s, host, seed=11 + 2 * i)
         tot_fl += fl
     dt = time.perf_counter() - t0
     value = tot_fl / dt / 1e12
@@ -403,7 +466,7 @@ def run_reference(args):
             "config": {"workload": WORKLOAD, "step": f"oracle on {rows} seeded rows of each op's output",
                        "parallelism": "host cores"},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
-                             "sample": f"{rows} rows of each op per step"},
+                             "sample": f"{rows} seeded rows of each op per step"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -412,8 +475,9 @@ def run_reference(args):
 # ----------------------------------------------------------------------------- main
 def workload_call(s, dev):
     """Device-resident inputs of one workload and a closure that runs its call.
-    Returns (fn, work, unit): work is FLOPs (or OPs) for the GEMMs, bytes for
-    the HBM-bound QuantAllReduce."""
+    Returns (fn, work, unit, launches): work is FLOPs (or OPs) of the GEMM, or
+    bytes for the HBM-bound QuantAllReduce; launches is the number of kernels
+    the call launches (the last one is the GEMM for every GEMM workload)."""
     import quantized_gemm_rank_gb300 as mc2
     if isinstance(s, mc2_inputs.QARShape):
         inp = mc2_inputs.qar_inputs(s, seed=0)
@@ -421,7 +485,7 @@ def workload_call(s, dev):
         ss = [x.to(dev) for x in inp["scale_chunks"]]
         out = torch.empty((s.bs, s.h), dtype=s.out_dtype, device=dev)
         return (lambda: mc2.mc2_quant_all_reduce(xs, ss, x_kind=s.x_kind, out_dtype=s.out_dtype, out=out)), \
-            s.bytes, "bytes"
+            s.bytes, "bytes", 1
     if isinstance(s, mc2_inputs.AGShape):
         inp = mc2_inputs.ag_inputs(s, seed=0)
         ch = [c.to(dev) for c in inp["chunks"]]
@@ -430,13 +494,13 @@ def workload_call(s, dev):
         out = torch.empty((s.m, s.n), dtype=s.dtype, device=dev)
         g = torch.empty((s.m, s.k), dtype=s.dtype, device=dev)
         return (lambda: mc2.mc2_all_gather_mm(ch, x2, x2_is_nk=s.x2_is_nk, bias=b, out=out, gathered=g)), \
-            s.flops, "flops"
+            s.flops, "flops", 1
     if isinstance(s, mc2_inputs.WGradShape):
         inp = mc2_inputs.wgrad_inputs(s, seed=0)
         dy, x = inp["dy"].to(dev), inp["x"].to(dev)
         dwo = torch.empty((s.n, s.k), dtype=s.dtype, device=dev)
         dbo = torch.empty((s.n,), dtype=s.dtype, device=dev)
-        return (lambda: mc2.mc2_matmul_weight_grad(dy, x, dw=dwo, db=dbo)), s.flops, "flops"
+        return (lambda: mc2.mc2_matmul_weight_grad(dy, x, dw=dwo, db=dbo)), s.flops, "flops", 2
     if isinstance(s, mc2_inputs.MMRSShape):
         inp = mc2_inputs.mmrs_inputs(s, seed=0)
         xs = [x.to(dev) for x in inp["x_chunks"]]
@@ -444,7 +508,7 @@ def workload_call(s, dev):
         b = None if inp["bias"] is None else inp["bias"].to(dev)
         outs = [torch.empty((s.m // s.world_size, s.n), dtype=s.dtype, device=dev) for _ in range(s.world_size)]
         return (lambda: mc2.mc2_matmul_reduce_scatter(xs, ws, w_is_nk=s.w_is_nk, bias=b, out_chunks=outs)), \
-            s.flops, "flops"
+            s.flops, "flops", 1
     inp = mc2_inputs.a2a_inputs(s, seed=0)
     ch = [c.to(dev) for c in inp["chunks"]]
     x1s = None if inp["x1_scale"] is None else inp["x1_scale"].to(dev)
@@ -452,24 +516,57 @@ def workload_call(s, dev):
     out = torch.empty((s.bs_local, s.n), dtype=torch.bfloat16, device=dev)
     ws = torch.empty(mc2.mc2_alltoall_quant_mm_workspace(s.rank_size, s.bs_local, s.h, s.n, s.quant_mode,
                                                          ch[0].dtype), dtype=torch.uint8, device=dev)
+    # mode 7: the fused quant + x2 widening, then the GEMM; mode 3: two widenings, then the GEMM
+    nl = 2 if s.quant_mode == 7 and s.k <= 32768 and s.h % 8 == 0 else 3
     return (lambda: mc2.mc2_alltoall_quant_mm(ch, x2, x2s, b, x1_quant_mode=s.quant_mode, x1_scale=x1s, out=out,
-                                              workspace=ws)), s.ops, "flops"
+                                              workspace=ws)), s.ops, "flops", nl
 
 
-def extra_table(dev, flush, stream, steps, hbm_peak):
-    """Per-workload device times of each call alone (every workload but the step's two);
+def host_call_us(fn, calls=200):
+    """Host-side time of one call (argument marshalling, validation, tensor-map
+    encoding, launch), the GPU kept busy so that no call waits on it: mean over
+    `calls` calls enqueued back to back behind a long fill."""
+    big = torch.empty(4 << 30, dtype=torch.uint8, device="cuda")
+    fn()
+    torch.cuda.synchronize()
+    big.zero_()
+    t0 = time.perf_counter()
+    for _ in range(calls):
+        fn()
+    dt = time.perf_counter() - t0
+    torch.cuda.synchronize()
+    del big
+    torch.cuda.empty_cache()
+    return dt / calls * 1e6
+
+
+def extra_table(dev, flush, stream, steps, peaks):
+    """Per-workload device times of each call alone (every workload but the
+    step's two): the call between the benchmark's events and its GEMM between
+    the library's launch events, with the GEMM's fraction of the tensor peak;
     the HBM-bound QuantAllReduce workloads report GB/s against the HBM peak."""
     res = {}
     for name, s in mc2_inputs.WORKLOADS.items():
         if name in (AG_NAME, A2A_NAME):
             continue
-        fn, work, unit = workload_call(s, dev)
+        fn, work, unit, nl = workload_call(s, dev)
         t = statistics.median(time_device(fn, steps, 3, flush, stream))
+        per = time_launches(fn, nl, steps, 3, flush, stream)
+        k_last = statistics.median(per[-1])
         if unit == "bytes":
-            gbs = work / (t * 1e-3) / 1e9
-            res[name] = {"us": round(t * 1e3, 2), "gbs": round(gbs, 1), "hbm_frac": round(gbs / hbm_peak, 4)}
+            gbs = work / (k_last * 1e-3) / 1e9
+            res[name] = {"us": round(t * 1e3, 2), "kernel_us": round(k_last * 1e3, 2), "gbs": round(gbs, 1),
+                         "hbm_frac": round(gbs / peaks["hbm"], 4)}
         else:
-            res[name] = {"us": round(t * 1e3, 2), "tflops": round(work / (t * 1e-3) / 1e12, 1)}
+            tf = work / (t * 1e-3) / 1e12
+            kt = work / (k_last * 1e-3) / 1e12
+            res[name] = {"us": round(t * 1e3, 2), "tflops": round(tf, 1), "frac": round(tf / peaks["bf16"], 4),
+                         "gemm_us": round(k_last * 1e3, 2), "gemm_tflops": round(kt, 1),
+                         "gemm_frac": round(kt / peaks["bf16"], 4)}
+            if nl > 1:
+                res[name]["prologue_us"] = [round(statistics.median(x) * 1e3, 2) for x in per[:-1]]
+        if name == "ag-tiny":
+            res[name]["host_call_us"] = round(host_call_us(fn), 2)
         del fn
         torch.cuda.empty_cache()
     res["int8_context"] = int8_context(dev, flush, stream, steps)
@@ -479,20 +576,26 @@ def extra_table(dev, flush, stream, steps, hbm_peak):
 def int8_context(dev, flush, stream, steps):
     """Context for the integer path's route (int8 as exact fp16 through tcgen05):
     the legacy mma.sync int8 and fp16 rates of this GPU (register operands, all
-    SMs busy), and torch._int_mm (the library int8 GEMM) on the a2a-dyn shape."""
-    import quantized_gemm_rank_gb300 as mc2
+    SMs busy; the probe in the separate calibration library), and
+    torch._int_mm (the library int8 GEMM) on the a2a-dyn shape."""
+    from quantized_gemm_rank_gb300 import build
+    C = ctypes.CDLL(build.build_calib())
+    C.mc2_calib_mma_sync.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                                     ctypes.POINTER(ctypes.c_double)]
+    C.mc2_calib_mma_sync.restype = ctypes.c_int
     out = {}
     blocks = 4 * torch.cuda.get_device_properties(dev).multi_processor_count
     sink = torch.empty(blocks * 256, dtype=torch.int32, device=dev)
     for kind, key in ((0, "mma_sync_s8_tops"), (1, "mma_sync_f16_tflops")):
-        ops = [0.0]
+        ops = ctypes.c_double(0.0)
 
         def fn(kind=kind):
-            ops[0] = mc2.mc2_calib_mma_sync(kind, 2048, blocks, sink, stream=stream)
+            if C.mc2_calib_mma_sync(kind, 2048, blocks, sink.data_ptr(), stream.cuda_stream, ctypes.byref(ops)) != 0:
+                raise RuntimeError("calibration launch failed")
 
         t = statistics.median(time_device(fn, steps, 3, flush, stream))
-        out[key] = round(ops[0] / (t * 1e-3) / 1e12, 1)
-    s = mc2_inputs.WORKLOADS[A2A_NAME]
+        out[key] = round(ops.value / (t * 1e-3) / 1e12, 1)
+    s = mc2_inputs.WORKLOADS["a2a-dyn"]
     a = torch.randint(-127, 128, (s.bs_local, s.k), dtype=torch.int8, device=dev)
     b = torch.randint(-127, 128, (s.n, s.k), dtype=torch.int8, device=dev).t()   # (k, n), column-major
     try:
@@ -511,12 +614,19 @@ def profile_workload(name, args):
     """--profile --workload NAME: only W + K calls of that workload (for ncu)."""
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
-    fn, work, unit = workload_call(mc2_inputs.WORKLOADS[name], dev)
+    fn, work, unit, _ = workload_call(mc2_inputs.WORKLOADS[name], dev)
     stream = torch.cuda.current_stream()
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     t = statistics.median(time_device(fn, args.steps, args.warmup, flush, stream))
     print(json.dumps({"workload": name, "ms": round(t, 4), "work": work, "unit": unit}), flush=True)
     return 0
+
+
+def kernel_work(ag_s, a2a_s):
+    """Algorithmic work per launch of each step kernel: FLOPs for the GEMMs,
+    bytes moved (int8 read + fp16 written) for the widening passes."""
+    return {"ag_gemm": ag_s.flops, "a2a_widen_a": 3.0 * a2a_s.bs_local * a2a_s.k,
+            "a2a_widen_b": 3.0 * a2a_s.k * a2a_s.n, "a2a_gemm": a2a_s.ops}
 
 
 def main():
@@ -535,7 +645,12 @@ def main():
 
     ag_s, a2a_s = mc2_inputs.WORKLOADS[AG_NAME], mc2_inputs.WORKLOADS[A2A_NAME]
     step = Step(dev, ag_s, a2a_s, seed=rank)
+    mc2 = step.mc2
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    # events: [0] step start, [1..2] around the AG GEMM, [3..6] around the a2a's
+    # three kernels (recorded by the library), [7] step end
+    evs = new_events(8, stream)
+    nk = len(STEP_KERNELS)
 
     # ---- timed region: K steps, barrier + synchronize on both sides
     sampler = ClockSampler(local)
@@ -547,19 +662,22 @@ def main():
     sampler.start()
     wall0 = time.perf_counter()
     step_ms, ag_ms = [], []
+    kern_ms = [[] for _ in range(nk)]
     for _ in range(args.steps):
         flush.zero_()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e2 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
+        evs[0].record(stream)
+        mc2.mc2_set_launch_events(evs[1:3])
         step.run_ag()
-        e1.record(stream)
+        mc2.mc2_set_launch_events(evs[3:7])
         step.run_a2a()
-        e2.record(stream)
-        e2.synchronize()
-        step_ms.append(e0.elapsed_time(e2))
-        ag_ms.append(e0.elapsed_time(e1))
+        mc2.mc2_set_launch_events(None)
+        evs[7].record(stream)
+        evs[7].synchronize()
+        step_ms.append(evs[0].elapsed_time(evs[7]))
+        ag_ms.append(evs[0].elapsed_time(evs[3]))
+        kern_ms[0].append(evs[1].elapsed_time(evs[2]))
+        for j in range(3):
+            kern_ms[1 + j].append(evs[3 + j].elapsed_time(evs[4 + j]))
     torch.cuda.synchronize()
     barrier(world)
     torch.cuda.synchronize()
@@ -570,39 +688,68 @@ def main():
     ms = max_over_ranks(ms, world)
     value = job_tflops(step.flops, world, ms)
     ag_mean = sum(ag_ms) / len(ag_ms)
-    ag_tflops = ag_s.flops / (ag_mean * 1e-3) / 1e12
+    a2a_mean = ms - ag_mean
+    kmean = [sum(x) / len(x) for x in kern_ms]
+    work = kernel_work(ag_s, a2a_s)
+    per_kernel = {}
+    for (key, desc, kind), t in zip(STEP_KERNELS, kmean):
+        d = {"kernel": desc, "us": round(t * 1e3, 2), "share": round(t / ms, 4)}
+        if kind == "tensor":
+            tf = work[key] / (t * 1e-3) / 1e12
+            d.update({"tflops": round(tf, 1), "frac": round(tf / peaks["bf16"], 4)})
+        else:
+            gbs = work[key] / (t * 1e-3) / 1e9
+            d.update({"gbs": round(gbs, 1), "hbm_frac": round(gbs / peaks["hbm"], 4)})
+        per_kernel[key] = d
+    dom_i = max(range(nk), key=lambda i: kmean[i])
+    dom_key, dom_desc, dom_kind = STEP_KERNELS[dom_i]
+    dom_t = kmean[dom_i]
+    if dom_kind == "tensor":
+        achieved = work[dom_key] / (dom_t * 1e-3) / 1e12
+        peak, unit_r, bound = peaks["bf16"], "TFLOP/s", "tensor"
+        pkind = f"bf16 dense burst, {peaks['source']}"
+    else:
+        achieved = work[dom_key] / (dom_t * 1e-3) / 1e9
+        peak, unit_r, bound = peaks["hbm"], "GB/s", "hbm"
+        pkind = f"HBM copy, {peaks['source']}"
+    traffic = None
+    if (DOMINANT_TRAFFIC is not None and DOMINANT_TRAFFIC_KERNEL == dom_key
+            and DOMINANT_TRAFFIC_SRC_HASH == kernel_src_hash()):
+        traffic = DOMINANT_TRAFFIC
+    roof = {"kernel": dom_desc, "bound": bound, "achieved": round(achieved, 1), "peak": peak, "unit": unit_r,
+            "frac": round(achieved / peak, 4), "traffic": traffic, "peak_kind": pkind,
+            "frac_of_sustained_peak": round(achieved / peaks["bf16_sustained"], 4) if bound == "tensor" else None,
+            "algorithmic_work_per_launch": work[dom_key], "mean_launch_us": round(dom_t * 1e3, 2),
+            "launches_timed": args.steps}
 
     # ---- end to end through the public calls with host buffers
     if args.profile:
         e2e_ms, h2d, d2h = float("nan"), 0, 0
     else:
-        e2e_ms, h2d, d2h = time_e2e(step, args.steps, 3, dev)
+        e2e_ms, h2d, d2h = time_e2e(step, max(10, args.steps // 2), 3, dev)
         e2e_ms = max_over_ranks(e2e_ms, world)
     e2e_value = None if args.profile else round(job_tflops(step.flops, world, e2e_ms), 2)
 
-    mc2 = step.mc2
     assert mc2.mc2_device_status() == mc2.MC2_OK, "a bounded device wait gave up"
 
-    extra = None if (args.no_extra or args.profile or rank != 0) else extra_table(dev, flush, stream, 10, peaks["hbm"])
+    extra = None if (args.no_extra or args.profile or rank != 0) else extra_table(dev, flush, stream, 10, peaks)
     cpu = oracle_baseline(ag_s, a2a_s, step.host) if (rank == 0 and world == 1 and not args.profile) else None
 
-    traffic = AG_GEMM_TRAFFIC if (AG_GEMM_TRAFFIC is not None and AG_GEMM_TRAFFIC_SRC_HASH == kernel_src_hash()) \
-        else None
-    roof = {"kernel": "mc2_gemm_kernel<bf16> (all-gather GEMM, ag-8x1024)", "bound": "tensor",
-            "achieved": round(ag_tflops, 1), "peak": peaks["bf16"], "unit": "TFLOP/s",
-            "frac": round(ag_tflops / peaks["bf16"], 4), "traffic": traffic,
-            "peak_kind": f"bf16 dense burst, {peaks['source']}",
-            "algorithmic_flops_per_launch": ag_s.flops}
     line = {"metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16+int8", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "all_gather_mm": "8 x (1024, 4096) bf16 @ (4096, 4096), gathered",
-                       "alltoall_quant_mm": "8 x (4096, 1024) bf16 -> (4096, 8192) @ int8 (8192, 4096), mode 7",
-                       "l2": "flushed between timed steps (512 MiB write outside the events)",
+            "config": {"workload": WORKLOAD,
+                       "all_gather_mm": "4 x (4096, 8192) bf16 @ w(7168, 8192)^T + bias, gathered",
+                       "alltoall_quant_mm": "8 x (16384, 4096) int8 -> (16384, 32768) @ int8 (32768, 7168), "
+                                            "mode 3 (per-token x1 scale)",
+                       "l2": "flushed between timed steps (512 MiB write outside the events); inputs > L2",
                        "parallelism": f"replicas x{world}", "wall_s": round(wall, 3)},
-            "per_op": {AG_NAME: {"ms": round(ag_mean, 4), "tflops": round(ag_tflops, 1)},
-                       A2A_NAME: {"ms": round(ms - ag_mean, 4),
-                                  "tops": round(a2a_s.ops / ((ms - ag_mean) * 1e-3) / 1e12, 1)}},
+            "per_op": {AG_NAME: {"ms": round(ag_mean, 4), "tflops": round(ag_s.flops / (ag_mean * 1e-3) / 1e12, 1),
+                                 "frac": round(ag_s.flops / (ag_mean * 1e-3) / 1e12 / peaks["bf16"], 4)},
+                       A2A_NAME: {"ms": round(a2a_mean, 4),
+                                  "tops": round(a2a_s.ops / (a2a_mean * 1e-3) / 1e12, 1),
+                                  "frac": round(a2a_s.ops / (a2a_mean * 1e-3) / 1e12 / peaks["bf16"], 4)}},
+            "per_kernel": per_kernel,
             "roofline": roof,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},

@@ -5,11 +5,24 @@
 // tensor-core instruction.  Each warp runs kChains independent accumulator
 // chains over fixed register operands (the values do not matter for the rate);
 // one store per thread keeps the work live.
+//
+// This is a measurement probe for the benchmark, not part of the operations:
+// it is built into its own library (libmc2_calib.so), which only bench.py
+// loads.  Its one entry point:
+//
+//   int mc2_calib_mma_sync(int kind, int64_t iters, int blocks, int32_t *sink,
+//                          void *stream, double *ops);
+//
+// launches `blocks` CTAs of 256 threads on `stream` (a cudaStream_t), each warp
+// running `iters` rounds of 8 independent mma.sync on register operands:
+// kind 0 = int8 x int8 -> int32 (m16n8k32), kind 1 = fp16 x fp16 -> fp32
+// (m16n8k16).  `sink` (device, blocks * 256 int32) receives one word per
+// thread; *ops receives the operations (2 per multiply-add) of the launch.
+// Returns 0, -1 for a NULL sink or ops, -2 for a bad kind, iters or blocks,
+// -6 if the launch fails.
 #include <cuda_runtime.h>
 
 #include <cstdint>
-
-#include "mc2_gb300.h"
 
 namespace {
 
@@ -61,17 +74,17 @@ __global__ void __launch_bounds__(kCalibThreads) mma_sync_rate_kernel(int64_t it
 extern "C" {
 
 int mc2_calib_mma_sync(int kind, int64_t iters, int blocks, int32_t *sink, void *stream, double *ops) {
-    if (!sink || !ops) return MC2_ERR_NULL;
-    if ((kind != 0 && kind != 1) || iters < 1 || blocks < 1) return MC2_ERR_SHAPE;
+    if (!sink || !ops) return -1;
+    if ((kind != 0 && kind != 1) || iters < 1 || blocks < 1) return -2;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (kind == 0)
         mma_sync_rate_kernel<true><<<blocks, kCalibThreads, 0, s>>>(iters, sink);
     else
         mma_sync_rate_kernel<false><<<blocks, kCalibThreads, 0, s>>>(iters, sink);
-    if (cudaGetLastError() != cudaSuccess) return MC2_ERR_CUDA;
+    if (cudaGetLastError() != cudaSuccess) return -6;
     const double per_mma = kind == 0 ? 2.0 * 16 * 8 * 32 : 2.0 * 16 * 8 * 16;
     *ops = per_mma * kChains * static_cast<double>(iters) * (kCalibThreads / 32) * blocks;
-    return MC2_OK;
+    return 0;
 }
 
 }  // extern "C"

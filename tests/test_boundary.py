@@ -42,17 +42,36 @@ def test_library_exports_every_declared_symbol():
         assert hasattr(L, name), name
 
 
-def test_calibration_rejects_before_launch():
-    import ctypes
-    L = mc2.lib()
+def test_calibration_probe_is_not_in_the_operations_library():
+    """The mma.sync calibration probe lives in its own library that only the
+    benchmark loads; it rejects bad arguments before launching."""
+    from quantized_gemm_rank_gb300 import build
+    assert not hasattr(mc2.lib(), "mc2_calib_mma_sync")
+    C = ctypes.CDLL(build.build_calib())
+    C.mc2_calib_mma_sync.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                                     ctypes.POINTER(ctypes.c_double)]
     ops = ctypes.c_double(-1.0)
     fake = ctypes.c_void_p(256)   # never dereferenced: validation fails first
-    assert L.mc2_calib_mma_sync(0, 16, 4, None, None, ctypes.byref(ops)) == mc2.MC2_ERR_NULL
-    assert L.mc2_calib_mma_sync(0, 16, 4, fake, None, None) == mc2.MC2_ERR_NULL
-    assert L.mc2_calib_mma_sync(2, 16, 4, fake, None, ctypes.byref(ops)) == mc2.MC2_ERR_SHAPE
-    assert L.mc2_calib_mma_sync(0, 0, 4, fake, None, ctypes.byref(ops)) == mc2.MC2_ERR_SHAPE
-    assert L.mc2_calib_mma_sync(1, 16, 0, fake, None, ctypes.byref(ops)) == mc2.MC2_ERR_SHAPE
+    assert C.mc2_calib_mma_sync(0, 16, 4, None, None, ctypes.byref(ops)) == -1
+    assert C.mc2_calib_mma_sync(0, 16, 4, fake, None, None) == -1
+    assert C.mc2_calib_mma_sync(2, 16, 4, fake, None, ctypes.byref(ops)) == -2
+    assert C.mc2_calib_mma_sync(0, 0, 4, fake, None, ctypes.byref(ops)) == -2
+    assert C.mc2_calib_mma_sync(1, 16, 0, fake, None, ctypes.byref(ops)) == -2
     assert ops.value == -1.0
+
+
+def test_launch_events_and_test_hook_validate_their_arguments():
+    L = mc2.lib()
+    assert L.mc2_set_launch_events(None, 0) == mc2.MC2_OK
+    assert L.mc2_set_launch_events(None, 2) == mc2.MC2_ERR_NULL
+    assert L.mc2_set_launch_events(None, 9) == mc2.MC2_ERR_SHAPE
+    assert L.mc2_set_launch_events(None, -1) == mc2.MC2_ERR_SHAPE
+    arr = (ctypes.c_void_p * 2)(FAKE, None)
+    assert L.mc2_set_launch_events(arr, 2) == mc2.MC2_ERR_NULL
+    assert "events[1]" in mc2.last_error()
+    # out-of-range limits are refused (and arm nothing)
+    assert L.mc2_test_expire_next_flag_waits(0) == mc2.MC2_ERR_SHAPE
+    assert L.mc2_test_expire_next_flag_waits(2_000_000_001) == mc2.MC2_ERR_SHAPE
 
 
 def test_status_strings():
