@@ -33,7 +33,10 @@
 //               the load pipeline, so it issues one copy for A and one for B
 //               (N-major B through a 3-D map when n % 64 == 0), with the copy
 //               forms fixed at compile time for its k-tile loop.
-//   warp 1      TMEM allocator; MMA issuer (one lane; the leader CTA for kG = 2)
+//   warp 1      TMEM allocator; MMA issuer (the leader CTA for kG = 2): the whole
+//               warp runs the issue loop converged and one elected lane issues
+//               each tcgen05 instruction (a loop run by a lone lane left the
+//               tensor pipe idle ~150 cycles per 512-cycle stage)
 //   warp 2      gathered-output TMA store (one lane; AllGather with gather only).
 //               On n-tile-0 tiles the MMA commits each stage to a "consumed"
 //               barrier instead of "empty"; this warp then stores the A tile
@@ -530,7 +533,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
             }
             ptx::nanosleep(20000);
         }
-    } else if (warp == 1 && lane == 0 && leader) {
+    } else if (warp == 1 && leader) {
         // ------------------------------------------------------------ MMA issuer
         const bool a_mn = p.a_mode == A_SINGLE_MN;
         const uint32_t idesc = ptx::idesc_f16(kBF16 && !kIntPath, p.b_mn_major != 0, Cfg::kTileM, kBN, a_mn);
@@ -564,8 +567,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
             for (int kt = kt_begin; kt < kt_end; ++kt) {
                 if (kin == 0) {
                     const uint32_t b = acc_iter & 1u;
-                    if (!wait_or_abort<kPair>(ptx::smem_u32(&tempty_bar[b]), ((acc_iter >> 1) & 1u) ^ 1u, p,
-                                              abort_flag)) {
+                    const bool got = wait_or_abort<kPair>(ptx::smem_u32(&tempty_bar[b]), ((acc_iter >> 1) & 1u) ^ 1u,
+                                                          p, abort_flag);
+                    if (!__all_sync(0xffffffffu, got)) {
                         ok = false;
                         break;
                     }
@@ -573,7 +577,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
                     d_tmem = tmem_base + b * kBN;
                 }
                 // (CTA scope: the stage is completed by the copies' transaction bytes)
-                if (!wait_or_abort<false>(full0 + 8u * stage, phase, p, abort_flag)) {
+                const bool gotf = wait_or_abort<false>(full0 + 8u * stage, phase, p, abort_flag);
+                if (!__all_sync(0xffffffffu, gotf)) {
                     ok = false;
                     break;
                 }
@@ -605,9 +610,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
         // On the normal path they have all completed already (the epilogue waited
         // for their accumulators) and this returns at once.
         ptx::mma_commit_local<kG>(ptx::smem_u32(drain_bar));
-        if (!ptx::mbar_wait(ptx::smem_u32(drain_bar), 0u, p.wait_limit_ns)) {
+        if (!__all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(drain_bar), 0u, p.wait_limit_ns))) {
             *abort_flag = 1;
-            if (p.status) atomicExch(p.status, -7);
+            if (p.status && lane == 0) atomicExch(p.status, -7);
         }
     } else if (warp == 2 && lane == 0 && p.gather) {
         // ------------------------------------------------------------ gathered store
