@@ -80,6 +80,9 @@ def parse_args():
                     help="only the timed steps (no e2e, per-workload table or CPU baseline): for ncu")
     ap.add_argument("--workload", default=None, choices=sorted(mc2_inputs.WORKLOADS),
                     help="with --profile: time only this workload's call")
+    ap.add_argument("--cublas", default=None, metavar="MxNxK",
+                    help="with --profile: time only torch.matmul (the library bf16 GEMM) on (M, K) @ (K, N), "
+                         "as context for the GEMM's profile")
     return ap.parse_args()
 
 
@@ -622,6 +625,24 @@ def profile_workload(name, args):
     return 0
 
 
+def profile_cublas(shape, args):
+    """--profile --cublas MxNxK: only W + K calls of torch.matmul on bf16 (M, K) @ (K, N)
+    with N(0, 1) and N(0, 1/K) data, for a library reference on the same problem (for ncu)."""
+    m, n, k = (int(x) for x in shape.split("x"))
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    g = torch.Generator(device=dev).manual_seed(0)
+    a = torch.randn(m, k, device=dev, generator=g).to(torch.bfloat16)
+    b = (torch.randn(k, n, device=dev, generator=g) * k ** -0.5).to(torch.bfloat16)
+    c = torch.empty(m, n, device=dev, dtype=torch.bfloat16)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    t = statistics.median(time_device(lambda: torch.matmul(a, b, out=c), args.steps, args.warmup, flush, stream))
+    print(json.dumps({"cublas": [m, n, k], "ms": round(t, 4), "tflops": round(2.0 * m * n * k / t / 1e9, 1)}),
+          flush=True)
+    return 0
+
+
 def kernel_work(ag_s, a2a_s):
     """Algorithmic work per launch of each step kernel: FLOPs for the GEMMs,
     bytes moved (int8 read + fp16 written) for the widening passes."""
@@ -637,6 +658,8 @@ def main():
         args.warmup = 3
     if args.profile and args.workload:
         return profile_workload(args.workload, args)
+    if args.profile and args.cublas:
+        return profile_cublas(args.cublas, args)
     rank, world, local = dist_setup(args.gpus)
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
