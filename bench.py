@@ -55,8 +55,7 @@ FLUSH_BYTES = 512 << 20
 # is a contraction measured in FLOP/s, "hbm" a format conversion in bytes/s.
 STEP_KERNELS = (
     ("ag_gemm", "mc2_gemm_kernel<bf16> (all-gather GEMM, ag-4x4096)", "tensor"),
-    ("a2a_widen_a", "widen_chunks_i8_kernel (a2a-full activations int8 -> fp16)", "hbm"),
-    ("a2a_widen_b", "widen_i8_kernel (a2a-full x2 int8 -> fp16)", "hbm"),
+    ("a2a_widen", "widen_a2a_kernel (a2a-full chunks and x2 int8 -> fp16)", "hbm"),
     ("a2a_gemm", "mc2_gemm_kernel<int8 as fp16> (a2a-full GEMM)", "tensor"),
 )
 
@@ -255,8 +254,8 @@ class Step:
         self.run_ag()
         self.run_a2a()
 
-    # ag: the GEMM; a2a (mode 3): activations widened, x2 widened, the GEMM
-    launches_per_step = 4
+    # ag: the GEMM; a2a (mode 3): the chunks and x2 widened in one pass, the GEMM
+    launches_per_step = 3
 
     @property
     def flops(self):
@@ -519,8 +518,12 @@ def workload_call(s, dev):
     out = torch.empty((s.bs_local, s.n), dtype=torch.bfloat16, device=dev)
     ws = torch.empty(mc2.mc2_alltoall_quant_mm_workspace(s.rank_size, s.bs_local, s.h, s.n, s.quant_mode,
                                                          ch[0].dtype), dtype=torch.uint8, device=dev)
-    # mode 7: the fused quant + x2 widening, then the GEMM; mode 3: two widenings, then the GEMM
-    nl = 2 if s.quant_mode == 7 and s.k <= 32768 and s.h % 8 == 0 else 3
+    # mode 7: the fused quant + x2 widening, then the GEMM (3 launches past 32768 columns);
+    # mode 3: one widening pass then the GEMM when h % 64 == 0, else two widenings
+    if s.quant_mode == 7:
+        nl = 2 if s.k <= 32768 and s.h % 8 == 0 else 3
+    else:
+        nl = 2 if s.h % 64 == 0 else 3
     return (lambda: mc2.mc2_alltoall_quant_mm(ch, x2, x2s, b, x1_quant_mode=s.quant_mode, x1_scale=x1s, out=out,
                                               workspace=ws)), s.ops, "flops", nl
 
@@ -646,8 +649,8 @@ def profile_cublas(shape, args):
 def kernel_work(ag_s, a2a_s):
     """Algorithmic work per launch of each step kernel: FLOPs for the GEMMs,
     bytes moved (int8 read + fp16 written) for the widening passes."""
-    return {"ag_gemm": ag_s.flops, "a2a_widen_a": 3.0 * a2a_s.bs_local * a2a_s.k,
-            "a2a_widen_b": 3.0 * a2a_s.k * a2a_s.n, "a2a_gemm": a2a_s.ops}
+    return {"ag_gemm": ag_s.flops, "a2a_widen": 3.0 * (a2a_s.bs_local * a2a_s.k + a2a_s.k * a2a_s.n),
+            "a2a_gemm": a2a_s.ops}
 
 
 def main():
@@ -670,9 +673,9 @@ def main():
     step = Step(dev, ag_s, a2a_s, seed=rank)
     mc2 = step.mc2
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    # events: [0] step start, [1..2] around the AG GEMM, [3..6] around the a2a's
-    # three kernels (recorded by the library), [7] step end
-    evs = new_events(8, stream)
+    # events: [0] step start, [1..2] around the AG GEMM, [3..5] around the a2a's
+    # two kernels (recorded by the library), [6] step end
+    evs = new_events(7, stream)
     nk = len(STEP_KERNELS)
 
     # ---- timed region: K steps, barrier + synchronize on both sides
@@ -691,15 +694,15 @@ def main():
         evs[0].record(stream)
         mc2.mc2_set_launch_events(evs[1:3])
         step.run_ag()
-        mc2.mc2_set_launch_events(evs[3:7])
+        mc2.mc2_set_launch_events(evs[3:6])
         step.run_a2a()
         mc2.mc2_set_launch_events(None)
-        evs[7].record(stream)
-        evs[7].synchronize()
-        step_ms.append(evs[0].elapsed_time(evs[7]))
+        evs[6].record(stream)
+        evs[6].synchronize()
+        step_ms.append(evs[0].elapsed_time(evs[6]))
         ag_ms.append(evs[0].elapsed_time(evs[3]))
         kern_ms[0].append(evs[1].elapsed_time(evs[2]))
-        for j in range(3):
+        for j in range(2):
             kern_ms[1 + j].append(evs[3 + j].elapsed_time(evs[4 + j]))
     torch.cuda.synchronize()
     barrier(world)

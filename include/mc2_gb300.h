@@ -313,8 +313,9 @@ int mc2_device_status(void);
  *   mc2_alltoall_quant_mm      x1_quant_mode 7: 2 (the fused quant and x2
  *                              widening, the GEMM), or 3 when rank_size*h > 32768
  *                              or h % 8 != 0 (the quant, the x2 widening, the
- *                              GEMM); x1_quant_mode 3: 3 (the activations'
- *                              widening, the x2 widening, the GEMM)
+ *                              GEMM); x1_quant_mode 3: 2 when h % 64 == 0 (the
+ *                              widening of the chunks and x2, the GEMM), else 3
+ *                              (the permuted widening, the x2 widening, the GEMM)
  * An event between two launches also keeps the second from starting early
  * (programmatic dependent launch), which can add a few microseconds to a
  * call.  The setting is per host thread and stays until changed; the caller

@@ -52,10 +52,13 @@ cudaError_t launch_a2a_prologue(const ChunkPtrs &chunks, int rank_size, int64_t 
                                 __half *x2h, int64_t x2_count, void *comm_out, int *status, uint64_t wait_limit_ns,
                                 cudaStream_t stream);
 cudaError_t launch_widen_i8(const int8_t *src, __half *dst, int64_t count, int num_sms, cudaStream_t stream);
-// Widens each rank's int8 chunk to fp16 in its own layout at dst + r*bs_local*h
-// (h % 16 == 0); q_out (optional) receives the permuted int8 matrix.
-cudaError_t launch_widen_chunks_i8(const ChunkPtrs &chunks, int rank_size, int64_t bs_local, int h, __half *dst,
-                                   int8_t *q_out, int8_t *comm_out, int num_sms, cudaStream_t stream);
+// The full-quant path's widenings in one launch: each rank's int8 chunk to fp16
+// in its own layout at dst_a + r*bs_local*h (h % 16 == 0), and x2 (x2_count
+// elements, a multiple of 16) to dst_b; q_out (optional) receives the permuted
+// int8 matrix.
+cudaError_t launch_widen_a2a(const ChunkPtrs &chunks, int rank_size, int64_t bs_local, int h, __half *dst_a,
+                             const int8_t *x2, __half *dst_b, int64_t x2_count, int8_t *q_out, int8_t *comm_out,
+                             int num_sms, cudaStream_t stream);
 cudaError_t launch_permute_widen_i8(const ChunkPtrs &chunks, int rank_size, int64_t bs_local, int h, __half *dst,
                                     int8_t *q_out, int8_t *comm_out, int num_sms, cudaStream_t stream);
 // db[j] = sum_t dy[t, j] for dy (m, n) 16-bit row-major, n % 8 == 0: fp32 sums

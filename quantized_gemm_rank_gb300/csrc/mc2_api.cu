@@ -550,9 +550,10 @@ int mc2_alltoall_quant_mm(const void *const *chunks, int rank_size, int64_t bs_l
     memset(&cp, 0, sizeof(cp));
     for (int r = 0; r < rank_size; ++r) cp.p[r] = chunks[r];
 
-    // Mode 3 with h % 64 == 0: each chunk is widened in place of its own and the
-    // GEMM reads the permuted matrix through one tensor map per chunk (a k-tile
-    // never straddles two chunks); otherwise the widening writes it permuted.
+    // Mode 3 with h % 64 == 0: each chunk is widened in place of its own (with x2,
+    // in one pass) and the GEMM reads the permuted matrix through one tensor map
+    // per chunk (a k-tile never straddles two chunks); otherwise the widening
+    // writes it permuted.
     const bool a_by_chunk = x1_quant_mode == MC2_QUANT_PERTOKEN && h % mc2::kBK == 0;
     // stream-K tail: the tiles left over after whole waves of the co-resident pairs
     // (or CTAs) are split by K blocks over all of them (needs >= 2 K blocks a tile)
@@ -577,11 +578,13 @@ int mc2_alltoall_quant_mm(const void *const *chunks, int rank_size, int64_t bs_l
         e = mc2::launch_quant_pertoken(cp, rank_size, bs_local, static_cast<int>(h), x1_dtype == MC2_BF16, x1_scale,
                                        ah, q_out, scale, alltoall_out, dev.num_sms, s);
     } else {
-        // mode 3: the scales are the caller's; the int8 chunks are widened
-        if (a_by_chunk)
-            e = mc2::launch_widen_chunks_i8(cp, rank_size, bs_local, static_cast<int>(h), ah, q_out,
-                                            static_cast<int8_t *>(alltoall_out), dev.num_sms, s);
-        else
+        // mode 3: the scales are the caller's; the int8 chunks and x2 are widened, in
+        // one pass when the GEMM reads the chunks in their own layout
+        if (a_by_chunk) {
+            e = mc2::launch_widen_a2a(cp, rank_size, bs_local, static_cast<int>(h), ah, x2, x2h, K * n, q_out,
+                                      static_cast<int8_t *>(alltoall_out), dev.num_sms, s);
+            x2_done = true;
+        } else
             e = mc2::launch_permute_widen_i8(cp, rank_size, bs_local, static_cast<int>(h), ah, q_out,
                                              static_cast<int8_t *>(alltoall_out), dev.num_sms, s);
         scale = const_cast<float *>(static_cast<const float *>(x1_scale));

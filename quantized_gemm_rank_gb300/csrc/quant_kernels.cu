@@ -369,36 +369,69 @@ __global__ void __launch_bounds__(256) widen_i8_kernel(const int8_t *__restrict_
     ptx::allow_dependent_launch();
 }
 
-// Each rank's int8 chunk -> fp16 in its own layout (dst + r * bs_local * h), so
-// the GEMM reads the permuted matrix through per-chunk tensor maps instead of
-// a materialised permuted copy; q_out (optional) gets the permuted int8 matrix.
-// h % 16 == 0.
-__global__ void __launch_bounds__(256) widen_chunks_i8_kernel(const __grid_constant__ ChunkPtrs chunks, int h,
-                                                              int64_t bs_local, int rank_size,
-                                                              __half *__restrict__ dst, int8_t *__restrict__ q_out,
-                                                              int8_t *__restrict__ comm_out) {
-    ptx::allow_dependent_launch();
-    const int64_t per_chunk = bs_local * h / 16;  // 16-element vectors per chunk
-    const int64_t total = per_chunk * rank_size;
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+// The full-quant path's two widenings in one launch: each rank's int8 chunk
+// -> fp16 in its own layout at dst_a + r * bs_local * h (the GEMM then reads
+// the permuted matrix through one tensor map per chunk instead of a permuted
+// copy), and x2 (K, n) int8 -> fp16 (dst_b); q_out (optional) gets the permuted
+// int8 matrix.  The two are one vector
+// space of 16-element vectors: [0, total_a) the chunks, [total_a, total_a +
+// total_b) x2.  Each warp moves 128 consecutive vectors per step, lane l taking
+// vectors l, l + 32, l + 64 and l + 96, so each of its four 16-byte loads is a
+// coalesced 512 bytes and all four are in flight before the first conversion
+// (one load per thread kept only ~32 KiB in flight per SM, about two thirds of
+// what the HBM latency needs).  h % 16 == 0 and n % 16 == 0.
+__global__ void __launch_bounds__(256) widen_a2a_kernel(const __grid_constant__ ChunkPtrs chunks, int h,
+                                                        int64_t bs_local, int rank_size, __half *__restrict__ dst_a,
+                                                        const int8_t *__restrict__ x2, __half *__restrict__ dst_b,
+                                                        int64_t total_b, int8_t *__restrict__ q_out,
+                                                        int8_t *__restrict__ comm_out) {
+    const int64_t per_chunk = bs_local * h / 16;
+    const int64_t total_a = per_chunk * rank_size;
+    const int64_t total = total_a + total_b;
+    const int lane = threadIdx.x & 31;
+    const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
     const int vpr = h / 16;
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += stride) {
-        const int r = static_cast<int>(i / per_chunk);
-        const int64_t li = i - r * per_chunk;
-        const int4 v = __ldg(reinterpret_cast<const int4 *>(chunks.p[r]) + li);
-        uint4 o[2];
-        i8x16_to_f16x16(v, o);
-        uint4 *d = reinterpret_cast<uint4 *>(dst) + 2 * i;
-        d[0] = o[0];
-        d[1] = o[1];
-        // commOut (rank_size, bs_local, h) is the chunks back to back: vector i
-        if (comm_out) reinterpret_cast<int4 *>(comm_out)[i] = v;
-        if (q_out) {
-            const int64_t t = li / vpr;
-            const int j = static_cast<int>(li - t * vpr) * 16;
-            *reinterpret_cast<int4 *>(q_out + t * (static_cast<int64_t>(rank_size) * h) + r * h + j) = v;
+    for (int64_t base = warp0 * 128; base < total; base += nwarps * 128) {
+        int4 v[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int64_t i = base + 32 * j + lane;
+            if (i < total_a) {
+                const int r = static_cast<int>(i / per_chunk);
+                v[j] = __ldg(reinterpret_cast<const int4 *>(chunks.p[r]) + (i - r * per_chunk));
+            } else if (i < total) {
+                v[j] = __ldg(reinterpret_cast<const int4 *>(x2) + (i - total_a));
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int64_t i = base + 32 * j + lane;
+            if (i >= total) continue;
+            uint4 o[2];
+            i8x16_to_f16x16(v[j], o);
+            if (i < total_a) {
+                uint4 *d = reinterpret_cast<uint4 *>(dst_a) + 2 * i;
+                d[0] = o[0];
+                d[1] = o[1];
+                // commOut (rank_size, bs_local, h) is the chunks back to back: vector i
+                if (comm_out) reinterpret_cast<int4 *>(comm_out)[i] = v[j];
+                if (q_out) {
+                    const int r = static_cast<int>(i / per_chunk);
+                    const int64_t li = i - r * per_chunk;
+                    const int64_t t = li / vpr;
+                    const int c = static_cast<int>(li - t * vpr) * 16;
+                    *reinterpret_cast<int4 *>(q_out + t * (static_cast<int64_t>(rank_size) * h) + r * h + c) = v[j];
+                }
+            } else {
+                uint4 *d = reinterpret_cast<uint4 *>(dst_b) + 2 * (i - total_a);
+                d[0] = o[0];
+                d[1] = o[1];
+            }
         }
     }
+    // the GEMM that follows launches once every CTA got here (see a2a_prologue_kernel)
+    ptx::allow_dependent_launch();
 }
 
 // Permuted int8 chunks -> fp16 GEMM operand (and optionally the int8
@@ -521,11 +554,17 @@ cudaError_t launch_widen_i8(const int8_t *src, __half *dst, int64_t count, int n
     return cudaGetLastError();
 }
 
-cudaError_t launch_widen_chunks_i8(const ChunkPtrs &chunks, int rank_size, int64_t bs_local, int h, __half *dst,
-                                   int8_t *q_out, int8_t *comm_out, int num_sms, cudaStream_t stream) {
-    const int64_t items = bs_local * static_cast<int64_t>(rank_size) * h / 16;
-    widen_chunks_i8_kernel<<<grid_for(items, 256, num_sms), 256, 0, stream>>>(chunks, h, bs_local, rank_size, dst,
-                                                                             q_out, comm_out);
+cudaError_t launch_widen_a2a(const ChunkPtrs &chunks, int rank_size, int64_t bs_local, int h, __half *dst_a,
+                             const int8_t *x2, __half *dst_b, int64_t x2_count, int8_t *q_out, int8_t *comm_out,
+                             int num_sms, cudaStream_t stream) {
+    const int64_t total = bs_local * static_cast<int64_t>(rank_size) * h / 16 + x2_count / 16;
+    // 8 CTAs of 256 threads fill an SM; one warp moves 128 vectors per step
+    int64_t grid = (total + 8 * 128 - 1) / (8 * 128);
+    const int64_t cap = static_cast<int64_t>(num_sms) * 8;
+    if (grid > cap) grid = cap;
+    if (grid < 1) grid = 1;
+    widen_a2a_kernel<<<static_cast<unsigned>(grid), 256, 0, stream>>>(chunks, h, bs_local, rank_size, dst_a, x2, dst_b,
+                                                                      x2_count / 16, q_out, comm_out);
     return cudaGetLastError();
 }
 
