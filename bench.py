@@ -546,6 +546,29 @@ def host_call_us(fn, calls=200):
     return dt / calls * 1e6
 
 
+def c_abi_all_gather_call(s, dev):
+    """A closure that calls mc2_all_gather_mm through the C ABI with every
+    argument marshalled once in advance (no per-call Python wrapper work), for
+    the host-time breakdown of the smallest workload."""
+    import quantized_gemm_rank_gb300 as mc2
+    inp = mc2_inputs.ag_inputs(s, seed=0)
+    keep = [c.to(dev) for c in inp["chunks"]] + [inp["x2"].to(dev)]
+    out = torch.empty((s.m, s.n), dtype=s.dtype, device=dev)
+    g = torch.empty((s.m, s.k), dtype=s.dtype, device=dev)
+    keep += [out, g]
+    ptrs = (ctypes.c_void_p * s.world_size)(*[c.data_ptr() for c in keep[:s.world_size]])
+    L = mc2.lib()
+    code = mc2.MC2_F16 if s.dtype == torch.float16 else mc2.MC2_BF16
+    args = (ptrs, s.world_size, s.m_local, s.k, keep[s.world_size].data_ptr(), s.n, int(s.x2_is_nk), None, code, 1,
+            out.data_ptr(), g.data_ptr(), torch.cuda.current_stream().cuda_stream)
+
+    def call():
+        if L.mc2_all_gather_mm(*args) != 0:
+            raise RuntimeError(mc2.last_error())
+    call.keep = keep
+    return call
+
+
 def extra_table(dev, flush, stream, steps, peaks):
     """Per-workload device times of each call alone (every workload but the
     step's two): the call between the benchmark's events and its GEMM between
@@ -573,6 +596,7 @@ def extra_table(dev, flush, stream, steps, peaks):
                 res[name]["prologue_us"] = [round(statistics.median(x) * 1e3, 2) for x in per[:-1]]
         if name == "ag-tiny":
             res[name]["host_call_us"] = round(host_call_us(fn), 2)
+            res[name]["c_abi_call_us"] = round(host_call_us(c_abi_all_gather_call(s, dev)), 2)
         del fn
         torch.cuda.empty_cache()
     res["int8_context"] = int8_context(dev, flush, stream, steps)

@@ -120,9 +120,17 @@ def _opt(t: Optional[torch.Tensor], what: str) -> Optional[int]:
     return None if t is None else _dev(t, what)
 
 
+_raw_current_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream(stream) -> Optional[int]:
-    s = torch.cuda.current_stream() if stream is None else stream
-    return s.cuda_stream
+    if stream is None:
+        if _raw_current_stream is not None:
+            # the current stream's handle without building a Stream object (a call's
+            # largest single piece of Python-side work)
+            return _raw_current_stream(torch.cuda.current_device())
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
 
 
 def _ptrs(ts: Sequence[torch.Tensor], what: str):

@@ -239,17 +239,18 @@ __device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int 
 
 // Stream-K publication: one more part of this launch (epoch) written for the
 // (tile, cta) flag.  The first publisher of a launch replaces whatever an
-// earlier launch left; the CAS loop only retries while other publishers of
-// the same flag win, so its bound is never reached in practice.
-__device__ __forceinline__ bool sk_publish(unsigned long long *flag, unsigned long long epoch) {
-    unsigned long long cur = *reinterpret_cast<volatile unsigned long long *>(flag);
-    for (int it = 0; it < (1 << 20); ++it) {
-        const unsigned long long want = (cur >> 24) == epoch ? cur + 1 : ((epoch << 24) | 1ull);
-        const unsigned long long prev = atomicCAS(flag, cur, want);
-        if (prev == cur) return true;
-        cur = prev;
+// earlier launch left (one compare-and-swap); every later one, and a first
+// one that lost that race, adds 1 (only this launch's publishers change the
+// flag while it runs, so a failed swap means the flag already holds this
+// epoch).  At most two atomics per publisher: a retry loop of swaps among the
+// eight epilogue warps of a CTA took several microseconds.
+__device__ __forceinline__ void sk_publish(unsigned long long *flag, unsigned long long epoch) {
+    const unsigned long long cur = *reinterpret_cast<volatile unsigned long long *>(flag);
+    if ((cur >> 24) == epoch) {
+        atomicAdd(flag, 1ull);
+        return;
     }
-    return false;
+    if (atomicCAS(flag, cur, (epoch << 24) | 1ull) != cur) atomicAdd(flag, 1ull);
 }
 
 // Slow path of a barrier wait: poll with a wall-clock limit and the CTA's
@@ -332,6 +333,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
     uint64_t *tempty_bar = bars + 3 * S + 2;  // accumulator buffer drained (the leader's counts both CTAs)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 3 * S + 4);
     uint64_t *drain_bar = bars + 3 * S + 5;   // every MMA this CTA issued has completed
+    uint64_t *skr_bar = bars + 3 * S + 6;     // per epilogue warp: its share of a stream-K partial landed
     // the epilogue's output slabs, after the 1 KiB barrier area (1024-byte aligned)
     uint8_t *epi_stage = smem + S * Cfg::kStageBytes + 1024;
     __shared__ int abort_flag_s;
@@ -363,6 +365,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
             ptx::mbar_init(ptx::smem_u32(&tempty_bar[b]), kNumEpiWarps * kG);
         }
         ptx::mbar_init(ptx::smem_u32(drain_bar), 1);
+        for (int e = 0; e < kNumEpiWarps; ++e) ptx::mbar_init(ptx::smem_u32(&skr_bar[e]), 1);
         ptx::fence_mbar_init();
     }
     if (warp == 1) {
@@ -657,6 +660,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
         const int half = (warp - 4) >> 2;     // which 128 of the 256 columns
         const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
         uint32_t acc_iter = 0;
+        uint32_t skr_phase = 0;   // phase of this warp's stream-K partial barrier
         for (int wi = 0; wi < sched.count(); ++wi) {
             const Work w = sched.get(wi);
             int mb, nb;
@@ -664,6 +668,17 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
             const int row = mb * Cfg::kTileM + kBM * static_cast<int>(cr) + 32 * q + lane;
             const int colh = nb * kBN + half * 128;
             bool ok = true;
+            if constexpr (kIntPath) {
+                // This warp's 128 column scales and biases are read only after the tile's
+                // last K block; fetching their lines into L1 now takes those reads (eight
+                // dependent ones per thread) off the tile's critical path.
+                if (lane < 8 && w.kind != WORK_WRITE) {
+                    const int c = min(colh + 16 * lane, p.n - 1);
+                    ptx::prefetch_l1(p.x2_scale + c);
+                    ptx::prefetch_l1(p.bias_q_bf16 ? static_cast<const void *>(static_cast<const uint16_t *>(p.bias_q) + c)
+                                                   : static_cast<const void *>(static_cast<const float *>(p.bias_q) + c));
+                }
+            }
             // Sum of the K blocks: exact int32 (integer path) or fp32 with
             // round-to-nearest adds (float path); one TMEM drain per block.
             using acc_t = typename std::conditional<kIntPath, int32_t, float>::type;
@@ -721,10 +736,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
                             __stcg(slot + j * 32, make_int4(sum[4 * j], sum[4 * j + 1], sum[4 * j + 2], sum[4 * j + 3]));
                         __threadfence();
                         __syncwarp();
-                        if (lane == 0 && !sk_publish(p.sk_flags + w.tile * 2 + cr, p.sk_epoch)) {
-                            *abort_flag = 1;
-                            if (p.status) atomicExch(p.status, -7);
-                        }
+                        if (lane == 0) sk_publish(p.sk_flags + w.tile * 2 + cr, p.sk_epoch);
                         continue;
                     }
                     // FINISH: wait until every epilogue warp of every earlier part has published.
@@ -752,21 +764,53 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
                         ok = false;
                         break;
                     }
-                    __threadfence();
-                    // the earlier parts' sums (exact int32: the order does not matter)
+                    // The earlier parts' sums (exact int32: the order does not matter).  This is
+                    // the unit's last work item and its own MMAs have completed, so the stage
+                    // ring is idle: each writer's share for this warp (16 KiB, contiguous in its
+                    // slot) comes in with one bulk copy into this warp's 16 KiB of the ring, and
+                    // is added from shared memory (one round trip instead of a chain of them).
+                    const uint32_t area = ptx::smem_u32(smem) + static_cast<uint32_t>(warp - 4) * 16384u;
+                    const uint32_t wbar = ptx::smem_u32(&skr_bar[warp - 4]);
+                    if (lane == 0) {
+                        __threadfence();                   // acquire: the writers' data, seen through the flag ...
+                        ptx::fence_proxy_async_global();   // ... before the bulk copies read it
+                    }
+                    bool got_all = true;
                     sched.for_each_writer(w.tile, [&](int u) {
-                        const int4 *slot =
-                            reinterpret_cast<const int4 *>(p.sk_partials + static_cast<size_t>(u * 2 + cr) * kBM * kBN) +
-                            lane_off;
+                        if (!got_all) return;
+                        if (lane == 0) {
+                            ptx::mbar_arrive_expect_tx(wbar, 16384u);
+                            ptx::bulk_load_1d(area,
+                                              reinterpret_cast<const int4 *>(p.sk_partials +
+                                                                             static_cast<size_t>(u * 2 + cr) * kBM * kBN) +
+                                                  static_cast<size_t>(warp - 4) * 32 * 32,
+                                              16384u, wbar);
+                        }
+                        if (!__all_sync(0xffffffffu, ptx::mbar_wait(wbar, skr_phase, p.wait_limit_ns))) {
+                            got_all = false;
+                            return;
+                        }
+                        skr_phase ^= 1u;
+                        const int4 *sv = reinterpret_cast<const int4 *>(smem + static_cast<size_t>(warp - 4) * 16384u);
 #pragma unroll
                         for (int j = 0; j < 32; ++j) {
-                            const int4 v = __ldcg(slot + j * 32);
+                            const int4 v = sv[j * 32 + lane];
                             sum[4 * j] += v.x;
                             sum[4 * j + 1] += v.y;
                             sum[4 * j + 2] += v.z;
                             sum[4 * j + 3] += v.w;
                         }
+                        // the area is read before the next copy overwrites it
+                        __syncwarp();
+                        ptx::fence_proxy_async_smem();
                     });
+                    if (!got_all) {
+                        *abort_flag = 1;
+                        if (p.status && lane == 0) atomicExch(p.status, -7);
+                        ptx::nanosleep(20000);   // a copy still in flight lands before the CTA exits
+                        ok = false;
+                        break;
+                    }
                 }
             }
             const bool row_ok = row < p.m;

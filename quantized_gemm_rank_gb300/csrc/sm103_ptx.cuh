@@ -110,6 +110,11 @@ __device__ __forceinline__ void cluster_sync() {
 
 __device__ __forceinline__ void nanosleep(uint32_t ns) { asm volatile("nanosleep.u32 %0;" ::"r"(ns)); }
 
+// Fetch the line holding `p` into L1 (no register result).
+__device__ __forceinline__ void prefetch_l1(const void *p) {
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)));
+}
+
 // Programmatic dependent launch: a kernel launched with programmatic stream
 // serialisation may start while the previous kernel of the stream is still
 // running; grid_dependency_wait() blocks until that kernel has completed and
@@ -157,6 +162,10 @@ __device__ __forceinline__ void bulk_load_1d(uint32_t dst, const void *src, uint
 // Makes this thread's prior generic-proxy writes to shared memory (an mbarrier
 // initialisation) visible to the async proxy (the bulk copies).
 __device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// Orders this thread's earlier generic-proxy view of global memory (data other
+// threads published and this one acquired) before its later bulk copies read it.
+__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 
 // 3-D tiled load for a CTA pair (see tma_load_2d_pair).
 __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap *m, int32_t c0, int32_t c1,
