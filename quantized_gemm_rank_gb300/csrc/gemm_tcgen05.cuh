@@ -695,18 +695,20 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
                     break;
                 }
                 ptx::tc_fence_after();
+                // 16 columns per TMEM load: with the 128 running sums live, a 32-column
+                // load pushed the epilogue past its registers into local memory
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    if (colh + c * 32 < p.n) {
-                        uint32_t r[32];
-                        ptx::tmem_ld_32x32b_x32(tmem_base + lane_addr + b * kBN + half * 128 + c * 32, r);
+                for (int c = 0; c < 8; ++c) {
+                    if (colh + c * 16 < p.n) {
+                        uint32_t r[16];
+                        ptx::tmem_ld_32x32b_x16(tmem_base + lane_addr + b * kBN + half * 128 + c * 16, r);
                         ptx::tmem_ld_wait();
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) {
+                        for (int i = 0; i < 16; ++i) {
                             if constexpr (kIntPath)
-                                sum[c * 32 + i] += __float2int_rn(__uint_as_float(r[i]));
+                                sum[c * 16 + i] += __float2int_rn(__uint_as_float(r[i]));
                             else
-                                sum[c * 32 + i] = __fadd_rn(sum[c * 32 + i], __uint_as_float(r[i]));
+                                sum[c * 16 + i] = __fadd_rn(sum[c * 16 + i], __uint_as_float(r[i]));
                         }
                     }
                 }
@@ -868,17 +870,18 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
                 for (int c = 0; c < 4; ++c) {
                     const int col0 = colh + c * 32;
                     if (rs_direct && col0 >= p.n) continue;
-                    float v[32];
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] = sum[c * 32 + i];
+                    uint32_t pk[16];
                     if (p.bias16 != nullptr) {
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            v[i] = __fadd_rn(v[i], load16<kBF16>(p.bias16, min(col0 + i, p.n - 1)));
-                    }
-                    uint32_t pk[16];
+                        for (int i = 0; i < 16; ++i)
+                            pk[i] = pack2<kBF16>(
+                                __fadd_rn(sum[c * 32 + 2 * i], load16<kBF16>(p.bias16, min(col0 + 2 * i, p.n - 1))),
+                                __fadd_rn(sum[c * 32 + 2 * i + 1],
+                                          load16<kBF16>(p.bias16, min(col0 + 2 * i + 1, p.n - 1))));
+                    } else {
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) pk[i] = pack2<kBF16>(v[2 * i], v[2 * i + 1]);
+                        for (int i = 0; i < 16; ++i) pk[i] = pack2<kBF16>(sum[c * 32 + 2 * i], sum[c * 32 + 2 * i + 1]);
+                    }
                     put(c, pk);
                 }
             } else {
@@ -889,14 +892,14 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
                     uint32_t pk[16];
                     if (col0 + 32 <= p.n) {
                         // a whole chunk: its column scales and biases by 16-byte read-only
-                        // loads (16-byte aligned: col0 % 32 == 0), 16 columns at a time,
-                        // issued together before the arithmetic
+                        // loads (16-byte aligned: col0 % 32 == 0), 8 columns at a time (with the
+                        // 128 running sums live, a group of 16 left too few registers)
 #pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            const int cg = col0 + 16 * h;
-                            float sc[16], bs[16];
+                        for (int g = 0; g < 4; ++g) {
+                            const int cg = col0 + 8 * g;
+                            float sc[8], bs[8];
 #pragma unroll
-                            for (int q4 = 0; q4 < 4; ++q4) {
+                            for (int q4 = 0; q4 < 2; ++q4) {
                                 const float4 t = __ldg(reinterpret_cast<const float4 *>(p.x2_scale + cg) + q4);
                                 sc[4 * q4] = t.x;
                                 sc[4 * q4 + 1] = t.y;
@@ -904,20 +907,16 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
                                 sc[4 * q4 + 3] = t.w;
                             }
                             if (p.bias_q_bf16) {
+                                const uint4 t = __ldg(reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(p.bias_q) + cg));
+                                const uint32_t w[4] = {t.x, t.y, t.z, t.w};
 #pragma unroll
-                                for (int q8 = 0; q8 < 2; ++q8) {
-                                    const uint4 t = __ldg(
-                                        reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(p.bias_q) + cg) + q8);
-                                    const uint32_t w[4] = {t.x, t.y, t.z, t.w};
-#pragma unroll
-                                    for (int e = 0; e < 4; ++e) {
-                                        bs[8 * q8 + 2 * e] = __uint_as_float(w[e] << 16);
-                                        bs[8 * q8 + 2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
-                                    }
+                                for (int e = 0; e < 4; ++e) {
+                                    bs[2 * e] = __uint_as_float(w[e] << 16);
+                                    bs[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
                                 }
                             } else {
 #pragma unroll
-                                for (int q4 = 0; q4 < 4; ++q4) {
+                                for (int q4 = 0; q4 < 2; ++q4) {
                                     const float4 t =
                                         __ldg(reinterpret_cast<const float4 *>(static_cast<const float *>(p.bias_q) + cg) + q4);
                                     bs[4 * q4] = t.x;
@@ -927,16 +926,16 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
                                 }
                             }
 #pragma unroll
-                            for (int i = 0; i < 16; i += 2) {
+                            for (int i = 0; i < 8; i += 2) {
                                 float o[2];
 #pragma unroll
                                 for (int e = 0; e < 2; ++e) {
-                                    float v = __int2float_rn(sum[c * 32 + 16 * h + i + e]);
+                                    float v = __int2float_rn(sum[c * 32 + 8 * g + i + e]);
                                     v = __fmul_rn(v, s1);
                                     v = __fmul_rn(v, sc[i + e]);
                                     o[e] = __fadd_rn(v, bs[i + e]);
                                 }
-                                pk[8 * h + (i >> 1)] = pack2<true>(o[0], o[1]);
+                                pk[4 * g + (i >> 1)] = pack2<true>(o[0], o[1]);
                             }
                         }
                     } else {
