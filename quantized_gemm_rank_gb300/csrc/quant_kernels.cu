@@ -234,16 +234,18 @@ __global__ void __launch_bounds__(kPrologueThreads) a2a_prologue_kernel(
         const int64_t w = before;
         const int64_t per = (x2_vecs + widen_ctas - 1) / widen_ctas;
         const int64_t end = min(x2_vecs, (w + 1) * per);
-        // four loads in flight per thread before any conversion
-        for (int64_t i0 = w * per + threadIdx.x; i0 < end; i0 += 4 * blockDim.x) {
-            int4 v[4];
+        // two coalesced loads in flight per thread before any conversion, on many
+        // short CTAs (as in widen_a2a_kernel; four per thread measured 2 µs slower on
+        // a2a-dyn and a2a-dyn-small)
+        for (int64_t i0 = w * per + threadIdx.x; i0 < end; i0 += 2 * blockDim.x) {
+            int4 v[2];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
+            for (int u = 0; u < 2; ++u) {
                 const int64_t i = i0 + u * blockDim.x;
                 if (i < end) v[u] = __ldg(reinterpret_cast<const int4 *>(x2) + i);
             }
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
+            for (int u = 0; u < 2; ++u) {
                 const int64_t i = i0 + u * blockDim.x;
                 if (i >= end) break;
                 uint4 o[2];
@@ -351,18 +353,33 @@ __global__ void __launch_bounds__(kPrologueThreads) a2a_prologue_kernel(
     ptx::allow_dependent_launch();
 }
 
-// int8 -> fp16, exact, 16 elements per thread-iteration.
+// int8 -> fp16, exact.  Each warp moves 64 consecutive 16-element vectors per
+// step (two coalesced 16-byte loads per lane in flight), on a large grid (see
+// widen_a2a_kernel); the count % 16 elements past the last vector one by one.
 __global__ void __launch_bounds__(256) widen_i8_kernel(const int8_t *__restrict__ src, __half *__restrict__ dst,
                                                        int64_t count) {
     const int64_t nvec = count / 16;
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < nvec; i += stride) {
-        const int4 v = __ldg(reinterpret_cast<const int4 *>(src) + i);
-        uint4 o[2];
-        i8x16_to_f16x16(v, o);
-        reinterpret_cast<uint4 *>(dst)[2 * i] = o[0];
-        reinterpret_cast<uint4 *>(dst)[2 * i + 1] = o[1];
+    const int lane = threadIdx.x & 31;
+    const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    for (int64_t base = warp0 * 64; base < nvec; base += nwarps * 64) {
+        int4 v[2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int64_t i = base + 32 * j + lane;
+            if (i < nvec) v[j] = __ldg(reinterpret_cast<const int4 *>(src) + i);
+        }
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int64_t i = base + 32 * j + lane;
+            if (i >= nvec) continue;
+            uint4 o[2];
+            i8x16_to_f16x16(v[j], o);
+            reinterpret_cast<uint4 *>(dst)[2 * i] = o[0];
+            reinterpret_cast<uint4 *>(dst)[2 * i + 1] = o[1];
+        }
     }
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     for (int64_t i = nvec * 16 + static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < count; i += stride)
         dst[i] = __int2half_rn(src[i]);
     // the GEMM that follows launches once every CTA got here (see a2a_prologue_kernel)
@@ -375,11 +392,12 @@ __global__ void __launch_bounds__(256) widen_i8_kernel(const int8_t *__restrict_
 // copy), and x2 (K, n) int8 -> fp16 (dst_b); q_out (optional) gets the permuted
 // int8 matrix.  The two are one vector
 // space of 16-element vectors: [0, total_a) the chunks, [total_a, total_a +
-// total_b) x2.  Each warp moves 128 consecutive vectors per step, lane l taking
-// vectors l, l + 32, l + 64 and l + 96, so each of its four 16-byte loads is a
-// coalesced 512 bytes and all four are in flight before the first conversion
-// (one load per thread kept only ~32 KiB in flight per SM, about two thirds of
-// what the HBM latency needs).  h % 16 == 0 and n % 16 == 0.
+// total_b) x2.  Each warp moves 64 consecutive vectors per step, lane l taking
+// vectors l and l + 32, so each 16-byte load is a coalesced 512 bytes and both
+// are in flight before the first conversion, and the grid is large (up to 128
+// CTAs per SM, most of them one step long).  On a2a-full that measured 376 µs
+// (90% of the copy rate) against 537 µs for four vectors per lane on a grid of
+// 8 CTAs per SM and 464–471 µs for other mixes.  h % 16 == 0 and n % 16 == 0.
 __global__ void __launch_bounds__(256) widen_a2a_kernel(const __grid_constant__ ChunkPtrs chunks, int h,
                                                         int64_t bs_local, int rank_size, __half *__restrict__ dst_a,
                                                         const int8_t *__restrict__ x2, __half *__restrict__ dst_b,
@@ -392,10 +410,10 @@ __global__ void __launch_bounds__(256) widen_a2a_kernel(const __grid_constant__ 
     const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
     const int vpr = h / 16;
-    for (int64_t base = warp0 * 128; base < total; base += nwarps * 128) {
-        int4 v[4];
+    for (int64_t base = warp0 * 64; base < total; base += nwarps * 64) {
+        int4 v[2];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int j = 0; j < 2; ++j) {
             const int64_t i = base + 32 * j + lane;
             if (i < total_a) {
                 const int r = static_cast<int>(i / per_chunk);
@@ -405,7 +423,7 @@ __global__ void __launch_bounds__(256) widen_a2a_kernel(const __grid_constant__ 
             }
         }
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int j = 0; j < 2; ++j) {
             const int64_t i = base + 32 * j + lane;
             if (i >= total) continue;
             uint4 o[2];
@@ -516,7 +534,7 @@ cudaError_t launch_a2a_prologue(const ChunkPtrs &chunks, int rank_size, int64_t 
     const size_t smem = static_cast<size_t>(K) * 2 + 16;
     // one quant CTA per row; widen CTAs for ~4 vectors per thread
     const int64_t x2_vecs = x2_count / 16;
-    int64_t widen_ctas = (x2_vecs + 4ll * threads - 1) / (4ll * threads);
+    int64_t widen_ctas = (x2_vecs + 2ll * threads - 1) / (2ll * threads);
     if (widen_ctas < 1) widen_ctas = 1;
     if (widen_ctas > (1ll << 30)) widen_ctas = 1ll << 30;
     const int64_t grid = bs_local + widen_ctas;
@@ -550,7 +568,12 @@ cudaError_t launch_a2a_prologue(const ChunkPtrs &chunks, int rank_size, int64_t 
 }
 
 cudaError_t launch_widen_i8(const int8_t *src, __half *dst, int64_t count, int num_sms, cudaStream_t stream) {
-    widen_i8_kernel<<<grid_for(count / 16 + 1, 256, num_sms), 256, 0, stream>>>(src, dst, count);
+    // one step of 8 warps x 64 vectors per CTA, up to 128 CTAs per SM
+    int64_t grid = (count / 16 + 8 * 64 - 1) / (8 * 64);
+    const int64_t cap = static_cast<int64_t>(num_sms) * 128;
+    if (grid > cap) grid = cap;
+    if (grid < 1) grid = 1;
+    widen_i8_kernel<<<static_cast<unsigned>(grid), 256, 0, stream>>>(src, dst, count);
     return cudaGetLastError();
 }
 
@@ -558,9 +581,9 @@ cudaError_t launch_widen_a2a(const ChunkPtrs &chunks, int rank_size, int64_t bs_
                              const int8_t *x2, __half *dst_b, int64_t x2_count, int8_t *q_out, int8_t *comm_out,
                              int num_sms, cudaStream_t stream) {
     const int64_t total = bs_local * static_cast<int64_t>(rank_size) * h / 16 + x2_count / 16;
-    // 8 CTAs of 256 threads fill an SM; one warp moves 128 vectors per step
-    int64_t grid = (total + 8 * 128 - 1) / (8 * 128);
-    const int64_t cap = static_cast<int64_t>(num_sms) * 8;
+    // one step of 8 warps x 64 vectors per CTA, up to 128 CTAs per SM
+    int64_t grid = (total + 8 * 64 - 1) / (8 * 64);
+    const int64_t cap = static_cast<int64_t>(num_sms) * 128;
     if (grid > cap) grid = cap;
     if (grid < 1) grid = 1;
     widen_a2a_kernel<<<static_cast<unsigned>(grid), 256, 0, stream>>>(chunks, h, bs_local, rank_size, dst_a, x2, dst_b,
