@@ -889,6 +889,22 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     const int col0 = colh + c * 32;
+                    // the exact sums first (debug output): stored after the dequant, they
+                    // stayed live across it and pushed the epilogue into local memory
+                    if (p.acc_out != nullptr && row_ok && col0 < p.n) {
+                        int32_t *dst = p.acc_out + static_cast<int64_t>(row) * p.n + col0;
+                        if (col0 + 32 <= p.n) {
+#pragma unroll
+                            for (int j = 0; j < 8; ++j)
+                                reinterpret_cast<int4 *>(dst)[j] =
+                                    make_int4(sum[c * 32 + 4 * j], sum[c * 32 + 4 * j + 1], sum[c * 32 + 4 * j + 2],
+                                              sum[c * 32 + 4 * j + 3]);
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i)
+                                if (col0 + i < p.n) dst[i] = sum[c * 32 + i];
+                        }
+                    }
                     uint32_t pk[16];
                     if (col0 + 32 <= p.n) {
                         // a whole chunk: its column scales and biases by 16-byte read-only
@@ -957,20 +973,6 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
                         }
                     }
                     put(c, pk);
-                    if (p.acc_out != nullptr && row_ok && col0 < p.n) {
-                        int32_t *dst = p.acc_out + static_cast<int64_t>(row) * p.n + col0;
-                        if (col0 + 32 <= p.n) {
-#pragma unroll
-                            for (int j = 0; j < 8; ++j)
-                                reinterpret_cast<int4 *>(dst)[j] =
-                                    make_int4(sum[c * 32 + 4 * j], sum[c * 32 + 4 * j + 1], sum[c * 32 + 4 * j + 2],
-                                              sum[c * 32 + 4 * j + 3]);
-                        } else {
-#pragma unroll
-                            for (int i = 0; i < 32; ++i)
-                                if (col0 + i < p.n) dst[i] = sum[c * 32 + i];
-                        }
-                    }
                 }
             }
         }
