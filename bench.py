@@ -329,48 +329,63 @@ def _arena(tensors, device):
 def time_e2e(step: Step, steps, warmup, dev):
     """Same step through the public calls with HOST buffers: every step copies all
     of its inputs from pinned host memory to the device and all of its outputs
-    back.  A step's inputs sit back to back in one pinned buffer (and its
-    outputs in another), as a caller streaming batches would stage them, so
-    each direction is one copy per step.  Three device buffer sets and three
-    streams (upload, compute, download) ordered by events let step i+1's upload
-    and step i-1's download run while step i computes."""
+    back.  A step's inputs sit back to back in one pinned buffer (the
+    all-gather's first, then the all-to-all's) and its outputs in another, as a
+    caller streaming batches would stage them; each direction is two copies per
+    step, one per operation, so the all-gather computes as soon as its own
+    inputs have landed and its outputs leave while the all-to-all computes.
+    Three device buffer sets and three streams (upload, compute, download),
+    ordered by events, let step i+1's upload and step i-1's download run while
+    step i computes.  The timed region is the whole job of `steps` steps, from
+    the first upload to the last download."""
     ag_t, a2a_t = _ag_host_tensors(step.host["ag"]), _a2a_host_tensors(step.host["a2a"])
     host_in = ag_t + a2a_t
     h_in_buf, h_in = _arena(host_in, torch.device("cpu"))
     for v, t in zip(h_in, host_in):
         v.copy_(t)
+    split_in = h_in[len(ag_t)].data_ptr() - h_in_buf.data_ptr()   # first byte of the all-to-all's inputs
     nsets = 3
     sets = [step] + [Step(dev, step.ag_s, step.a2a_s, host=step.host) for _ in range(nsets - 1)]
     d_in_bufs, d_out_bufs, h_out_bufs = [], [], []
+    split_out = 0
     for st in sets:
         buf, v = _arena(host_in, dev)
         st.set_inputs(v[:len(ag_t)], v[len(ag_t):])
         d_in_bufs.append(buf)
         obuf, ov = _arena(st.outputs(), dev)
         st.set_outputs(ov)
+        split_out = ov[-1].data_ptr() - obuf.data_ptr()   # first byte of the all-to-all's output
         d_out_bufs.append(obuf)
         h_out_bufs.append(_arena(st.outputs(), torch.device("cpu"))[0])
     h2d = h_in_buf.numel()
     d2h = h_out_bufs[0].numel()
     up, comp, down = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
-    ev = [{k: torch.cuda.Event() for k in ("up", "comp", "down")} for _ in sets]
+    names = ("up_ag", "up", "comp_ag", "comp", "down")
+    ev = [{k: torch.cuda.Event() for k in names} for _ in sets]
 
     def one(i):
         b = i % nsets
         st, e = sets[b], ev[b]
         up.wait_event(e["comp"])           # step i-3 has finished reading this set's inputs
         with torch.cuda.stream(up):
-            d_in_bufs[b].copy_(h_in_buf, non_blocking=True)
-        e["up"].record(up)
-        comp.wait_event(e["up"])
+            d_in_bufs[b][:split_in].copy_(h_in_buf[:split_in], non_blocking=True)
+            e["up_ag"].record(up)
+            d_in_bufs[b][split_in:].copy_(h_in_buf[split_in:], non_blocking=True)
+            e["up"].record(up)
+        comp.wait_event(e["up_ag"])
         comp.wait_event(e["down"])         # step i-3's outputs of this set are on the host
         with torch.cuda.stream(comp):
-            st.run()
-        e["comp"].record(comp)
-        down.wait_event(e["comp"])
+            st.run_ag()
+            e["comp_ag"].record(comp)
+            comp.wait_event(e["up"])
+            st.run_a2a()
+            e["comp"].record(comp)
+        down.wait_event(e["comp_ag"])
         with torch.cuda.stream(down):
-            h_out_bufs[b].copy_(d_out_bufs[b], non_blocking=True)
-        e["down"].record(down)
+            h_out_bufs[b][:split_out].copy_(d_out_bufs[b][:split_out], non_blocking=True)
+            down.wait_event(e["comp"])
+            h_out_bufs[b][split_out:].copy_(d_out_bufs[b][split_out:], non_blocking=True)
+            e["down"].record(down)
 
     for i in range(warmup):
         one(i)
@@ -776,7 +791,7 @@ def main():
     if args.profile:
         e2e_ms, h2d, d2h = float("nan"), 0, 0
     else:
-        e2e_ms, h2d, d2h = time_e2e(step, max(10, args.steps // 2), 3, dev)
+        e2e_ms, h2d, d2h = time_e2e(step, args.steps, 3, dev)
         e2e_ms = max_over_ranks(e2e_ms, world)
     e2e_value = None if args.profile else round(job_tflops(step.flops, world, e2e_ms), 2)
 
