@@ -311,6 +311,16 @@ def time_launches(fn, nlaunch, steps, warmup, flush, stream):
     return per
 
 
+def _arena_views(buf, tensors):
+    """Views of `buf` laid out as _arena lays out tensors shaped like `tensors`."""
+    views, off = [], 0
+    for t in tensors:
+        n = t.numel() * t.element_size()
+        views.append(buf[off:off + n].view(t.dtype).view(t.shape))
+        off += (n + 255) // 256 * 256
+    return views
+
+
 def _arena(tensors, device):
     """One flat buffer holding tensors shaped like `tensors` back to back (offsets
     rounded up to 256 bytes; pinned when on the host) and the views of it."""
@@ -326,7 +336,7 @@ def _arena(tensors, device):
     return buf, views
 
 
-def time_e2e(step: Step, steps, warmup, dev):
+def time_e2e(step: Step, steps, warmup, dev, return_outputs=False):
     """Same step through the public calls with HOST buffers: every step copies all
     of its inputs from pinned host memory to the device and all of its outputs
     back.  A step's inputs sit back to back in one pinned buffer (the
@@ -337,7 +347,8 @@ def time_e2e(step: Step, steps, warmup, dev):
     Three device buffer sets and three streams (upload, compute, download),
     ordered by events, let step i+1's upload and step i-1's download run while
     step i computes.  The timed region is the whole job of `steps` steps, from
-    the first upload to the last download."""
+    the first upload to the last download.  With return_outputs, the host copies
+    of the last step's outputs (in Step.outputs() order) come back as well."""
     ag_t, a2a_t = _ag_host_tensors(step.host["ag"]), _a2a_host_tensors(step.host["a2a"])
     host_in = ag_t + a2a_t
     h_in_buf, h_in = _arena(host_in, torch.device("cpu"))
@@ -400,8 +411,14 @@ def time_e2e(step: Step, steps, warmup, dev):
     t1.record(up)
     t1.synchronize()
     ms = t0.elapsed_time(t1) / steps
+    outs = None
+    if return_outputs:
+        last = (steps - 1) % nsets
+        outs = [o.clone() for o in _arena_views(h_out_bufs[last], sets[last].outputs())]
     del sets, d_in_bufs, d_out_bufs, h_out_bufs
     torch.cuda.empty_cache()
+    if return_outputs:
+        return ms, h2d, d2h, outs
     return ms, h2d, d2h
 
 
