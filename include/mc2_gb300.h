@@ -11,7 +11,10 @@
  * Conventions shared by every call
  *   - Every tensor is a DEVICE pointer, row-major and contiguous, owned by the
  *     caller.  Arrays of per-rank pointers (x_chunks, chunks) are HOST arrays
- *     of device pointers.
+ *     of device pointers.  Every device pointer must address memory of the
+ *     CUDA device current on the calling thread, and `stream` must belong to
+ *     that device: the library launches there and does not look up where a
+ *     pointer lives (that would be a driver query per pointer per call).
  *   - Work is enqueued on `stream` (a cudaStream_t passed as void*; NULL is the
  *     legacy default stream) and the call returns without synchronising.  The
  *     library never allocates device memory: scratch space is the caller's

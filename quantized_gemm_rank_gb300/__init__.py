@@ -108,33 +108,43 @@ def _dtype_code(dt: torch.dtype) -> int:
     return {torch.float16: MC2_F16, torch.bfloat16: MC2_BF16, torch.float32: MC2_F32, torch.int8: MC2_I8}[dt]
 
 
-def _dev(t: torch.Tensor, what: str) -> int:
-    if not t.is_cuda:
-        raise ValueError(f"{what} must be a CUDA tensor")
+def _current_device() -> int:
+    """The CUDA device the library launches on, or -1 without CUDA."""
+    return torch.cuda.current_device() if torch.cuda.is_available() else -1
+
+
+def _dev(t: torch.Tensor, what: str, cur: int) -> int:
+    # the library launches on the current device: a tensor elsewhere would reach
+    # its kernels as a foreign pointer
+    if cur < 0 or t.get_device() != cur:
+        where = "a CUDA device (none is available)" if cur < 0 else f"the current device (cuda:{cur})"
+        raise ValueError(f"{what} must be a CUDA tensor on {where}")
     if not t.is_contiguous():
         raise ValueError(f"{what} must be contiguous")
     return t.data_ptr()
 
 
-def _opt(t: Optional[torch.Tensor], what: str) -> Optional[int]:
-    return None if t is None else _dev(t, what)
+def _opt(t: Optional[torch.Tensor], what: str, cur: int) -> Optional[int]:
+    return None if t is None else _dev(t, what, cur)
 
 
 _raw_current_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
 
 
-def _stream(stream) -> Optional[int]:
+def _stream(stream, cur: int) -> Optional[int]:
     if stream is None:
         if _raw_current_stream is not None:
             # the current stream's handle without building a Stream object (a call's
             # largest single piece of Python-side work)
-            return _raw_current_stream(torch.cuda.current_device())
+            return _raw_current_stream(cur)
         stream = torch.cuda.current_stream()
+    elif stream.device_index != cur:
+        raise ValueError(f"stream must belong to the current device (cuda:{cur})")
     return stream.cuda_stream
 
 
-def _ptrs(ts: Sequence[torch.Tensor], what: str):
-    return (ctypes.c_void_p * len(ts))(*[_dev(t, f"{what}[{i}]") for i, t in enumerate(ts)])
+def _ptrs(ts: Sequence[torch.Tensor], what: str, cur: int):
+    return (ctypes.c_void_p * len(ts))(*[_dev(t, f"{what}[{i}]", cur) for i, t in enumerate(ts)])
 
 
 def mc2_all_gather_mm(x_chunks: Sequence[torch.Tensor], x2: torch.Tensor, *, x2_is_nk: bool = False,
@@ -146,6 +156,7 @@ def mc2_all_gather_mm(x_chunks: Sequence[torch.Tensor], x2: torch.Tensor, *, x2_
     x_chunks: world_size tensors (m_local, k); x2 (k, n), or w (n, k) with
     ``x2_is_nk``.  Returns (out (m, n), gathered (m, k) or None).
     """
+    cur = _current_device()
     R = len(x_chunks)
     m_local, k = x_chunks[0].shape
     n = x2.shape[0] if x2_is_nk else x2.shape[1]
@@ -154,10 +165,10 @@ def mc2_all_gather_mm(x_chunks: Sequence[torch.Tensor], x2: torch.Tensor, *, x2_
         out = torch.empty((R * m_local, n), dtype=dt, device=x_chunks[0].device)
     if gather_output and gathered is None:
         gathered = torch.empty((R * m_local, k), dtype=dt, device=x_chunks[0].device)
-    ptrs = _ptrs(x_chunks, "x_chunks")
-    st = lib().mc2_all_gather_mm(ptrs, R, m_local, k, _dev(x2, "x2"), n, int(x2_is_nk), _opt(bias, "bias"),
-                                 _dtype_code(dt), int(gather_output), _dev(out, "out"),
-                                 _opt(gathered, "gathered") if gather_output else None, _stream(stream))
+    ptrs = _ptrs(x_chunks, "x_chunks", cur)
+    st = lib().mc2_all_gather_mm(ptrs, R, m_local, k, _dev(x2, "x2", cur), n, int(x2_is_nk), _opt(bias, "bias", cur),
+                                 _dtype_code(dt), int(gather_output), _dev(out, "out", cur),
+                                 _opt(gathered, "gathered", cur) if gather_output else None, _stream(stream, cur))
     _check(st)
     return out, (gathered if gather_output else None)
 
@@ -171,15 +182,16 @@ def mc2_matmul_reduce_scatter(x_chunks: Sequence[torch.Tensor], w_chunks: Sequen
     (n, k_local) (or (k_local, n) with ``w_is_nk=False``).  Returns the list of
     the ranks' outputs, each (m / world_size, n).
     """
+    cur = _current_device()
     R = len(x_chunks)
     m, k_local = x_chunks[0].shape
     n = w_chunks[0].shape[0] if w_is_nk else w_chunks[0].shape[1]
     dt = x_chunks[0].dtype
     if out_chunks is None:
         out_chunks = [torch.empty((m // R, n), dtype=dt, device=x_chunks[0].device) for _ in range(R)]
-    st = lib().mc2_matmul_reduce_scatter(_ptrs(x_chunks, "x_chunks"), _ptrs(w_chunks, "w_chunks"), R, m, k_local, n,
-                                         int(w_is_nk), _opt(bias, "bias"), _dtype_code(dt),
-                                         _ptrs(out_chunks, "out_chunks"), _stream(stream))
+    st = lib().mc2_matmul_reduce_scatter(_ptrs(x_chunks, "x_chunks", cur), _ptrs(w_chunks, "w_chunks", cur), R, m, k_local, n,
+                                         int(w_is_nk), _opt(bias, "bias", cur), _dtype_code(dt),
+                                         _ptrs(out_chunks, "out_chunks", cur), _stream(stream, cur))
     _check(st)
     return list(out_chunks)
 
@@ -191,14 +203,15 @@ def mc2_matmul_weight_grad(dy: torch.Tensor, x: torch.Tensor, *, with_bias: bool
     dy (m, n) and x (m, k) of one 16-bit type on this GPU (for the all-gather
     layer, x is the ``gathered`` output of its forward call).  Returns (dw, db).
     """
+    cur = _current_device()
     m, n = dy.shape
     k = x.shape[1]
     if dw is None:
         dw = torch.empty((n, k), dtype=dy.dtype, device=dy.device)
     if with_bias and db is None:
         db = torch.empty((n,), dtype=dy.dtype, device=dy.device)
-    st = lib().mc2_matmul_weight_grad(_dev(dy, "dy"), m, n, _dev(x, "x"), k, _dtype_code(dy.dtype), _dev(dw, "dw"),
-                                      _opt(db if with_bias else None, "db"), _stream(stream))
+    st = lib().mc2_matmul_weight_grad(_dev(dy, "dy", cur), m, n, _dev(x, "x", cur), k, _dtype_code(dy.dtype), _dev(dw, "dw", cur),
+                                      _opt(db if with_bias else None, "db", cur), _stream(stream, cur))
     _check(st)
     return dw, (db if with_bias else None)
 
@@ -218,6 +231,7 @@ def mc2_quant_all_reduce(x_chunks: Sequence[torch.Tensor], scale_chunks: Sequenc
     codes (bs, h/64, 2) as uint8 (mx).  Returns out of the same leading shape
     as x in ``out_dtype`` (fp32, fp16 or bf16).
     """
+    cur = _current_device()
     x0 = x_chunks[0]
     if x_kind is None:
         if x0.dtype not in _QAR_X_BY_DTYPE:
@@ -229,9 +243,9 @@ def mc2_quant_all_reduce(x_chunks: Sequence[torch.Tensor], scale_chunks: Sequenc
     sdt = MC2_F32 if s0.dtype == torch.float32 else MC2_E8M0
     if out is None:
         out = torch.empty(x0.shape, dtype=out_dtype, device=x0.device)
-    st = lib().mc2_quant_all_reduce(_ptrs(x_chunks, "x_chunks"), _ptrs(scale_chunks, "scale_chunks"),
+    st = lib().mc2_quant_all_reduce(_ptrs(x_chunks, "x_chunks", cur), _ptrs(scale_chunks, "scale_chunks", cur),
                                     len(x_chunks), bs, h, _QAR_X[x_kind], sdt, _dtype_code(out.dtype),
-                                    _dev(out, "out"), _stream(stream))
+                                    _dev(out, "out", cur), _stream(stream, cur))
     _check(st)
     return out
 
@@ -259,6 +273,7 @@ def mc2_alltoall_quant_mm(chunks: Sequence[torch.Tensor], x2: torch.Tensor, x2_s
     Returns dict(out, q, x1_scale, acc, alltoall_out) with the optional outputs
     that were given.
     """
+    cur = _current_device()
     R = len(chunks)
     bs_local, h = chunks[0].shape
     n = x2.shape[1]
@@ -269,14 +284,14 @@ def mc2_alltoall_quant_mm(chunks: Sequence[torch.Tensor], x2: torch.Tensor, x2_s
     if workspace is None:
         need = mc2_alltoall_quant_mm_workspace(R, bs_local, h, n, x1_quant_mode, x1_dtype)
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
-    ptrs = _ptrs(chunks, "chunks")
-    st = lib().mc2_alltoall_quant_mm(ptrs, R, bs_local, h, _dtype_code(x1_dtype), _opt(x1_scale, "x1_scale"),
-                                     _dev(x2, "x2"), _dev(x2_scale, "x2_scale"), _dev(bias, "bias"),
-                                     _dtype_code(bias.dtype), x1_quant_mode, x2_quant_mode, n, _dev(out, "out"),
-                                     _opt(alltoall_out, "alltoall_out"), _opt(q_out, "q_out"),
-                                     _opt(x1_scale_out, "x1_scale_out"), _opt(acc_out, "acc_out"),
-                                     _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
-                                     _stream(stream))
+    ptrs = _ptrs(chunks, "chunks", cur)
+    st = lib().mc2_alltoall_quant_mm(ptrs, R, bs_local, h, _dtype_code(x1_dtype), _opt(x1_scale, "x1_scale", cur),
+                                     _dev(x2, "x2", cur), _dev(x2_scale, "x2_scale", cur), _dev(bias, "bias", cur),
+                                     _dtype_code(bias.dtype), x1_quant_mode, x2_quant_mode, n, _dev(out, "out", cur),
+                                     _opt(alltoall_out, "alltoall_out", cur), _opt(q_out, "q_out", cur),
+                                     _opt(x1_scale_out, "x1_scale_out", cur), _opt(acc_out, "acc_out", cur),
+                                     _dev(workspace, "workspace", cur), workspace.numel() * workspace.element_size(),
+                                     _stream(stream, cur))
     _check(st)
     return {"out": out, "q": q_out, "x1_scale": x1_scale_out, "acc": acc_out, "alltoall_out": alltoall_out}
 
@@ -298,16 +313,17 @@ def mc2_alltoall_quant_mm_no_alloc(chunks: Sequence[torch.Tensor], x2: torch.Ten
     allocated here).  Calls that may overlap on the GPU share that scratch and
     must be serialised by the caller.
     """
+    cur = _current_device()
     R = len(chunks)
     bs_local, h = chunks[0].shape
     n = x2.shape[1]
-    ptrs = _ptrs(chunks, "chunks")
+    ptrs = _ptrs(chunks, "chunks", cur)
     st = lib().mc2_alltoall_quant_mm_no_alloc(ptrs, R, bs_local, h, _dtype_code(chunks[0].dtype),
-                                              _opt(x1_scale, "x1_scale"), _dev(x2, "x2"), _dev(x2_scale, "x2_scale"),
-                                              _dev(bias, "bias"), _dtype_code(bias.dtype), x1_quant_mode,
-                                              x2_quant_mode, n, _dev(out, "out"), _opt(alltoall_out, "alltoall_out"),
-                                              _opt(q_out, "q_out"), _opt(x1_scale_out, "x1_scale_out"),
-                                              _opt(acc_out, "acc_out"), _stream(stream))
+                                              _opt(x1_scale, "x1_scale", cur), _dev(x2, "x2", cur), _dev(x2_scale, "x2_scale", cur),
+                                              _dev(bias, "bias", cur), _dtype_code(bias.dtype), x1_quant_mode,
+                                              x2_quant_mode, n, _dev(out, "out", cur), _opt(alltoall_out, "alltoall_out", cur),
+                                              _opt(q_out, "q_out", cur), _opt(x1_scale_out, "x1_scale_out", cur),
+                                              _opt(acc_out, "acc_out", cur), _stream(stream, cur))
     _check(st)
     return {"out": out, "q": q_out, "x1_scale": x1_scale_out, "acc": acc_out, "alltoall_out": alltoall_out}
 

@@ -166,3 +166,15 @@ def test_several_k_blocks_integer_valued_bit_exact(x2_is_nk):
     ref, ref_g = oracle.all_gather_mm(chunks, x2, x2_is_nk=x2_is_nk)
     assert_bits_equal(out, ref, "out")
     assert_bits_equal(gathered, ref_g, "gathered")
+
+
+def test_binding_refuses_a_host_tensor_among_device_ones():
+    """The library launches on the current device; the binding refuses any
+    operand that lives elsewhere (here x2 on the host) before calling it."""
+    dev = torch.device("cuda")
+    x = [torch.zeros(16, 256, dtype=torch.bfloat16, device=dev)] * 2
+    with pytest.raises(ValueError, match="x2 must be a CUDA tensor on the current device"):
+        mc2.mc2_all_gather_mm(x, torch.zeros(256, 64, dtype=torch.bfloat16))
+    with pytest.raises(ValueError, match="out must be a CUDA tensor"):
+        mc2.mc2_all_gather_mm(x, torch.zeros(256, 64, dtype=torch.bfloat16, device=dev),
+                              out=torch.zeros(32, 64, dtype=torch.bfloat16))
