@@ -88,10 +88,10 @@ unsigned long long next_sk_epoch() {
     return kLo + counter.fetch_add(1, std::memory_order_relaxed) % kSpan;
 }
 
-template <int kG, bool kBF16, bool kIntPath, bool kRS = false>
+template <int kG, bool kBF16, bool kIntPath, bool kRS = false, bool kDyn = false>
 cudaError_t launch_one(const GemmParams &p_in, int num_sms, cudaStream_t stream) {
     using Cfg = TileCfg<kG, true>;
-    auto kern = mc2_gemm_kernel<kG, kBF16, kIntPath, kRS>;
+    auto kern = mc2_gemm_kernel<kG, kBF16, kIntPath, kRS, kDyn>;
     GemmParams p = p_in;
     // once per host thread and context (a device switch or reset makes a new
     // context): the status word's address and the shared-memory opt-in
@@ -128,9 +128,14 @@ cudaError_t launch_one(const GemmParams &p_in, int num_sms, cudaStream_t stream)
         attr[1].val.clusterDim.y = 1;
         attr[1].val.clusterDim.z = 1;
         cfg.numAttrs = 2;
-        const int clusters = concurrent_pairs<kBF16, kIntPath, kRS>(num_sms);
-        // with a stream-K tail every co-resident pair takes part
-        const int grid_clusters = (p.sk_tiles > 0 || num_tiles >= clusters) ? clusters : num_tiles;
+        // run-time tiles: one pair per tile (the running pairs cancel the launches of
+        // the rest); otherwise persistent, and with a stream-K tail every co-resident
+        // pair takes part
+        int grid_clusters = num_tiles;
+        if constexpr (!kDyn) {
+            const int clusters = concurrent_pairs<kBF16, kIntPath, kRS>(num_sms);
+            grid_clusters = (p.sk_tiles > 0 || num_tiles >= clusters) ? clusters : num_tiles;
+        }
         cfg.gridDim = dim3(2 * grid_clusters, 1, 1);
     } else {
         const int units = p.sk_tiles > 0 ? num_sms : (num_tiles < num_sms ? num_tiles : num_sms);
@@ -158,9 +163,12 @@ int gemm_units(GemmKind kind, int group, int num_sms) {
 
 cudaError_t launch_gemm(GemmKind kind, int group, const GemmParams &p, int num_sms, cudaStream_t stream) {
     if (group == 2) {
+        // the plain float GEMM takes its tiles at run time (cluster launch control): on
+        // the 28-tile-wide all-gather the slowest persistent pairs had set the time; the
+        // reduce-scatter measured no better that way and stays persistent
         switch (kind) {
-            case GEMM_F16: return launch_one<2, false, false>(p, num_sms, stream);
-            case GEMM_BF16: return launch_one<2, true, false>(p, num_sms, stream);
+            case GEMM_F16: return launch_one<2, false, false, false, true>(p, num_sms, stream);
+            case GEMM_BF16: return launch_one<2, true, false, false, true>(p, num_sms, stream);
             case GEMM_INT_AS_F16: return launch_one<2, false, true>(p, num_sms, stream);
             case GEMM_RS_F16: return launch_one<2, false, false, true>(p, num_sms, stream);
             case GEMM_RS_BF16: return launch_one<2, true, false, true>(p, num_sms, stream);

@@ -24,6 +24,13 @@
 //           tcgen05.mma.cta_group::2 M=256 N=256 issued by the leader CTA;
 //           each CTA loads its own 128 rows of A and 128 rows of B (half the
 //           B traffic per CTA of kG = 1), 6-stage ring of 32 KiB stages.
+// Tile order (template parameter kDyn):
+//   false   persistent: the grid is the co-resident pairs (or CTAs), unit c takes
+//           tiles c, c + U, ...; on the integer path the last partial wave is
+//           split by K blocks over all units (stream-K, see the Schedule)
+//   true    one pair launched per tile; a running pair takes over the tile of a
+//           pair that has not launched yet (cluster launch control), so pairs
+//           that run faster take more tiles (the plain float GEMM)
 // 16-bit operands live in 128-byte-swizzled shared memory; accumulators are
 // two 256-column fp32 TMEM buffers per CTA so the epilogue of one K block (or
 // tile) overlaps the MMAs of the next.
@@ -281,6 +288,54 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, con
     return wait_slow<kCluster>(bar, parity, p.wait_limit_ns, p.status, abort_flag);
 }
 
+// The work items of one role, in order: the static schedule, or (kDyn) the
+// tiles this CTA pair obtains at run time with cluster launch control: its own
+// tile first, then each tile whose pair it cancels before that pair launched.
+// The leader CTA's producer asks for the next tile when it starts a tile; the
+// answer lands in a two-slot ring in both CTAs, and every role of both CTAs
+// reads it there when it finishes that tile, then releases the slot on the
+// leader's barrier (one release per role).
+template <bool kDyn>
+struct TileWalk {
+    const Schedule *sched;
+    int wi;            // static: next schedule index
+    int tile;          // dynamic: the current tile, -1 before the first
+    int first_tile;    // dynamic: this pair's own tile
+    int reads;         // dynamic: answers read so far
+    int num_k;
+    uint32_t resp0;    // dynamic: the ring's answers (this CTA)
+    uint32_t full0;    // dynamic: the ring's arrival barriers (this CTA)
+    uint32_t free0;    // dynamic: the ring's release barriers (the leader's, cluster address)
+    bool releaser;     // this thread releases the slot for its role
+
+    template <bool kPair>
+    __device__ __forceinline__ bool next(Work &w, const GemmParams &p, volatile int *abort_flag) {
+        if constexpr (!kDyn) {
+            if (wi >= sched->count()) return false;
+            w = sched->get(wi++);
+            return true;
+        } else {
+            if (tile < 0) {
+                tile = first_tile;
+                w = Work{tile, 0, (num_k + p.kblock_tiles - 1) / p.kblock_tiles, WORK_FULL};
+                return true;
+            }
+            const int j = reads & 1;
+            const unsigned mask = __activemask();
+            const bool got = __all_sync(mask, wait_or_abort<false>(full0 + 8u * j, (reads >> 1) & 1, p, abort_flag));
+            uint32_t x = 0;
+            const bool more = got && ptx::clc_query(resp0 + 16u * j, x);
+            __syncwarp(mask);
+            if (releaser && got) ptx::mbar_arrive_remote_relaxed(free0 + 8u * j);
+            ++reads;
+            if (!more) return false;
+            tile = static_cast<int>(x) / (kPair ? 2 : 1);
+            w = Work{tile, 0, (num_k + p.kblock_tiles - 1) / p.kblock_tiles, WORK_FULL};
+            return true;
+        }
+    }
+};
+
 template <bool kBF16>
 __device__ __forceinline__ uint32_t pack2(float a, float b) {
     if constexpr (kBF16) {
@@ -317,8 +372,11 @@ __device__ __forceinline__ void store_row32_16(uint16_t *row_ptr, int n, int col
     }
 }
 
-template <int kG, bool kBF16, bool kIntPath, bool kRS = false>
+// kDyn: one CTA pair launched per tile, balanced at run time by cluster launch
+// control (float path only: no stream-K tail).
+template <int kG, bool kBF16, bool kIntPath, bool kRS = false, bool kDyn = false>
 __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_constant__ GemmParams p) {
+    static_assert(!kDyn || (kG == 2 && !kIntPath), "run-time tiles are a CTA-pair float-path form");
     constexpr bool kTmaOut = true;  // epilogue stores through shared slabs and TMA (see the epilogue)
     using Cfg = TileCfg<kG, kTmaOut>;
     constexpr bool kPair = kG == 2;
@@ -334,6 +392,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 3 * S + 4);
     uint64_t *drain_bar = bars + 3 * S + 5;   // every MMA this CTA issued has completed
     uint64_t *skr_bar = bars + 3 * S + 6;     // per epilogue warp: its share of a stream-K partial landed
+    uint64_t *walk_resp = bars + 3 * S + 14;  // kDyn: two 16-byte answers (16-byte aligned)
+    uint64_t *walk_full = bars + 3 * S + 18;  // kDyn: answer landed (this CTA)
+    uint64_t *walk_free = bars + 3 * S + 20;  // kDyn: answer read by every role (the leader's counts both CTAs)
     // the epilogue's output slabs, after the 1 KiB barrier area (1024-byte aligned)
     uint8_t *epi_stage = smem + S * Cfg::kStageBytes + 1024;
     __shared__ int abort_flag_s;
@@ -352,6 +413,18 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
     const int nkb = (num_k + p.kblock_tiles - 1) / p.kblock_tiles;  // K blocks per tile
     Schedule sched;
     sched.init(cluster_id, num_clusters, num_tiles, p.sk_tiles, nkb);
+    // every role walks its own copy
+    TileWalk<kDyn> walk0;
+    walk0.sched = &sched;
+    walk0.wi = 0;
+    walk0.tile = -1;
+    walk0.first_tile = cluster_id;
+    walk0.reads = 0;
+    walk0.num_k = num_k;
+    walk0.resp0 = ptx::smem_u32(&walk_resp[0]);
+    walk0.full0 = ptx::smem_u32(&walk_full[0]);
+    walk0.free0 = kPair ? ptx::mapa(ptx::smem_u32(&walk_free[0]), 0) : ptx::smem_u32(&walk_free[0]);
+    walk0.releaser = lane == 0;
 
     if (threadIdx.x == 0) {
         abort_flag_s = 0;
@@ -366,6 +439,15 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
         }
         ptx::mbar_init(ptx::smem_u32(drain_bar), 1);
         for (int e = 0; e < kNumEpiWarps; ++e) ptx::mbar_init(ptx::smem_u32(&skr_bar[e]), 1);
+        if constexpr (kDyn) {
+            // releases per answer: per CTA the producer, the epilogue warps and the
+            // gathered-store lane, plus the leader's MMA warp
+            const uint32_t roles = kG * (1 + kNumEpiWarps + (p.gather ? 1 : 0)) + 1;
+            for (int j = 0; j < 2; ++j) {
+                ptx::mbar_init(ptx::smem_u32(&walk_full[j]), 1);
+                ptx::mbar_init(ptx::smem_u32(&walk_free[j]), roles);
+            }
+        }
         ptx::fence_mbar_init();
     }
     if (warp == 1) {
@@ -483,8 +565,26 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
                 if (++stage == S) stage = 0, phase ^= 1u;
             }
         };
-        for (int wi = 0; wi < sched.count() && ok; ++wi) {
-            const Work w = sched.get(wi);
+        TileWalk<kDyn> walk = walk0;
+        int asked = 0;   // kDyn: answers asked for (one per tile started)
+        Work w;
+        while (ok && walk.template next<kPair>(w, p, abort_flag)) {
+            if constexpr (kDyn) {
+                // ask for the tile after this one: the answer goes to slot asked & 1 of both CTAs
+                const uint32_t j = asked & 1;
+                const uint32_t wf = ptx::smem_u32(&walk_full[j]);
+                if (leader) {
+                    if (!wait_or_abort<false>(ptx::smem_u32(&walk_free[j]), ((asked >> 1) & 1) ^ 1u, p, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::mbar_arrive_expect_tx(wf, 16);
+                    ptx::clc_try_cancel_multicast(ptx::smem_u32(&walk_resp[2 * j]), wf);
+                } else {
+                    ptx::mbar_arrive_expect_tx(wf, 16);
+                }
+                ++asked;
+            }
             const int kt_begin = w.kb0 * p.kblock_tiles, kt_end = min(num_k, w.kb1 * p.kblock_tiles);
             int mb, nb;
             tile_coords<kIntPath>(w.tile, num_m, num_n, mb, nb);
@@ -559,8 +659,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
         bool ok = true;
         uint32_t d_tmem = tmem_base;
         const uint32_t consumed0 = ptx::smem_u32(&consumed_bar[0]);
-        for (int wi = 0; wi < sched.count() && ok; ++wi) {
-            const Work w = sched.get(wi);
+        TileWalk<kDyn> walk = walk0;
+        Work w;
+        while (ok && walk.template next<kPair>(w, p, abort_flag)) {
             const int kt_begin = w.kb0 * kblock, kt_end = min(num_k, w.kb1 * kblock);
             int mb, nb;
             tile_coords<kIntPath>(w.tile, num_m, num_n, mb, nb);
@@ -624,8 +725,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
         uint32_t consumed_parity = 0;  // bit s: parity of the next consumed_bar[s] phase
         int pending_stage = -1;        // stage whose store may still be reading shared memory
         bool ok = true;
-        for (int wi = 0; wi < sched.count() && ok; ++wi) {
-            const Work w = sched.get(wi);
+        TileWalk<kDyn> walk = walk0;
+        Work w;
+        while (ok && walk.template next<kPair>(w, p, abort_flag)) {
             const int kt_begin = w.kb0 * p.kblock_tiles, kt_end = min(num_k, w.kb1 * p.kblock_tiles);
             int mb, nb;
             tile_coords<kIntPath>(w.tile, num_m, num_n, mb, nb);
@@ -661,8 +763,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
         const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
         uint32_t acc_iter = 0;
         uint32_t skr_phase = 0;   // phase of this warp's stream-K partial barrier
-        for (int wi = 0; wi < sched.count(); ++wi) {
-            const Work w = sched.get(wi);
+        TileWalk<kDyn> walk = walk0;
+        Work w;
+        while (walk.template next<kPair>(w, p, abort_flag)) {
             int mb, nb;
             tile_coords<kIntPath>(w.tile, num_m, num_n, mb, nb);
             const int row = mb * Cfg::kTileM + kBM * static_cast<int>(cr) + 32 * q + lane;

@@ -104,8 +104,41 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
+// Arrive on an mbarrier of a CTA of this cluster without release semantics (the
+// caller has already consumed what it read).
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Cluster launch control: ask to cancel the launch of a cluster of this grid
+// that has not started; the 16-byte answer goes to `resp` in every CTA of this
+// cluster and completes 16 transaction bytes on `bar` in each.
+__device__ __forceinline__ void clc_try_cancel_multicast(uint32_t resp, uint32_t bar) {
+    asm volatile(
+        "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.multicast::cluster::all.b128 "
+        "[%0], [%1];" ::"r"(resp),
+        "r"(bar)
+        : "memory");
+}
+
+// Decode an answer: true if a cluster was cancelled, with the x index of its first CTA
+// (read only when one was: it is undefined otherwise).
+__device__ __forceinline__ bool clc_query(uint32_t resp, uint32_t &first_ctaid_x) {
+    uint32_t ok, x;
+    asm volatile(
+        "{\n\t.reg .b128 rr;\n\t.reg .pred p;\n\tld.shared.b128 rr, [%2];\n\t"
+        "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, rr;\n\tselp.u32 %0, 1, 0, p;\n\t"
+        "mov.u32 %1, 0;\n\t"
+        "@p clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %1, rr;\n\t}"
+        : "=r"(ok), "=r"(x)
+        : "r"(resp)
+        : "memory");
+    first_ctaid_x = x;
+    return ok != 0;
 }
 
 __device__ __forceinline__ void nanosleep(uint32_t ns) { asm volatile("nanosleep.u32 %0;" ::"r"(ns)); }
