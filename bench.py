@@ -65,7 +65,7 @@ STEP_KERNELS = (
 # with: the figure is reported only while they match.
 DOMINANT_TRAFFIC = 8.68e9      # dram__bytes_read.sum 8.43 GB + dram__bytes_write.sum 0.26 GB
 DOMINANT_TRAFFIC_KERNEL = "a2a_gemm"
-DOMINANT_TRAFFIC_SRC_HASH = "a6c100cf31316497"
+DOMINANT_TRAFFIC_SRC_HASH = "f94f7cb94b8f64bd"
 
 
 def parse_args():

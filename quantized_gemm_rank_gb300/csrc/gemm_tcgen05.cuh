@@ -1,6 +1,6 @@
 // gemm_tcgen05.cuh -- the fused MC2 GEMM for sm_103a.
 //
-// One persistent kernel serves both operations:
+// One kernel serves both operations (the tile order is below):
 //   * AllGatherMatmul ("torch_npu.npu_all_gather_base_mm", 功能说明/输出说明):
 //     A = concat_m of the per-rank chunks, read in place through one TMA
 //     tensor map per chunk; out = A @ B (+ bias) rounded to bf16/fp16; the
