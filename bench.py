@@ -155,14 +155,33 @@ class ClockSampler:
         self.gpu = gpu_index
         self.file = tempfile.NamedTemporaryFile(mode="w+", suffix=".csv", delete=False)
         self.proc = None
+        self.skip = 0
+
+    def _lines(self) -> int:
+        with open(self.file.name) as f:
+            return sum(1 for r in f if r.strip())
 
     def start(self):
+        """Start sampling every 20 ms; returns once the first sample is in (at most
+        ~3 s), so that the region marked next is sampled from its start."""
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
-                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
                                          stdout=self.file, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
+            return
+        t0 = time.perf_counter()
+        while time.perf_counter() - t0 < 3.0 and self.proc.poll() is None:
+            self.file.flush()
+            if self._lines() > 0:
+                break
+            time.sleep(0.01)
+
+    def mark(self):
+        """Keep only the samples taken from now on."""
+        if self.proc is not None:
+            self.skip = self._lines()
 
     def stop(self) -> dict:
         if self.proc is None:
@@ -174,7 +193,7 @@ class ClockSampler:
             self.proc.kill()
         self.file.flush()
         self.file.seek(0)
-        rows = [r.strip().split(",") for r in self.file.read().splitlines() if r.strip()]
+        rows = [r.strip().split(",") for r in self.file.read().splitlines() if r.strip()][self.skip:]
         os.unlink(self.file.name)
         sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
@@ -736,12 +755,13 @@ def main():
 
     # ---- timed region: K steps, barrier + synchronize on both sides
     sampler = ClockSampler(local)
+    sampler.start()
     for _ in range(args.warmup):
         step.run()
     torch.cuda.synchronize()
     barrier(world)
     torch.cuda.synchronize()
-    sampler.start()
+    sampler.mark()
     wall0 = time.perf_counter()
     step_ms, ag_ms = [], []
     kern_ms = [[] for _ in range(nk)]
