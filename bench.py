@@ -63,9 +63,9 @@ STEP_KERNELS = (
 # ncu capture (dram__bytes_read.sum + dram__bytes_write.sum) of that kernel on
 # this workload, and the hash of the GEMM sources (GEMM_SOURCES) it was taken
 # with: the figure is reported only while they match.
-DOMINANT_TRAFFIC = 8.68e9      # dram__bytes_read.sum 8.43 GB + dram__bytes_write.sum 0.26 GB
+DOMINANT_TRAFFIC = 9.65e9      # dram__bytes_read.sum 9.39 GB + dram__bytes_write.sum 0.26 GB
 DOMINANT_TRAFFIC_KERNEL = "a2a_gemm"
-DOMINANT_TRAFFIC_SRC_HASH = "f94f7cb94b8f64bd"
+DOMINANT_TRAFFIC_SRC_HASH = "67ccfb57e3fa3bb7"
 
 
 def parse_args():
@@ -526,8 +526,10 @@ def run_reference(args):
 
 
 # ----------------------------------------------------------------------------- main
-def workload_call(s, dev):
+def workload_call(s, dev, separate_chunks=False):
     """Device-resident inputs of one workload and a closure that runs its call.
+    All-gather chunks are the slices of one buffer, or (separate_chunks) each
+    its own allocation.
     Returns (fn, work, unit, launches): work is FLOPs (or OPs) of the GEMM, or
     bytes for the HBM-bound QuantAllReduce; launches is the number of kernels
     the call launches (the last one is the GEMM for every GEMM workload)."""
@@ -541,7 +543,15 @@ def workload_call(s, dev):
             s.bytes, "bytes", 1
     if isinstance(s, mc2_inputs.AGShape):
         inp = mc2_inputs.ag_inputs(s, seed=0)
-        ch = [c.to(dev) for c in inp["chunks"]]
+        if separate_chunks:
+            # every chunk its own allocation, 1 MiB apart
+            ch, gaps = [], []
+            for c in inp["chunks"]:
+                ch.append(c.to(dev))
+                gaps.append(torch.empty(1 << 20, dtype=torch.uint8, device=dev))
+        else:
+            # the slices of one receive buffer, as an all-gather leaves them
+            ch = list(torch.cat(inp["chunks"]).to(dev).split(s.m_local))
         x2 = inp["x2"].to(dev)
         b = None if inp["bias"] is None else inp["bias"].to(dev)
         out = torch.empty((s.m, s.n), dtype=s.dtype, device=dev)
@@ -648,6 +658,10 @@ def extra_table(dev, flush, stream, steps, peaks):
         if name == "ag-tiny":
             res[name]["host_call_us"] = round(host_call_us(fn), 2)
             res[name]["c_abi_call_us"] = round(host_call_us(c_abi_all_gather_call(s, dev)), 2)
+            # the same call with every chunk its own allocation (read box by box)
+            fn_sep = workload_call(s, dev, separate_chunks=True)[0]
+            res[name]["separate_chunks_us"] = round(statistics.median(time_device(fn_sep, steps, 3, flush, stream)) * 1e3, 2)
+            del fn_sep
         del fn
         torch.cuda.empty_cache()
     res["int8_context"] = int8_context(dev, flush, stream, steps)

@@ -88,10 +88,10 @@ unsigned long long next_sk_epoch() {
     return kLo + counter.fetch_add(1, std::memory_order_relaxed) % kSpan;
 }
 
-template <int kG, bool kBF16, bool kIntPath, bool kRS = false, bool kDyn = false>
+template <int kG, bool kBF16, bool kIntPath, bool kRS = false, bool kDyn = false, bool kNarrow = false>
 cudaError_t launch_one(const GemmParams &p_in, int num_sms, cudaStream_t stream) {
-    using Cfg = TileCfg<kG, true>;
-    auto kern = mc2_gemm_kernel<kG, kBF16, kIntPath, kRS, kDyn>;
+    using Cfg = TileCfg<kG, true, kNarrow>;
+    auto kern = mc2_gemm_kernel<kG, kBF16, kIntPath, kRS, kDyn, kNarrow>;
     GemmParams p = p_in;
     // once per host thread and context (a device switch or reset makes a new
     // context): the status word's address and the shared-memory opt-in
@@ -180,6 +180,8 @@ cudaError_t launch_gemm(GemmKind kind, int group, const GemmParams &p, int num_s
             case GEMM_INT_AS_F16: return launch_one<1, false, true>(p, num_sms, stream);
             case GEMM_RS_F16: return launch_one<1, false, false, true>(p, num_sms, stream);
             case GEMM_RS_BF16: return launch_one<1, true, false, true>(p, num_sms, stream);
+            case GEMM_F16_NARROW: return launch_one<1, false, false, false, false, true>(p, num_sms, stream);
+            case GEMM_BF16_NARROW: return launch_one<1, true, false, false, false, true>(p, num_sms, stream);
         }
     }
     return cudaErrorInvalidValue;

@@ -84,13 +84,16 @@ constexpr uint32_t kEpiStageBytes = kNumEpiWarps * kEpiSlabBytes;
 
 // kTmaOut: reserve the epilogue's shared staging slabs (8 x 4 KiB) after the
 // stage ring; every instantiation of the GEMM stores its outputs through them.
-template <int kG, bool kTmaOut = false>
+// kNarrow (one CTA, outputs at most 64 wide): MMA N = 64 and 24 KiB stages, so
+// a ring of 8 holds the whole K of a short problem at once.
+template <int kG, bool kTmaOut = false, bool kNarrow = false>
 struct TileCfg {
     static constexpr int kTileM = kBM * kG;               // rows per tile
-    static constexpr int kBRows = kBN / kG;               // rows of B (N) per CTA
+    static constexpr int kMmaN = kNarrow ? 64 : kBN;      // MMA N (accumulator columns written)
+    static constexpr int kBRows = kMmaN / kG;             // rows of B (N) per CTA
     static constexpr uint32_t kBTileBytes = kBRows * kBK * 2;
     static constexpr uint32_t kStageBytes = kATileBytes + kBTileBytes;
-    static constexpr int kStages = kG == 1 ? 4 : 6;
+    static constexpr int kStages = kNarrow ? 8 : (kG == 1 ? 4 : 6);
     // stages | barriers (1 KiB) | epilogue staging | alignment slack (1 KiB)
     static constexpr uint32_t kSmemBytes = kStages * kStageBytes + 1024 + (kTmaOut ? kEpiStageBytes : 0) + 1024;
 };
@@ -373,12 +376,14 @@ __device__ __forceinline__ void store_row32_16(uint16_t *row_ptr, int n, int col
 }
 
 // kDyn: one CTA pair launched per tile, balanced at run time by cluster launch
-// control (float path only: no stream-K tail).
-template <int kG, bool kBF16, bool kIntPath, bool kRS = false, bool kDyn = false>
+// control (float path only: no stream-K tail).  kNarrow: see TileCfg (float
+// path, one CTA per tile, n <= 64).
+template <int kG, bool kBF16, bool kIntPath, bool kRS = false, bool kDyn = false, bool kNarrow = false>
 __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_constant__ GemmParams p) {
     static_assert(!kDyn || (kG == 2 && !kIntPath), "run-time tiles are a CTA-pair float-path form");
+    static_assert(!kNarrow || (kG == 1 && !kIntPath && !kRS && !kDyn), "the narrow tile is a one-CTA float-path form");
     constexpr bool kTmaOut = true;  // epilogue stores through shared slabs and TMA (see the epilogue)
-    using Cfg = TileCfg<kG, kTmaOut>;
+    using Cfg = TileCfg<kG, kTmaOut, kNarrow>;
     constexpr bool kPair = kG == 2;
     constexpr int S = Cfg::kStages;
     extern __shared__ uint8_t smem_raw[];
@@ -639,7 +644,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
     } else if (warp == 1 && leader) {
         // ------------------------------------------------------------ MMA issuer
         const bool a_mn = p.a_mode == A_SINGLE_MN;
-        const uint32_t idesc = ptx::idesc_f16(kBF16 && !kIntPath, p.b_mn_major != 0, Cfg::kTileM, kBN, a_mn);
+        const uint32_t idesc = ptx::idesc_f16(kBF16 && !kIntPath, p.b_mn_major != 0, Cfg::kTileM, Cfg::kMmaN, a_mn);
         // descriptors of stage 0, k-slice 0; later ones add to the address field
         // (>> 4 units): per 16-wide k-slice +2 (K-major: 32 bytes into the
         // swizzled row) or +128 (MN-major: 16 rows of 128 bytes), +stage bytes per stage

@@ -18,7 +18,12 @@ struct GemmParams;
 
 // GEMM launch: kind selects the instantiation.
 // GEMM_RS_*: the reduce-scatter instantiation (per-rank B shards, scattered rows)
-enum GemmKind : int { GEMM_F16 = 0, GEMM_BF16 = 1, GEMM_INT_AS_F16 = 2, GEMM_RS_F16 = 3, GEMM_RS_BF16 = 4 };
+// GEMM_*_NARROW: the float GEMM with an N = 64 tile (group 1 only, n <= 64; B
+// maps with 64-column boxes)
+enum GemmKind : int {
+    GEMM_F16 = 0, GEMM_BF16 = 1, GEMM_INT_AS_F16 = 2, GEMM_RS_F16 = 3, GEMM_RS_BF16 = 4,
+    GEMM_F16_NARROW = 5, GEMM_BF16_NARROW = 6
+};
 // group: 1 = one CTA per 128 x 256 tile, 2 = a CTA pair per 256 x 256 tile.
 int gemm_group_for(int m);
 // Work units (CTAs for group 1, CTA pairs for group 2) co-resident on the device;

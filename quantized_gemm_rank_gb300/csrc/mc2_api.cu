@@ -341,23 +341,43 @@ int mc2_all_gather_mm(const void *const *x_chunks, int world_size, int64_t m_loc
     mc2::GemmParams p;
     memset(&p, 0, sizeof(p));
     // A: one map per rank's chunk, box rows = the largest power of two dividing
-    // both m_local and the 128-row tile, so that no box crosses a chunk.
+    // both m_local and the 128-row tile, so that no box crosses a chunk.  When the
+    // chunks lie back to back (the slices of one receive buffer, as an all-gather
+    // writes them) and a chunk is shorter than a tile, A is read through one map of
+    // the whole (m, k) instead: one 128-row box per k-tile rather than one small box
+    // per chunk (on 8 chunks of 16 rows that is 8 copies instead of 64 for a K of 512).
     int box_rows = mc2::kBM;
     while (m_local % box_rows != 0) box_rows >>= 1;
-    for (int r = 0; r < world_size; ++r)
-        if (!make_map16(&p.a_maps[r], x_chunks[r], k, m_local, mc2::kBK, box_rows))
-            return fail(MC2_ERR_CUDA, "cuTensorMapEncodeTiled failed for x_chunks[%d]", r);
-    p.num_a_maps = world_size;
-    p.a_mode = mc2::A_MCONCAT;
-    p.a_box_rows = box_rows;
+    bool back_to_back = true;
+    const int64_t chunk_bytes = m_local * k * 2;
+    for (int r = 1; r < world_size; ++r)
+        if (static_cast<const char *>(x_chunks[r]) != static_cast<const char *>(x_chunks[0]) + r * chunk_bytes)
+            back_to_back = false;
+    if (back_to_back && box_rows < mc2::kBM) {
+        if (!make_map16(&p.a_maps[0], x_chunks[0], k, m, mc2::kBK, mc2::kBM))
+            return fail(MC2_ERR_CUDA, "cuTensorMapEncodeTiled failed for the chunks (one buffer)");
+        p.num_a_maps = 1;
+        p.a_mode = mc2::A_SINGLE;
+    } else {
+        for (int r = 0; r < world_size; ++r)
+            if (!make_map16(&p.a_maps[r], x_chunks[r], k, m_local, mc2::kBK, box_rows))
+                return fail(MC2_ERR_CUDA, "cuTensorMapEncodeTiled failed for x_chunks[%d]", r);
+        p.num_a_maps = world_size;
+        p.a_mode = mc2::A_MCONCAT;
+        p.a_box_rows = box_rows;
+    }
     p.m_local = static_cast<int>(m_local);
     const int group = mc2::gemm_group_for(static_cast<int>(m));
+    // one CTA and an output at most 64 wide: the narrow tile (N = 64), whose short
+    // stages let the whole K of such a problem be in flight at once
+    const bool narrow = group == 1 && n <= 64;
+    const uint32_t b_cols = narrow ? 64u : static_cast<uint32_t>(mc2::kBN / group);   // B columns per CTA
     if (x2_is_nk) {
-        if (!make_map16(&p.b_map, x2, k, n, mc2::kBK, mc2::kBN / group))
+        if (!make_map16(&p.b_map, x2, k, n, mc2::kBK, b_cols))
             return fail(MC2_ERR_CUDA, "cuTensorMapEncodeTiled failed for x2 (n, k)");
         p.b_mn_major = 0;
     } else {
-        if (make_map16_nmajor3d(&p.b_map, x2, n, k, mc2::kBK, (mc2::kBN / group) / 64))
+        if (make_map16_nmajor3d(&p.b_map, x2, n, k, mc2::kBK, b_cols / 64))
             p.b_3d = 1;
         else if (!make_map16(&p.b_map, x2, n, k, 64, mc2::kBK))
             return fail(MC2_ERR_CUDA, "cuTensorMapEncodeTiled failed for x2 (k, n)");
@@ -377,7 +397,8 @@ int mc2_all_gather_mm(const void *const *x_chunks, int world_size, int64_t m_loc
         return fail(MC2_ERR_CUDA, "cuTensorMapEncodeTiled failed for the output");
     p.bias16 = bias;
     p.wait_limit_ns = kWaitLimitNs;
-    const mc2::GemmKind kind = dtype == MC2_BF16 ? mc2::GEMM_BF16 : mc2::GEMM_F16;
+    const mc2::GemmKind kind = narrow ? (dtype == MC2_BF16 ? mc2::GEMM_BF16_NARROW : mc2::GEMM_F16_NARROW)
+                                      : (dtype == MC2_BF16 ? mc2::GEMM_BF16 : mc2::GEMM_F16);
     LaunchMarks marks(static_cast<cudaStream_t>(stream));
     cudaError_t e = mc2::launch_gemm(kind, group, p, dev.num_sms, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail(MC2_ERR_CUDA, "GEMM launch: %s", cudaGetErrorString(e));

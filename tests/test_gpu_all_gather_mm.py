@@ -39,6 +39,13 @@ CASES = {
                                            gather_output=False),
     "bf16-kn-bias-tile-aligned": mc2_inputs.AGShape(world_size=2, m_local=256, k=1024, n=512, bias=True),
     "ag-tiny": mc2_inputs.WORKLOADS["ag-tiny"],
+    # one CTA with an output at most 64 wide: the N = 64 tile, its B as one 3-D box
+    # (n = 64), as a 2-D box with the columns past n zero-filled (n = 40), or K-major
+    # (x2 = w^T); ragged rows; K spanning several 1024-deep blocks
+    "narrow-bf16-kn-n40-ragged": mc2_inputs.AGShape(world_size=2, m_local=56, k=600, n=40),
+    "narrow-fp16-nk-bias-n8": mc2_inputs.AGShape(world_size=8, m_local=8, k=2056, n=8, dtype=torch.float16,
+                                                 x2_is_nk=True, bias=True),
+    "narrow-bf16-kn-n64-k3000": mc2_inputs.AGShape(world_size=4, m_local=32, k=3000, n=64, bias=True),
 }
 
 
@@ -178,3 +185,36 @@ def test_binding_refuses_a_host_tensor_among_device_ones():
     with pytest.raises(ValueError, match="out must be a CUDA tensor"):
         mc2.mc2_all_gather_mm(x, torch.zeros(256, 64, dtype=torch.bfloat16, device=dev),
                               out=torch.zeros(32, 64, dtype=torch.bfloat16))
+
+
+@pytest.mark.parametrize("name", ["ag-tiny", "ragged-bf16-kn", "narrow-fp16-nk-bias-n8", "bf16-kn-bias-tile-aligned"])
+def test_chunks_of_one_buffer_match_separate_chunks(name):
+    """Chunks that lie back to back (the slices of one receive buffer) are read
+    through one map of the whole A when a chunk is shorter than a tile; chunks
+    in separate allocations box by box.  Both layouts give the same bits, and
+    the oracle's result."""
+    shape = CASES[name]
+    inp = mc2_inputs.ag_inputs(shape, seed=11)
+    dev = torch.device("cuda")
+    x2 = inp["x2"].to(dev)
+    bias = None if inp["bias"] is None else inp["bias"].to(dev)
+    whole = torch.cat(inp["chunks"]).to(dev)
+    sliced = list(whole.split(shape.m_local))
+    separate, gaps = [], []
+    for c in inp["chunks"]:
+        separate.append(c.to(dev))
+        gaps.append(torch.empty(1 << 16, dtype=torch.uint8, device=dev))   # keep them apart
+    outs = []
+    for chunks in (sliced, separate):
+        out, g = mc2.mc2_all_gather_mm(chunks, x2, x2_is_nk=shape.x2_is_nk, bias=bias,
+                                       gather_output=shape.gather_output)
+        torch.cuda.synchronize()
+        assert mc2.mc2_device_status() == mc2.MC2_OK
+        outs.append((out.cpu(), None if g is None else g.cpu()))
+    assert_bits_equal(outs[0][0], outs[1][0], f"{name}: out, one buffer vs separate")
+    ref, ref_g = oracle.all_gather_mm(inp["chunks"], inp["x2"], x2_is_nk=shape.x2_is_nk, bias=inp["bias"],
+                                      gather_output=shape.gather_output)
+    assert_close_16(outs[0][0], ref, f"{name}: out")
+    if shape.gather_output:
+        assert_bits_equal(outs[0][1], ref_g, f"{name}: gathered")
+
