@@ -90,7 +90,11 @@ typedef enum {
  *   (nearest-even) to `dtype`.  bias, if given, is added in fp32 before the
  *   rounding.
  *
- *   x_chunks      host array of world_size device pointers, each (m_local, k)
+ *   x_chunks      host array of world_size device pointers, each (m_local, k);
+ *                 chunks that lie back to back (x_chunks[r] = x_chunks[0] +
+ *                 r * m_local * k elements, the slices of one receive buffer)
+ *                 are read faster when m_local < 128: through one tensor map,
+ *                 in 128-row boxes, instead of one small box per chunk
  *   world_size    2, 4 or 8
  *   m_local       rows per rank, >= 1 (this kernel: a multiple of 8)
  *   k             contraction size, 256 <= k < 65535 (this kernel: k % 8 == 0)
