@@ -563,7 +563,7 @@ def workload_call(s, dev, separate_chunks=False):
         dy, x = inp["dy"].to(dev), inp["x"].to(dev)
         dwo = torch.empty((s.n, s.k), dtype=s.dtype, device=dev)
         dbo = torch.empty((s.n,), dtype=s.dtype, device=dev)
-        return (lambda: mc2.mc2_matmul_weight_grad(dy, x, dw=dwo, db=dbo)), s.flops, "flops", 2
+        return (lambda: mc2.mc2_matmul_weight_grad(dy, x, dw=dwo, db=dbo)), s.flops, "flops", 1
     if isinstance(s, mc2_inputs.MMRSShape):
         inp = mc2_inputs.mmrs_inputs(s, seed=0)
         xs = [x.to(dev) for x in inp["x_chunks"]]

@@ -155,7 +155,9 @@ int mc2_matmul_reduce_scatter(const void *const *x_chunks, const void *const *w_
  *   db[i]    = sum_t dy[t, i]                  (n)
  *
  *   Both sums are accumulated in fp32 (dw in blocks of 1024 rows summed in fp32
- *   registers) and rounded once (nearest-even) to `dtype`.
+ *   registers; db in the same launch, from the dY tiles the GEMM has in shared
+ *   memory, as four interleaved row partials added at the end) and rounded once
+ *   (nearest-even) to `dtype`.
  *
  *   dy     (m, n) row-major          x    (m, k) row-major
  *   dw     (n, k) row-major          db   NULL or (n)
@@ -315,7 +317,7 @@ int mc2_device_status(void);
  * cudaEventElapsedTime(events[i], events[i+1]) is the device time of launch i.
  * The calls launch, in order:
  *   mc2_all_gather_mm, mc2_matmul_reduce_scatter   1: the GEMM
- *   mc2_matmul_weight_grad     2: the bias-gradient sums (only with db), the GEMM
+ *   mc2_matmul_weight_grad     1: the GEMM (which also forms db)
  *   mc2_quant_all_reduce       1: the reduction
  *   mc2_alltoall_quant_mm      x1_quant_mode 7: 2 (the fused quant and x2
  *                              widening, the GEMM), or 3 when rank_size*h > 32768

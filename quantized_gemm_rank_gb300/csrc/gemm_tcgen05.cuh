@@ -49,7 +49,12 @@
 //               barrier instead of "empty"; this warp then stores the A tile
 //               (already complete: the MMA read it) and frees the stage, so
 //               the store never delays the MMAs.
-//   warp 3      idle
+//   warps 2-3   (weight gradient with its bias gradient) on the first column of
+//               tiles, sum each stage's A rows over K from shared memory after
+//               the MMAs have read it (the stage comes to them through the same
+//               "consumed" barrier), then free it; each tile's sums are the
+//               bias gradient of its 128 rows
+//   warp 3      otherwise idle
 //   warps 4-11  epilogue: warp w reads TMEM lanes 32*(w%4)..+31 (its rows) and
 //               half (w-4)/4 of the 256 accumulator columns.  The float path
 //               stores its rounded outputs through a swizzled shared slab and a
@@ -140,6 +145,10 @@ struct GemmParams {
     // i / out_rows at row i % out_rows
     CUtensorMap b_rank_maps[kMaxAMaps];
     void *out_chunks[kMaxAMaps];
+    // weight gradient (A = dY^T read M-major): when set, the column sums of dY,
+    // i.e. the sums of A's rows over K, rounded once to 16 bits into this (m)
+    // vector (the bias gradient)
+    void *colsum_out;
     int out_rows;
     // rank r's output (out_rows, n) 16-bit, box 64 columns x 32 rows, 128-byte
     // swizzle; used when rs_tma (out_rows % 32 == 0: a warp's 32 rows are one rank's)
@@ -447,7 +456,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
         if constexpr (kDyn) {
             // releases per answer: per CTA the producer, the epilogue warps and the
             // gathered-store lane, plus the leader's MMA warp
-            const uint32_t roles = kG * (1 + kNumEpiWarps + (p.gather ? 1 : 0)) + 1;
+            const uint32_t roles = kG * (1 + kNumEpiWarps + (p.gather ? 1 : (p.colsum_out ? 2 : 0))) + 1;
             for (int j = 0; j < 2; ++j) {
                 ptx::mbar_init(ptx::smem_u32(&walk_full[j]), 1);
                 ptx::mbar_init(ptx::smem_u32(&walk_free[j]), roles);
@@ -670,8 +679,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
             const int kt_begin = w.kb0 * kblock, kt_end = min(num_k, w.kb1 * kblock);
             int mb, nb;
             tile_coords<kIntPath>(w.tile, num_m, num_n, mb, nb);
-            // stages of gathered tiles go to the gathered-store warp before being freed
-            const uint32_t release0 = (p.gather && nb == 0) ? consumed0 : empty0;
+            // stages of gathered tiles go to the gathered-store warp, and those of bias-gradient
+            // tiles to the summing warps, before being freed
+            const uint32_t release0 = ((p.gather || p.colsum_out != nullptr) && nb == 0) ? consumed0 : empty0;
             int kin = 0;  // k-tile index inside the current K block
             for (int kt = kt_begin; kt < kt_end; ++kt) {
                 if (kin == 0) {
@@ -722,6 +732,86 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
         if (!__all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(drain_bar), 0u, p.wait_limit_ns))) {
             *abort_flag = 1;
             if (p.status && lane == 0) atomicExch(p.status, -7);
+        }
+    } else if ((warp == 2 || warp == 3) && p.colsum_out != nullptr) {
+        // ------------------------------------------------------------ bias gradient
+        // A is dY^T read M-major: a stage holds, per CTA, two 64-column slabs of dY
+        // (its 128 output rows), 64 dY rows of 128 bytes each, 128-byte swizzled (chunk
+        // c of row r at chunk c ^ (r % 8)).  Warp 2 sums slab 0 and warp 3 slab 1: lane
+        // (c = l % 8, g = l / 8) adds chunk c of rows g, g + 4, ... (16 per stage) into
+        // 8 fp32 sums; at the tile's end the 4 row groups are added (lanes g = 0..3)
+        // and rounded once.  Fixed order: the result is deterministic.
+        const int slab = warp - 2;
+        const int c = lane & 7;
+        const int g = lane >> 3;
+        int stage = 0;
+        uint32_t consumed_parity = 0;  // bit s: parity of the next consumed_bar[s] phase
+        bool ok = true;
+        TileWalk<kDyn> walk = walk0;
+        Work w;
+        while (ok && walk.template next<kPair>(w, p, abort_flag)) {
+            const int kt_begin = w.kb0 * p.kblock_tiles, kt_end = min(num_k, w.kb1 * p.kblock_tiles);
+            int mb, nb;
+            tile_coords<kIntPath>(w.tile, num_m, num_n, mb, nb);
+            if (nb != 0) {  // its stages are freed by the MMA directly
+                stage = (stage + (kt_end - kt_begin)) % S;
+                continue;
+            }
+            float acc[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
+            for (int kt = kt_begin; kt < kt_end; ++kt) {
+                const bool got = __all_sync(0xffffffffu, wait_or_abort<kPair>(ptx::smem_u32(&consumed_bar[stage]),
+                                                                              (consumed_parity >> stage) & 1u, p,
+                                                                              abort_flag));
+                if (got) {
+                    const uint8_t *slab_p = smem + stage * Cfg::kStageBytes + slab * (kBK * 128);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const int r = g + 4 * i;
+                        const uint4 v = *reinterpret_cast<const uint4 *>(slab_p + r * 128 + ((c ^ (r & 7)) << 4));
+                        const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            float lo, hi;
+                            if constexpr (kBF16) {
+                                lo = __uint_as_float(vw[e] << 16);
+                                hi = __uint_as_float(vw[e] & 0xFFFF0000u);
+                            } else {
+                                const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&vw[e]));
+                                lo = f.x;
+                                hi = f.y;
+                            }
+                            acc[2 * e] = __fadd_rn(acc[2 * e], lo);
+                            acc[2 * e + 1] = __fadd_rn(acc[2 * e + 1], hi);
+                        }
+                    }
+                }
+                // both warps have read the stage (or both give up): the stage is free
+                if (!ptx::bar_red_and(1, 64, got)) {
+                    ok = false;
+                    break;
+                }
+                consumed_parity ^= 1u << stage;
+                if (warp == 2 && lane == 0) ptx::mbar_arrive(ptx::smem_u32(&empty_bar[stage]));
+                if (++stage == S) stage = 0;
+            }
+            if (!ok) break;
+            // the four row groups of each chunk, in a fixed order
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                acc[e] = __fadd_rn(acc[e], __shfl_xor_sync(0xffffffffu, acc[e], 8));
+                acc[e] = __fadd_rn(acc[e], __shfl_xor_sync(0xffffffffu, acc[e], 16));
+            }
+            const int col = mb * Cfg::kTileM + kBM * static_cast<int>(cr) + 64 * slab + 8 * c;
+            if (g == 0 && col < p.m) {
+                uint4 o;
+                o.x = pack2<kBF16>(acc[0], acc[1]);
+                o.y = pack2<kBF16>(acc[2], acc[3]);
+                o.z = pack2<kBF16>(acc[4], acc[5]);
+                o.w = pack2<kBF16>(acc[6], acc[7]);
+                *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.colsum_out) + col) = o;
+            }
         }
     } else if (warp == 2 && lane == 0 && p.gather) {
         // ------------------------------------------------------------ gathered store

@@ -66,9 +66,6 @@ cudaError_t launch_widen_a2a(const ChunkPtrs &chunks, int rank_size, int64_t bs_
                              int num_sms, cudaStream_t stream);
 cudaError_t launch_permute_widen_i8(const ChunkPtrs &chunks, int rank_size, int64_t bs_local, int h, __half *dst,
                                     int8_t *q_out, int8_t *comm_out, int num_sms, cudaStream_t stream);
-// db[j] = sum_t dy[t, j] for dy (m, n) 16-bit row-major, n % 8 == 0: fp32 sums
-// rounded once to the same type.
-cudaError_t launch_colsum16(const void *dy, int64_t m, int n, bool bf16, void *db, cudaStream_t stream);
 // comm_out (optional, NULL for none): the received chunks stacked as
 // (rank_size, bs_local, h) in their own dtype, written by the kernel that reads them.
 

@@ -499,13 +499,9 @@ int mc2_matmul_weight_grad(const void *dy, int64_t m, int64_t n, const void *x, 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaSuccess;
     LaunchMarks marks(s);
-    if (db) {
-        e = mc2::launch_colsum16(dy, m, static_cast<int>(n), dtype == MC2_BF16, db, s);
-        if (e != cudaSuccess) return fail(MC2_ERR_CUDA, "bias-gradient launch: %s", cudaGetErrorString(e));
-        marks.launched();
-    }
     // dW (n, k) = dY^T @ X: A = dY^T read M-major from dY (m, n), B = X (m, k) N-major,
-    // the contraction runs down the m rows of both
+    // the contraction runs down the m rows of both; the same launch sums A's rows
+    // over the contraction (the column sums of dY) into db
     mc2::GemmParams p;
     memset(&p, 0, sizeof(p));
     if (!make_map16(&p.a_maps[0], dy, n, m, 64, mc2::kBK)) return fail(MC2_ERR_CUDA, "cuTensorMapEncodeTiled failed for dy");
@@ -524,6 +520,7 @@ int mc2_matmul_weight_grad(const void *dy, int64_t m, int64_t n, const void *x, 
     p.out = dw;
     if (!make_map16(&p.out_map, p.out, static_cast<uint64_t>(p.n), static_cast<uint64_t>(p.m), 64, 32))
         return fail(MC2_ERR_CUDA, "cuTensorMapEncodeTiled failed for the output");
+    p.colsum_out = db;
     p.wait_limit_ns = kWaitLimitNs;
     const int group = mc2::gemm_group_for(static_cast<int>(n));
     e = mc2::launch_gemm(dtype == MC2_BF16 ? mc2::GEMM_BF16 : mc2::GEMM_F16, group, p, dev.num_sms, s);

@@ -141,6 +141,19 @@ __device__ __forceinline__ bool clc_query(uint32_t resp, uint32_t &first_ctaid_x
     return ok != 0;
 }
 
+// Named barrier `id` over `count` threads (a multiple of 32) with an AND
+// reduction: every participating thread gets true iff all of them passed true.
+__device__ __forceinline__ bool bar_red_and(uint32_t id, uint32_t count, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred q, p;\n\tsetp.ne.u32 q, %1, 0;\n\tbar.red.and.pred p, %2, %3, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
+}
+
 __device__ __forceinline__ void nanosleep(uint32_t ns) { asm volatile("nanosleep.u32 %0;" ::"r"(ns)); }
 
 // Fetch the line holding `p` into L1 (no register result).
