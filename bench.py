@@ -65,7 +65,7 @@ STEP_KERNELS = (
 # with: the figure is reported only while they match.
 DOMINANT_TRAFFIC = 19.18e9     # dram__bytes_read.sum 18.92 GB + dram__bytes_write.sum 0.26 GB (8.7-19.2 GB across captures)
 DOMINANT_TRAFFIC_KERNEL = "a2a_gemm"
-DOMINANT_TRAFFIC_SRC_HASH = "bddce4b79fa2ea8c"
+DOMINANT_TRAFFIC_SRC_HASH = "3348030a6a738d00"
 
 
 def parse_args():

@@ -3,7 +3,8 @@
 // One kernel serves both operations (the tile order is below):
 //   * AllGatherMatmul ("torch_npu.npu_all_gather_base_mm", 功能说明/输出说明):
 //     A = concat_m of the per-rank chunks, read in place through one TMA
-//     tensor map per chunk; out = A @ B (+ bias) rounded to bf16/fp16; the
+//     tensor map per chunk (or one map, when the chunks lie back to back);
+//     out = A @ B (+ bias) rounded to bf16/fp16; the
 //     gathered matrix is written from the A tiles already in shared memory
 //     (one TMA store per (m-tile, k-tile), by the n-tile-0 tiles only).
 //   * AlltoAllQuantMatmul ("aclnnAlltoAllQuantMatmul", 计算公式): A and B
@@ -19,7 +20,8 @@
 //
 // Two shapes of the same kernel (template parameter kG):
 //   kG = 1  one CTA per tile: tile 128 x 256 x 64, tcgen05.mma.cta_group::1
-//           M=128 N=256, 4-stage ring of 48 KiB stages.
+//           M=128 N=256, 4-stage ring of 48 KiB stages; or (kNarrow, outputs at
+//           most 64 wide) N=64 and an 8-stage ring of 24 KiB stages.
 //   kG = 2  a CTA pair (cluster of 2) per tile: tile 256 x 256 x 64,
 //           tcgen05.mma.cta_group::2 M=256 N=256 issued by the leader CTA;
 //           each CTA loads its own 128 rows of A and 128 rows of B (half the
@@ -56,10 +58,10 @@
 //               bias gradient of its 128 rows
 //   warp 3      otherwise idle
 //   warps 4-11  epilogue: warp w reads TMEM lanes 32*(w%4)..+31 (its rows) and
-//               half (w-4)/4 of the 256 accumulator columns.  The float path
-//               stores its rounded outputs through a swizzled shared slab and a
-//               TMA tensor store; the integer path and the reduce-scatter store
-//               from registers.
+//               half (w-4)/4 of the 256 accumulator columns.  Rounded outputs
+//               leave through a swizzled shared slab and a TMA tensor store, but
+//               for the reduce-scatter whose warps' rows may span two ranks
+//               (stored from registers).
 #pragma once
 
 #include <cuda_bf16.h>
