@@ -133,9 +133,12 @@ __device__ __forceinline__ void load_vec(const QarPtrs &p, int64_t v, uint4 (&xv
 // kOut: 0 fp32, 1 fp16, 2 bf16.  kR: ranks.  With int8 codes each thread
 // takes two vectors per step (v and v + stride, the loads of both in flight
 // before either is reduced); the fp8 decode needs more registers, and there
-// one vector per step keeps more threads resident.
+// one vector per step keeps more threads resident.  The launch bound asks for 4
+// CTAs per SM (64 registers): at the 80 registers the compiler chose otherwise,
+// 3 fit, and the loads in flight of the 4th are worth more than the registers
+// (qar-8x4096x8192: 68.2 -> 62.1 us; 6 CTAs at 40 registers spill and run slower).
 template <int kX, int kS, int kOut, int kR>
-__global__ void __launch_bounds__(kThreads) quant_all_reduce_kernel(QarPtrs p, int64_t nvec, void *__restrict__ out) {
+__global__ void __launch_bounds__(kThreads, 4) quant_all_reduce_kernel(QarPtrs p, int64_t nvec, void *__restrict__ out) {
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
     int64_t v = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
     if constexpr (kX == 0) {
