@@ -218,3 +218,23 @@ def test_chunks_of_one_buffer_match_separate_chunks(name):
     if shape.gather_output:
         assert_bits_equal(outs[0][1], ref_g, f"{name}: gathered")
 
+
+
+def test_run_time_tiles_on_a_large_grid():
+    """8192 tiles of 256 x 256 (one CTA pair launched per tile; the running pairs
+    take over the tiles of pairs not yet launched): one seeded row of every
+    256-row tile block checked against the oracle, the gathered output bit for
+    bit, and every output finite."""
+    shape = mc2_inputs.AGShape(world_size=8, m_local=8192, k=256, n=8192, bias=True)
+    inp = mc2_inputs.ag_inputs(shape, seed=21)
+    dev = torch.device("cuda")
+    out, gathered = mc2.mc2_all_gather_mm([c.to(dev) for c in inp["chunks"]], inp["x2"].to(dev),
+                                          bias=inp["bias"].to(dev))
+    torch.cuda.synchronize()
+    assert mc2.mc2_device_status() == mc2.MC2_OK
+    rows = rows_per_block(shape.m, 256, seed=22)
+    ref, _ = oracle.all_gather_mm(inp["chunks"], inp["x2"], bias=inp["bias"], rows=rows, gather_output=False)
+    o = out.cpu()
+    assert_close_16(o[rows], ref, "8192 tiles: sampled rows")
+    assert torch.isfinite(o).all()
+    assert_bits_equal(gathered.cpu(), torch.cat(inp["chunks"]), "8192 tiles: gathered")
