@@ -238,3 +238,34 @@ def test_run_time_tiles_on_a_large_grid():
     assert_close_16(o[rows], ref, "8192 tiles: sampled rows")
     assert torch.isfinite(o).all()
     assert_bits_equal(gathered.cpu(), torch.cat(inp["chunks"]), "8192 tiles: gathered")
+
+
+def _ag_sweep(count, seed):
+    import random
+    rng = random.Random(seed)
+    shapes = []
+    for _ in range(count):
+        R = rng.choice([2, 4, 8])
+        m_local = rng.choice([8, 16, 40, 64, 72, 128, 136, 256, 512, 1000])
+        k = rng.choice([256, 264, 512, 1032, 2048])
+        n = rng.choice([8, 64, 136, 256, 264, 520, 1000, 2048])
+        shapes.append(mc2_inputs.AGShape(world_size=R, m_local=m_local, k=k, n=n,
+                                         dtype=rng.choice([torch.bfloat16, torch.float16]),
+                                         x2_is_nk=rng.choice([True, False]), bias=rng.choice([True, False]),
+                                         gather_output=rng.choice([True, False])))
+    return shapes
+
+
+@pytest.mark.parametrize("case,shape", list(enumerate(_ag_sweep(24, 2026))))
+def test_seeded_shape_sweep(case, shape):
+    """Seeded random shapes over both tile forms (one CTA, narrow or wide; CTA
+    pairs with run-time tiles), both x2 layouts, with and without bias and the
+    gathered output: every output within the stated tolerance of the oracle,
+    the gathered output bit for bit."""
+    inp = mc2_inputs.ag_inputs(shape, seed=300 + case)
+    out, gathered = run_gpu(inp, shape)
+    ref, ref_g = oracle.all_gather_mm(inp["chunks"], inp["x2"], x2_is_nk=shape.x2_is_nk, bias=inp["bias"],
+                                      gather_output=shape.gather_output)
+    assert_close_16(out, ref, f"sweep {case}: out")
+    if shape.gather_output:
+        assert_bits_equal(gathered, ref_g, f"sweep {case}: gathered")

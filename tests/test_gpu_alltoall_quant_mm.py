@@ -295,3 +295,31 @@ def test_stream_k_workspace_needs_no_zeroing():
         outs.append(res["out"].cpu())
     for o in outs[1:]:
         assert_bits_equal(o, outs[0], "every launch identical")
+
+
+def _sweep_shapes(count, seed):
+    import random
+    rng = random.Random(seed)
+    shapes = []
+    for _ in range(count):
+        R = rng.choice([2, 4, 8])
+        mode = rng.choice([3, 7])
+        h = rng.choice([8, 16, 24, 40, 64, 96, 128, 136, 256, 320, 512])
+        if (R * h) % 16:
+            h += 8
+        bs = rng.choice([1, 7, 64, 100, 128, 129, 200, 256, 300, 513, 1100])
+        n = rng.choice([16, 48, 256, 272, 512, 784, 1024, 2048])
+        extra = {"x1_dtype": rng.choice([torch.bfloat16, torch.float16])} if mode == 7 else {}
+        shapes.append(A2A(rank_size=R, bs_local=bs, h=h, n=n, quant_mode=mode, **extra))
+    return shapes
+
+
+@pytest.mark.parametrize("case,shape", list(enumerate(_sweep_shapes(30, 7))))
+def test_seeded_shape_sweep(case, shape):
+    """Seeded random shapes: ranks 2/4/8, both quant modes, rows on both sides of
+    the one-CTA / CTA-pair boundary (and with stream-K tails), ragged h and n;
+    every output bit for bit against the oracle."""
+    inp = mc2_inputs.a2a_inputs(shape, seed=100 + case)
+    got = run_gpu(inp, shape)
+    ref = run_oracle(inp, shape)
+    compare(got, ref, f"sweep {case} {shape}")
