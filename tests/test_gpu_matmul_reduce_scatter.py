@@ -96,3 +96,26 @@ def test_full_size_row_of_every_warp_block():
     rows = rows_per_block(shape.m, 32, seed=1, extra=edges)
     assert_close_16(got[rows], run_oracle(inp, shape, rows=rows), "mmrs-4x2048 rows")
     assert torch.isfinite(got.float()).all()
+
+
+def _sweep(count, seed):
+    import random
+    rng = random.Random(seed)
+    shapes = []
+    for _ in range(count):
+        R = rng.choice([2, 4, 8])
+        m = R * rng.choice([8, 17, 32, 64, 100, 128, 256])
+        k_local = rng.choice([256, 320, 512, 1024])
+        n = rng.choice([8, 64, 264, 520, 1024])
+        shapes.append(S(world_size=R, m=m, k_local=k_local, n=n, dtype=rng.choice([torch.bfloat16, torch.float16]),
+                        w_is_nk=rng.choice([True, False]), bias=rng.choice([True, False])))
+    return shapes
+
+
+@pytest.mark.parametrize("case,shape", list(enumerate(_sweep(16, 77))))
+def test_seeded_shape_sweep(case, shape):
+    """Seeded random shapes (one CTA and CTA pairs, ranks whose row blocks do and
+    do not fill a warp's 32 rows, both weight layouts, with and without bias):
+    every row of every rank's output within the stated tolerance of the oracle."""
+    inp = mc2_inputs.mmrs_inputs(shape, seed=400 + case)
+    assert_close_16(run_gpu(inp, shape), run_oracle(inp, shape), f"sweep {case}")

@@ -96,3 +96,23 @@ def test_full_size_row_of_every_warp_block():
     assert_close_16(dw[rows], ref_w, "wgrad-ag-4x4096 rows")
     assert_close_16(db, ref_b, "wgrad-ag-4x4096 db")
     assert torch.isfinite(dw.float()).all()
+
+
+def _sweep(count, seed):
+    import random
+    rng = random.Random(seed)
+    return [S(m=rng.choice([1, 64, 100, 513, 1090, 2048]), n=rng.choice([8, 64, 128, 136, 272, 520, 1024]),
+              k=rng.choice([8, 64, 264, 512, 1000]), dtype=rng.choice([torch.bfloat16, torch.float16]))
+            for _ in range(count)]
+
+
+@pytest.mark.parametrize("case,shape", list(enumerate(_sweep(16, 88))))
+def test_seeded_shape_sweep(case, shape):
+    """Seeded random shapes (one CTA and CTA pairs over dW's rows; contraction
+    lengths from 1 to 2048 rows, ragged): dW and the bias gradient summed inside
+    the GEMM, within the stated tolerance of the oracle."""
+    inp = mc2_inputs.wgrad_inputs(shape, seed=500 + case)
+    dw, db = run_gpu(inp)
+    ref_w, ref_b = oracle.matmul_weight_grad(inp["dy"], inp["x"])
+    assert_close_16(dw, ref_w, f"sweep {case}: dw")
+    assert_close_16(db, ref_b, f"sweep {case}: db")
