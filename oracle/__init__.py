@@ -39,22 +39,31 @@ _I64 = ctypes.c_int64
 _INT = ctypes.c_int
 
 
+def compile_library(src: str, out: str) -> str:
+    """gcc the oracle source `src` into the shared library `out` (OpenMP, no FMA contraction)."""
+    tmp = out + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-std=c11", "-O2", "-fopenmp", "-ffp-contract=off", "-fno-fast-math",
+           "-fPIC", "-shared", "-o", tmp, src, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out)
+    return out
+
+
 def build(force: bool = False) -> str:
-    """Compile the C oracle with gcc (OpenMP, no FMA contraction)."""
+    """Compile the C oracle (when its source is newer than the library)."""
     if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
-        tmp = _LIB + f".tmp{os.getpid()}"
-        cmd = ["gcc", "-std=c11", "-O2", "-fopenmp", "-ffp-contract=off", "-fno-fast-math",
-               "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"]
-        subprocess.run(cmd, check=True)
-        os.replace(tmp, _LIB)
+        compile_library(_SRC, _LIB)
     return _LIB
 
 
 def _load():
     global _lib
     if _lib is None:
-        build()
-        lib = ctypes.CDLL(_LIB)
+        # MC2_ORACLE_LIB names an oracle library built elsewhere from a copy of
+        # mc2_oracle.c: the planted-mistake tests (tests/test_oracle_mutants.py)
+        # run the pins against copies with one mistake each through it
+        path = os.environ.get("MC2_ORACLE_LIB") or build()
+        lib = ctypes.CDLL(path)
         lib.oracle_decode16.restype = ctypes.c_double
         lib.oracle_decode16.argtypes = [ctypes.c_uint16, _INT]
         lib.oracle_encode16_rne.restype = ctypes.c_uint16

@@ -6,10 +6,16 @@
   properties on random rows: max|q| = 127, |q*scale - y| <= scale/2
 * int8 matmul: numpy's integer matmul, the all-127 accumulator bound, overflow
 * dequant: scales 1 and bias 0 reduce to bf16(float(acc))
+* the steps decided by fp32 rounding (the quant's division by the scale, the
+  dequant's left-to-right products) against exact rational arithmetic with
+  each IEEE rounding written out (fractions.Fraction), on inputs where the
+  other plausible readings give another result
 * the whole path on hand-derived tiny examples (tests/golden/a2a_tiny.json)
 """
 import json
 import os
+import struct
+from fractions import Fraction
 
 import numpy as np
 import pytest
@@ -79,6 +85,71 @@ def test_comm_out_index_tracing(R, elem):
         # and its permute(1, 0, 2).view is the permuted matrix
         P = oracle.permute(chunks if elem == torch.int8 else [c.view(torch.bfloat16) for c in chunks])
         assert torch.equal(got.permute(1, 0, 2).reshape(BS // R, R * H), P.view(elem))
+
+
+def _round_binary(x: Fraction, p: int, emin: int = -126) -> Fraction:
+    """x rounded to the nearest binary float with p significand bits (ties to
+    even), exponent >= emin (subnormals below it): one IEEE rounding, done
+    exactly.  p = 24 is fp32, p = 8 is bf16 (overflow is out of range here)."""
+    if x == 0:
+        return Fraction(0)
+    a = abs(x)
+    e = a.numerator.bit_length() - a.denominator.bit_length()   # 2^e <= a < 2^(e+2)
+    if Fraction(2) ** e > a:
+        e -= 1
+    if Fraction(2) ** (e + 1) <= a:
+        e += 1
+    quantum = Fraction(2) ** (max(e, emin) - p + 1)
+    n = a / quantum
+    r = n.numerator // n.denominator
+    rest = n - r
+    if rest > Fraction(1, 2) or (rest == Fraction(1, 2) and r % 2 == 1):
+        r += 1
+    return (r * quantum) if x > 0 else -(r * quantum)
+
+
+def _rne_int(x: Fraction) -> int:
+    """Nearest integer, ties to even."""
+    r = x.numerator // x.denominator
+    rest = x - r
+    return r + 1 if rest > Fraction(1, 2) or (rest == Fraction(1, 2) and r % 2 == 1) else r
+
+
+def _f32(bits: int) -> Fraction:
+    return Fraction(struct.unpack("<f", struct.pack("<I", bits))[0])
+
+
+@pytest.mark.parametrize("amax,y", [(Fraction(9, 8), Fraction(9, 16)), (Fraction(75, 64), Fraction(75, 128))])
+def test_quant_divides_by_the_fp32_scale(amax, y):
+    # A row [amax, y] with y = amax / 2: the real quotient y / (amax / 127) is the
+    # tie 63.5, so the fp32 rounding of the scale decides q.  Exactly:
+    # scale = fl32(amax / 127), q = rne(fl32(y / scale)).  Multiplying by
+    # fl32(1 / scale) instead lands on the other side of the tie here.
+    scale = _round_binary(amax / 127, 24)
+    q_div = _rne_int(_round_binary(y / scale, 24))
+    q_rcp = _rne_int(_round_binary(y * _round_binary(1 / scale, 24), 24))
+    assert q_div != q_rcp, "the case no longer separates the two readings"
+    x = torch.tensor([[float(amax), float(y)]], dtype=torch.bfloat16)
+    assert x.double().tolist() == [[float(amax), float(y)]]
+    q, sc = oracle.quant_pertoken_dynamic(x)
+    assert Fraction(sc.item()) == scale
+    assert q[0].tolist() == [127, q_div]
+
+
+@pytest.mark.parametrize("acc,s1_bits,s2_bits", [(5951682, 0x3BF14CAA, 0x3B0336D7), (434371, 0x3C1A1E4B, 0x3B4F01C5)])
+def test_dequant_products_left_to_right(acc, s1_bits, s2_bits):
+    # out = bf16(((float(acc) * x1s) * x2s) + bias), each step one fp32 rounding,
+    # in the order the formula prints.  On these inputs the fp32 result lands on
+    # (or next to) a bf16 tie, and the product taken in the other order rounds
+    # to another bf16 value.
+    s1, s2 = _f32(s1_bits), _f32(s2_bits)
+    a = _round_binary(Fraction(acc), 24)
+    printed = _round_binary(_round_binary(_round_binary(a * s1, 24) * s2, 24), 8)
+    swapped = _round_binary(_round_binary(_round_binary(a * s2, 24) * s1, 24), 8)
+    assert printed != swapped, "the case no longer separates the two orders"
+    out = oracle.dequant(torch.tensor([[acc]], dtype=torch.int32), torch.tensor([float(s1)]),
+                         torch.tensor([float(s2)]), torch.zeros(1))
+    assert Fraction(out.double().item()) == printed
 
 
 def test_quant_golden_rows():
@@ -225,6 +296,12 @@ def test_full_quant_mode_uses_input_scale():
     assert torch.equal(res["x1_scale"], inp["x1_scale"])
     ref = P.numpy().astype(np.int64) @ inp["x2"].numpy().astype(np.int64)
     assert np.array_equal(res["acc"].numpy().astype(np.int64), ref)
+    # a row subset takes each token's own scale: the rows of the full result
+    rows = [15, 0, 9, 4]
+    sub = oracle.alltoall_quant_mm(inp["chunks"], inp["x2"], inp["x2_scale"], inp["bias"], quant_mode=3,
+                                   x1_scale=inp["x1_scale"], rows=rows)
+    assert torch.equal(sub["x1_scale"], inp["x1_scale"][rows])
+    assert torch.equal(sub["out"].view(torch.int16), res["out"][rows].view(torch.int16))
 
 
 def test_fp64_int8_mm_route_equals_integer_loop():
