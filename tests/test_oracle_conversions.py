@@ -59,3 +59,18 @@ def test_roundtrip_is_identity():
         keep = ~torch.isnan(v)
         back = oracle.encode16(v[keep], is_bf16).view(torch.int16)
         assert torch.equal(back, bits[keep])
+
+
+@pytest.mark.parametrize("is_bf16", [True, False])
+def test_encode_special_values(is_bf16):
+    # NaN stays NaN, infinities keep their sign, every value past the largest
+    # finite one (after rounding) is infinity: the IEEE layouts' special codes,
+    # decoded back by torch's own conversion
+    dt = torch.bfloat16 if is_bf16 else torch.float16
+    big = 3.5e38 if is_bf16 else 7.0e4
+    vals = torch.tensor([float("nan"), -float("nan"), float("inf"), -float("inf"), big, -big],
+                        dtype=torch.float64)
+    got = oracle.encode16(vals, is_bf16).to(torch.float64)
+    assert torch.isnan(got[:2]).all()
+    assert got[2:].tolist() == [float("inf"), -float("inf"), float("inf"), -float("inf")]
+    assert oracle.encode16(vals[2:], is_bf16).dtype == dt

@@ -38,6 +38,15 @@ MUTANTS = {
         "if (ri == (1u << (fb + 1))) {", "if (0) {"),
     "encode16 treats subnormals as normals": (
         "if (E < emin) E = emin;", "(void)emin;"),
+    "decode16 reads NaN patterns as infinity": (
+        "r = f ? NAN : INFINITY;", "r = INFINITY;"),
+    "encode16 turns NaN into infinity": (
+        "if (isnan(x)) return (uint16_t)(sign | inf | (1u << (fb - 1)));",
+        "if (isnan(x)) return (uint16_t)(sign | inf);"),
+    "encode16 loses the sign of zero": (
+        "if (a == 0.0) return sign;", "if (a == 0.0) return 0;"),
+    "encode16 wraps on overflow": (
+        "if (efield >= (1u << eb) - 1u) return (uint16_t)(sign | inf);", "(void)inf;"),
     # AllGatherMatmul
     "AG interleaves the shards instead of concatenating them": (
         "int64_t r = i / m_local;          /* which rank's shard */\n"
@@ -49,6 +58,12 @@ MUTANTS = {
     "AG drops the last k term": (
         "for (int64_t kk = 0; kk < k; ++kk) {\n                        double a = tab[arow[kk]];",
         "for (int64_t kk = 0; kk < k - 1; ++kk) {\n                        double a = tab[arow[kk]];"),
+    "gather stacks the shards in reverse rank order": (
+        "memcpy(gathered + (int64_t)r * m_local * k, chunks[r],",
+        "memcpy(gathered + (int64_t)r * m_local * k, chunks[world_size - 1 - r],"),
+    "AG ignores the requested rows": (
+        "int64_t i = rows ? rows[ii] : ii;\n                int64_t r = i / m_local;",
+        "int64_t i = ii;\n                int64_t r = i / m_local;"),
     "AG drops the bias": (
         "double v = acc[j] + (bias ? (double)tab[bias[j]] : 0.0);", "double v = acc[j];"),
     "AG rounds before adding the bias": (
@@ -60,6 +75,16 @@ MUTANTS = {
     "commOut stacks (token, rank) instead of (rank, token)": (
         "int64_t dst = ((int64_t)r * bs_local + t) * h + hh;",
         "int64_t dst = ((int64_t)t * rank_size + r) * h + hh;"),
+    "permute ignores the requested rows": (
+        "int64_t t = rows ? rows[ii] : ii;\n        if (t < 0 || t >= bs_local) return OR_ERR_ARG;\n        for (int r",
+        "int64_t t = ii;\n        if (t < 0 || t >= bs_local) return OR_ERR_ARG;\n        for (int r"),
+    "quant takes the signed maximum instead of the absolute one": (
+        "float ay = fabsf(y);", "float ay = y;"),
+    "int8 product reads the activations as unsigned": (
+        "int64_t av = a[t * k + kk];", "int64_t av = (uint8_t)a[t * k + kk];"),
+    "dequant takes the x1 scale by column": (
+        "v = v * x1_scale[t];\n            v = v * x2_scale[j];",
+        "v = v * x1_scale[j % n_rows];\n            v = v * x2_scale[j];"),
     "quant divides the absmax by 128": (
         "float scale = amax / 127.0f;", "float scale = amax / 128.0f;"),
     "quant truncates": (
@@ -95,6 +120,9 @@ MUTANTS = {
     "reduce-scatter reads the (n, k) weight as (k, n)": (
         "uint16_t wv = w_is_nk ? w_chunks[r][j * k_local + kk] : w_chunks[r][kk * n + j];",
         "uint16_t wv = w_chunks[r][kk * n + j];"),
+    "reduce-scatter ignores the requested rows": (
+        "int64_t i = rows ? rows[ii] : ii;\n        for (int64_t j = 0; j < n; ++j) {\n            double s = 0.0;",
+        "int64_t i = ii;\n        for (int64_t j = 0; j < n; ++j) {\n            double s = 0.0;"),
     "reduce-scatter drops the bias": (
         "if (bias) s += (double)tab[bias[j]];\n            out[ii * n + j] = oracle_encode16_rne(s, is_bf16);",
         "out[ii * n + j] = oracle_encode16_rne(s, is_bf16);"),
@@ -103,6 +131,9 @@ MUTANTS = {
         "double a = (double)tab[dy[t * n + i]];", "double a = (double)tab[dy[i * m + t]];"),
     "weight gradient reverses the columns of X": (
         "acc[j] += a * (double)tab[xrow[j]];", "acc[j] += a * (double)tab[xrow[k - 1 - j]];"),
+    "weight gradient ignores the requested rows": (
+        "int64_t i = rows ? rows[ii] : ii;\n            for (int64_t j = 0; j < k; ++j) acc[j] = 0.0;",
+        "int64_t i = ii;\n            for (int64_t j = 0; j < k; ++j) acc[j] = 0.0;"),
     "bias gradient leaves out the first row": (
         "for (int64_t t = 0; t < m; ++t) s += (double)tab[dy[t * n + i]];",
         "for (int64_t t = 1; t < m; ++t) s += (double)tab[dy[t * n + i]];"),
@@ -113,11 +144,16 @@ MUTANTS = {
         "if (e == 15 && m == 7) return NAN;", "(void)0;"),
     "e5m2 subnormal scale 2^-15": (
         "ldexp((double)m / 4.0, -14)", "ldexp((double)m / 4.0, -15)"),
+    "e5m2 reads its infinities as NaN": (
+        "if (e == 31) return m == 0 ? (sign ? -INFINITY : INFINITY) : NAN;", "if (e == 31) return NAN;"),
     "e8m0 bias 128": (
         "return ldexp(1.0, (int)v - 127);", "return ldexp(1.0, (int)v - 128);"),
     "all-reduce picks the fp32 scale of the wrong group": (
         "(double)((const float *)scale_chunks[r])[t * groups + j / G]",
         "(double)((const float *)scale_chunks[r])[t * groups + j % groups]"),
+    "all-reduce picks the e8m0 scale of the wrong group": (
+        ": oracle_decode_e8m0(((const uint8_t *)scale_chunks[r])[t * groups + j / G]);",
+        ": oracle_decode_e8m0(((const uint8_t *)scale_chunks[r])[t * groups + j % groups]);"),
     "all-reduce leaves out the last rank": (
         "for (int r = 0; r < world_size; ++r) {\n                uint8_t xv",
         "for (int r = 0; r < world_size - 1; ++r) {\n                uint8_t xv"),
