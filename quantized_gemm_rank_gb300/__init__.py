@@ -104,8 +104,13 @@ def _check(status: int):
         raise Mc2Error(status, last_error())
 
 
+_DTYPE_CODES = {torch.float16: MC2_F16, torch.bfloat16: MC2_BF16, torch.float32: MC2_F32, torch.int8: MC2_I8}
+
+
 def _dtype_code(dt: torch.dtype) -> int:
-    return {torch.float16: MC2_F16, torch.bfloat16: MC2_BF16, torch.float32: MC2_F32, torch.int8: MC2_I8}[dt]
+    if dt not in _DTYPE_CODES:
+        raise ValueError(f"unsupported dtype {dt}")
+    return _DTYPE_CODES[dt]
 
 
 def _current_device() -> int:
@@ -113,19 +118,52 @@ def _current_device() -> int:
     return torch.cuda.current_device() if torch.cuda.is_available() else -1
 
 
-def _dev(t: torch.Tensor, what: str, cur: int) -> int:
-    # the library launches on the current device: a tensor elsewhere would reach
-    # its kernels as a foreign pointer
+# Every tensor goes to the library as a bare pointer, and its kernels trust the
+# sizes passed beside it, so each tensor is checked first against the shape
+# and dtype those sizes imply (a smaller buffer would be read or written past
+# its end), against the current device (the library launches there: a tensor
+# elsewhere would reach its kernels as a foreign pointer) and for contiguity.
+# Without CUDA the device is -1, which a CPU tensor also reports: shape and
+# dtype mistakes are then still reported first, and _need_device refuses the
+# call before the library is reached.
+
+def _refuse(t: torch.Tensor, shape, dtype, what: str, cur: int):
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{what} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if t.dtype != dtype:
+        raise ValueError(f"{what} must be of dtype {dtype}, got {t.dtype}")
     if cur < 0 or t.get_device() != cur:
         where = "a CUDA device (none is available)" if cur < 0 else f"the current device (cuda:{cur})"
         raise ValueError(f"{what} must be a CUDA tensor on {where}")
-    if not t.is_contiguous():
-        raise ValueError(f"{what} must be contiguous")
+    raise ValueError(f"{what} must be contiguous")
+
+
+def _arg(t: torch.Tensor, shape, dtype, what: str, cur: int) -> int:
+    """The tensor's device pointer, once its shape, dtype, device and layout are right."""
+    if t.shape != shape or t.dtype != dtype or t.get_device() != cur or not t.is_contiguous():
+        _refuse(t, shape, dtype, what, cur)
     return t.data_ptr()
 
 
-def _opt(t: Optional[torch.Tensor], what: str, cur: int) -> Optional[int]:
-    return None if t is None else _dev(t, what, cur)
+def _opt(t: Optional[torch.Tensor], shape, dtype, what: str, cur: int) -> Optional[int]:
+    return None if t is None else _arg(t, shape, dtype, what, cur)
+
+
+def _args(ts: Sequence[torch.Tensor], shape, dtype, what: str, cur: int):
+    """A C array of the tensors' pointers, each checked as by _arg."""
+    if len(ts) == 0:
+        raise ValueError(f"{what} is empty")
+    ptrs = []
+    for t in ts:
+        if t.shape != shape or t.dtype != dtype or t.get_device() != cur or not t.is_contiguous():
+            _refuse(t, shape, dtype, f"{what}[{len(ptrs)}]", cur)
+        ptrs.append(t.data_ptr())
+    return (ctypes.c_void_p * len(ptrs))(*ptrs)
+
+
+def _need_device(cur: int) -> None:
+    if cur < 0:
+        raise ValueError("the tensors must be CUDA tensors on the current device, and no CUDA device is available")
 
 
 _raw_current_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
@@ -143,10 +181,6 @@ def _stream(stream, cur: int) -> Optional[int]:
     return stream.cuda_stream
 
 
-def _ptrs(ts: Sequence[torch.Tensor], what: str, cur: int):
-    return (ctypes.c_void_p * len(ts))(*[_dev(t, f"{what}[{i}]", cur) for i, t in enumerate(ts)])
-
-
 def mc2_all_gather_mm(x_chunks: Sequence[torch.Tensor], x2: torch.Tensor, *, x2_is_nk: bool = False,
                       bias: Optional[torch.Tensor] = None, gather_output: bool = True,
                       out: Optional[torch.Tensor] = None, gathered: Optional[torch.Tensor] = None,
@@ -161,14 +195,20 @@ def mc2_all_gather_mm(x_chunks: Sequence[torch.Tensor], x2: torch.Tensor, *, x2_
     m_local, k = x_chunks[0].shape
     n = x2.shape[0] if x2_is_nk else x2.shape[1]
     dt = x_chunks[0].dtype
+    ptrs = _args(x_chunks, (m_local, k), dt, "x_chunks", cur)
+    x2p = _arg(x2, (n, k) if x2_is_nk else (k, n), dt, "x2", cur)
+    bp = _opt(bias, (n,), dt, "bias", cur)
     if out is None:
         out = torch.empty((R * m_local, n), dtype=dt, device=x_chunks[0].device)
-    if gather_output and gathered is None:
-        gathered = torch.empty((R * m_local, k), dtype=dt, device=x_chunks[0].device)
-    ptrs = _ptrs(x_chunks, "x_chunks", cur)
-    st = lib().mc2_all_gather_mm(ptrs, R, m_local, k, _dev(x2, "x2", cur), n, int(x2_is_nk), _opt(bias, "bias", cur),
-                                 _dtype_code(dt), int(gather_output), _dev(out, "out", cur),
-                                 _opt(gathered, "gathered", cur) if gather_output else None, _stream(stream, cur))
+    outp = _arg(out, (R * m_local, n), dt, "out", cur)
+    gp = None
+    if gather_output:
+        if gathered is None:
+            gathered = torch.empty((R * m_local, k), dtype=dt, device=x_chunks[0].device)
+        gp = _arg(gathered, (R * m_local, k), dt, "gathered", cur)
+    _need_device(cur)
+    st = lib().mc2_all_gather_mm(ptrs, R, m_local, k, x2p, n, int(x2_is_nk), bp, _dtype_code(dt), int(gather_output),
+                                 outp, gp, _stream(stream, cur))
     _check(st)
     return out, (gathered if gather_output else None)
 
@@ -187,11 +227,19 @@ def mc2_matmul_reduce_scatter(x_chunks: Sequence[torch.Tensor], w_chunks: Sequen
     m, k_local = x_chunks[0].shape
     n = w_chunks[0].shape[0] if w_is_nk else w_chunks[0].shape[1]
     dt = x_chunks[0].dtype
+    if len(w_chunks) != R:
+        raise ValueError(f"w_chunks must hold {R} shards (one per rank), got {len(w_chunks)}")
+    if out_chunks is not None and len(out_chunks) != R:
+        raise ValueError(f"out_chunks must hold {R} outputs (one per rank), got {len(out_chunks)}")
+    xp = _args(x_chunks, (m, k_local), dt, "x_chunks", cur)
+    wp = _args(w_chunks, (n, k_local) if w_is_nk else (k_local, n), dt, "w_chunks", cur)
+    bp = _opt(bias, (n,), dt, "bias", cur)
     if out_chunks is None:
         out_chunks = [torch.empty((m // R, n), dtype=dt, device=x_chunks[0].device) for _ in range(R)]
-    st = lib().mc2_matmul_reduce_scatter(_ptrs(x_chunks, "x_chunks", cur), _ptrs(w_chunks, "w_chunks", cur), R, m, k_local, n,
-                                         int(w_is_nk), _opt(bias, "bias", cur), _dtype_code(dt),
-                                         _ptrs(out_chunks, "out_chunks", cur), _stream(stream, cur))
+    op = _args(out_chunks, (m // R, n), dt, "out_chunks", cur)
+    _need_device(cur)
+    st = lib().mc2_matmul_reduce_scatter(xp, wp, R, m, k_local, n, int(w_is_nk), bp, _dtype_code(dt), op,
+                                         _stream(stream, cur))
     _check(st)
     return list(out_chunks)
 
@@ -206,12 +254,19 @@ def mc2_matmul_weight_grad(dy: torch.Tensor, x: torch.Tensor, *, with_bias: bool
     cur = _current_device()
     m, n = dy.shape
     k = x.shape[1]
+    dt = dy.dtype
+    dyp = _arg(dy, (m, n), dt, "dy", cur)
+    xp = _arg(x, (m, k), dt, "x", cur)
     if dw is None:
-        dw = torch.empty((n, k), dtype=dy.dtype, device=dy.device)
-    if with_bias and db is None:
-        db = torch.empty((n,), dtype=dy.dtype, device=dy.device)
-    st = lib().mc2_matmul_weight_grad(_dev(dy, "dy", cur), m, n, _dev(x, "x", cur), k, _dtype_code(dy.dtype), _dev(dw, "dw", cur),
-                                      _opt(db if with_bias else None, "db", cur), _stream(stream, cur))
+        dw = torch.empty((n, k), dtype=dt, device=dy.device)
+    dwp = _arg(dw, (n, k), dt, "dw", cur)
+    dbp = None
+    if with_bias:
+        if db is None:
+            db = torch.empty((n,), dtype=dt, device=dy.device)
+        dbp = _arg(db, (n,), dt, "db", cur)
+    _need_device(cur)
+    st = lib().mc2_matmul_weight_grad(dyp, m, n, xp, k, _dtype_code(dt), dwp, dbp, _stream(stream, cur))
     _check(st)
     return dw, (db if with_bias else None)
 
@@ -239,13 +294,27 @@ def mc2_quant_all_reduce(x_chunks: Sequence[torch.Tensor], scale_chunks: Sequenc
         x_kind = _QAR_X_BY_DTYPE[x0.dtype]
     h = x0.shape[-1]
     bs = x0.numel() // h
+    if len(scale_chunks) != len(x_chunks):
+        raise ValueError(f"scale_chunks must hold {len(x_chunks)} tensors (one per rank), got {len(scale_chunks)}")
+    xp = _args(x_chunks, x0.shape, x0.dtype, "x_chunks", cur)
     s0 = scale_chunks[0]
     sdt = MC2_F32 if s0.dtype == torch.float32 else MC2_E8M0
+    # fp32: one scale per token per 128 elements, any shape; e8m0: one uint8 code per 32
+    sdtype = torch.float32 if sdt == MC2_F32 else torch.uint8
+    if h % 128 == 0:
+        count = bs * (h // 128 if sdt == MC2_F32 else h // 32)
+        for i, sc in enumerate(scale_chunks):
+            if sc.numel() != count or sc.dtype != sdtype:
+                raise ValueError(f"scale_chunks[{i}] must hold {count} "
+                                 f"{'fp32 scales' if sdt == MC2_F32 else 'e8m0 codes (uint8)'}, "
+                                 f"got {sc.numel()} of {sc.dtype}")
+    sp = _args(scale_chunks, s0.shape, sdtype, "scale_chunks", cur)
     if out is None:
         out = torch.empty(x0.shape, dtype=out_dtype, device=x0.device)
-    st = lib().mc2_quant_all_reduce(_ptrs(x_chunks, "x_chunks", cur), _ptrs(scale_chunks, "scale_chunks", cur),
-                                    len(x_chunks), bs, h, _QAR_X[x_kind], sdt, _dtype_code(out.dtype),
-                                    _dev(out, "out", cur), _stream(stream, cur))
+    outp = _arg(out, x0.shape, out_dtype, "out", cur)
+    _need_device(cur)
+    st = lib().mc2_quant_all_reduce(xp, sp, len(x_chunks), bs, h, _QAR_X[x_kind], sdt, _dtype_code(out.dtype),
+                                    outp, _stream(stream, cur))
     _check(st)
     return out
 
@@ -256,6 +325,33 @@ def mc2_alltoall_quant_mm_workspace(rank_size: int, bs_local: int, h: int, n: in
     _check(lib().mc2_alltoall_quant_mm_workspace(rank_size, bs_local, h, n, x1_quant_mode, _dtype_code(x1_dtype),
                                                  ctypes.byref(nbytes)))
     return int(nbytes.value)
+
+
+def _a2a_args(chunks, x2, x2_scale, bias, x1_quant_mode, x1_scale, out, q_out, x1_scale_out, acc_out,
+              alltoall_out, cur: int) -> list:
+    """The pointers of an AlltoAllQuantMatmul call, each tensor checked against
+    the sizes of the first chunk and of x2 (the quant modes and the 16-bit /
+    int8 choice are the library's to refuse)."""
+    R = len(chunks)
+    bs_local, h = chunks[0].shape
+    K = R * h
+    n = x2.shape[1]
+    x1_dtype = chunks[0].dtype
+    if bias.dtype not in (torch.float32, torch.bfloat16):
+        raise ValueError(f"bias must be of dtype torch.float32 or torch.bfloat16, got {bias.dtype}")
+    if x1_quant_mode == QUANT_PERTOKEN:
+        x1p = _opt(x1_scale, (bs_local,), torch.float32, "x1_scale (per-token scale)", cur)
+    else:
+        x1p = _opt(x1_scale, (K,), x1_dtype, "x1_scale (smooth scale)", cur)
+    return [_args(chunks, (bs_local, h), x1_dtype, "chunks", cur), x1p,
+            _arg(x2, (K, n), torch.int8, "x2", cur),
+            _arg(x2_scale, (n,), torch.float32, "x2_scale", cur),
+            _arg(bias, (n,), bias.dtype, "bias", cur),
+            _arg(out, (bs_local, n), torch.bfloat16, "out", cur),
+            _opt(alltoall_out, (R, bs_local, h), x1_dtype, "alltoall_out", cur),
+            _opt(q_out, (bs_local, K), torch.int8, "q_out", cur),
+            _opt(x1_scale_out, (bs_local,), torch.float32, "x1_scale_out", cur),
+            _opt(acc_out, (bs_local, n), torch.int32, "acc_out", cur)]
 
 
 def mc2_alltoall_quant_mm(chunks: Sequence[torch.Tensor], x2: torch.Tensor, x2_scale: torch.Tensor,
@@ -281,16 +377,16 @@ def mc2_alltoall_quant_mm(chunks: Sequence[torch.Tensor], x2: torch.Tensor, x2_s
     x1_dtype = chunks[0].dtype
     if out is None:
         out = torch.empty((bs_local, n), dtype=torch.bfloat16, device=dev)
+    a = _a2a_args(chunks, x2, x2_scale, bias, x1_quant_mode, x1_scale, out, q_out, x1_scale_out, acc_out,
+                  alltoall_out, cur)
+    _need_device(cur)
     if workspace is None:
         need = mc2_alltoall_quant_mm_workspace(R, bs_local, h, n, x1_quant_mode, x1_dtype)
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
-    ptrs = _ptrs(chunks, "chunks", cur)
-    st = lib().mc2_alltoall_quant_mm(ptrs, R, bs_local, h, _dtype_code(x1_dtype), _opt(x1_scale, "x1_scale", cur),
-                                     _dev(x2, "x2", cur), _dev(x2_scale, "x2_scale", cur), _dev(bias, "bias", cur),
-                                     _dtype_code(bias.dtype), x1_quant_mode, x2_quant_mode, n, _dev(out, "out", cur),
-                                     _opt(alltoall_out, "alltoall_out", cur), _opt(q_out, "q_out", cur),
-                                     _opt(x1_scale_out, "x1_scale_out", cur), _opt(acc_out, "acc_out", cur),
-                                     _dev(workspace, "workspace", cur), workspace.numel() * workspace.element_size(),
+    wp = _arg(workspace, workspace.shape, workspace.dtype, "workspace", cur)
+    st = lib().mc2_alltoall_quant_mm(a[0], R, bs_local, h, _dtype_code(x1_dtype), a[1], a[2], a[3], a[4],
+                                     _dtype_code(bias.dtype), x1_quant_mode, x2_quant_mode, n, a[5], a[6], a[7],
+                                     a[8], a[9], wp, workspace.numel() * workspace.element_size(),
                                      _stream(stream, cur))
     _check(st)
     return {"out": out, "q": q_out, "x1_scale": x1_scale_out, "acc": acc_out, "alltoall_out": alltoall_out}
@@ -314,16 +410,17 @@ def mc2_alltoall_quant_mm_no_alloc(chunks: Sequence[torch.Tensor], x2: torch.Ten
     must be serialised by the caller.
     """
     cur = _current_device()
+    if out is None:
+        raise ValueError("out must be given (this entry point allocates nothing)")
     R = len(chunks)
     bs_local, h = chunks[0].shape
     n = x2.shape[1]
-    ptrs = _ptrs(chunks, "chunks", cur)
-    st = lib().mc2_alltoall_quant_mm_no_alloc(ptrs, R, bs_local, h, _dtype_code(chunks[0].dtype),
-                                              _opt(x1_scale, "x1_scale", cur), _dev(x2, "x2", cur), _dev(x2_scale, "x2_scale", cur),
-                                              _dev(bias, "bias", cur), _dtype_code(bias.dtype), x1_quant_mode,
-                                              x2_quant_mode, n, _dev(out, "out", cur), _opt(alltoall_out, "alltoall_out", cur),
-                                              _opt(q_out, "q_out", cur), _opt(x1_scale_out, "x1_scale_out", cur),
-                                              _opt(acc_out, "acc_out", cur), _stream(stream, cur))
+    a = _a2a_args(chunks, x2, x2_scale, bias, x1_quant_mode, x1_scale, out, q_out, x1_scale_out, acc_out,
+                  alltoall_out, cur)
+    _need_device(cur)
+    st = lib().mc2_alltoall_quant_mm_no_alloc(a[0], R, bs_local, h, _dtype_code(chunks[0].dtype), a[1], a[2], a[3],
+                                              a[4], _dtype_code(bias.dtype), x1_quant_mode, x2_quant_mode, n, a[5],
+                                              a[6], a[7], a[8], a[9], _stream(stream, cur))
     _check(st)
     return {"out": out, "q": q_out, "x1_scale": x1_scale_out, "acc": acc_out, "alltoall_out": alltoall_out}
 

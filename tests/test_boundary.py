@@ -319,3 +319,74 @@ def test_quant_all_reduce_bounds_accepted_by_validation():
         for sd in (mc2.MC2_F32, mc2.MC2_E8M0):
             for od in (mc2.MC2_F32, mc2.MC2_F16, mc2.MC2_BF16):
                 assert qar_call(world_size=8, x_dtype=xd, scale_dtype=sd, out_dtype=od) == mc2.MC2_ERR_CUDA
+
+
+def _z(*shape, dtype=torch.bfloat16):
+    return torch.zeros(*shape, dtype=dtype)
+
+
+_AG = dict(x_chunks=[_z(16, 256)] * 2, x2=_z(256, 64))
+_A2A = dict(chunks=[_z(8, 64)] * 4, x2=_z(256, 32, dtype=torch.int8), x2_scale=_z(32, dtype=torch.float32),
+            bias=_z(32, dtype=torch.float32))
+
+
+@pytest.mark.parametrize("call,kw,what", [
+    # AllGatherMatmul: every tensor against the sizes of chunk 0 and x2
+    ("ag", dict(x_chunks=[_z(16, 256), _z(8, 256)]), r"x_chunks\[1\] must have shape \(16, 256\)"),
+    ("ag", dict(x_chunks=[_z(16, 256), _z(16, 256, dtype=torch.float16)]), r"x_chunks\[1\] must be of dtype"),
+    ("ag", dict(x2=_z(128, 64)), r"x2 must have shape \(256, 64\)"),
+    ("ag", dict(x2=_z(256, 64, dtype=torch.float16)), "x2 must be of dtype"),
+    ("ag", dict(bias=_z(63)), r"bias must have shape \(64,\)"),
+    ("ag", dict(out=_z(31, 64)), r"out must have shape \(32, 64\)"),
+    ("ag", dict(gathered=_z(32, 128)), r"gathered must have shape \(32, 256\)"),
+    # MatmulReduceScatter
+    ("rs", dict(w_chunks=[_z(48, 64)]), "w_chunks must hold 2 shards"),
+    ("rs", dict(w_chunks=[_z(48, 64), _z(48, 32)]), r"w_chunks\[1\] must have shape \(48, 64\)"),
+    ("rs", dict(out_chunks=[_z(8, 48), _z(16, 48)]), r"out_chunks\[0\] must have shape \(16, 48\)"),
+    # weight gradient
+    ("wg", dict(x=_z(31, 128)), r"x must have shape \(32, 128\)"),
+    ("wg", dict(dw=_z(128, 48)), r"dw must have shape \(48, 128\)"),
+    ("wg", dict(db=_z(48, dtype=torch.float32)), "db must be of dtype"),
+    # QuantAllReduce
+    ("qar", dict(x_chunks=[_z(4, 1024, dtype=torch.int8), _z(4, 512, dtype=torch.int8)]),
+     r"x_chunks\[1\] must have shape \(4, 1024\)"),
+    ("qar", dict(scale_chunks=[_z(4, 8, dtype=torch.float32), _z(4, 4, dtype=torch.float32)]),
+     r"scale_chunks\[1\] must hold 32 fp32 scales"),
+    ("qar", dict(out=_z(4, 1024, dtype=torch.float16)), "out must be of dtype"),
+    # AlltoAllQuantMatmul (the workspace entry point and the one without)
+    ("a2a", dict(x2=_z(128, 32, dtype=torch.int8)), r"x2 must have shape \(256, 32\)"),
+    ("a2a", dict(x2_scale=_z(31, dtype=torch.float32)), r"x2_scale must have shape \(32,\)"),
+    ("a2a", dict(bias=_z(32, dtype=torch.float16)), "bias must be of dtype"),
+    ("a2a", dict(x1_scale=_z(128)), r"x1_scale \(smooth scale\) must have shape \(256,\)"),
+    ("a2a", dict(out=_z(8, 32, dtype=torch.float16)), "out must be of dtype"),
+    ("a2a", dict(q_out=_z(8, 128, dtype=torch.int8)), r"q_out must have shape \(8, 256\)"),
+    ("a2a", dict(acc_out=_z(8, 32, dtype=torch.float32)), "acc_out must be of dtype"),
+    ("a2a", dict(alltoall_out=_z(4, 8, 32)), r"alltoall_out must have shape \(4, 8, 64\)"),
+    ("a2a-full", dict(x1_scale=_z(4, dtype=torch.float32)), r"x1_scale \(per-token scale\) must have shape \(8,\)"),
+    ("no-alloc", dict(out=None), "out must be given"),
+])
+def test_binding_checks_shapes_and_dtypes_before_any_launch(call, kw, what):
+    """The kernels trust the sizes the binding passes them, so every tensor's
+    shape and dtype is checked against those sizes first (these run on CPU
+    tensors: the check comes before the device check and any library call)."""
+    with pytest.raises(ValueError, match=what):
+        if call == "ag":
+            a = dict(_AG, **kw)
+            mc2.mc2_all_gather_mm(a.pop("x_chunks"), a.pop("x2"), **a)
+        elif call == "rs":
+            a = dict(dict(x_chunks=[_z(32, 64)] * 2, w_chunks=[_z(48, 64)] * 2), **kw)
+            mc2.mc2_matmul_reduce_scatter(a.pop("x_chunks"), a.pop("w_chunks"), **a)
+        elif call == "wg":
+            a = dict(dict(dy=_z(32, 48), x=_z(32, 128)), **kw)
+            mc2.mc2_matmul_weight_grad(a.pop("dy"), a.pop("x"), **a)
+        elif call == "qar":
+            a = dict(dict(x_chunks=[_z(4, 1024, dtype=torch.int8)] * 2,
+                          scale_chunks=[_z(4, 8, dtype=torch.float32)] * 2), **kw)
+            mc2.mc2_quant_all_reduce(a.pop("x_chunks"), a.pop("scale_chunks"), **a)
+        elif call in ("a2a", "a2a-full"):
+            base = dict(_A2A) if call == "a2a" else dict(_A2A, chunks=[_z(8, 64, dtype=torch.int8)] * 4)
+            a = dict(base, x1_quant_mode=7 if call == "a2a" else 3, **kw)
+            mc2.mc2_alltoall_quant_mm(a.pop("chunks"), a.pop("x2"), a.pop("x2_scale"), a.pop("bias"), **a)
+        else:
+            a = dict(_A2A, x1_quant_mode=7, **kw)
+            mc2.mc2_alltoall_quant_mm_no_alloc(a.pop("chunks"), a.pop("x2"), a.pop("x2_scale"), a.pop("bias"), **a)
