@@ -15,6 +15,10 @@
  *     CUDA device current on the calling thread, and `stream` must belong to
  *     that device: the library launches there and does not look up where a
  *     pointer lives (that would be a driver query per pointer per call).
+ *   - Each buffer must hold at least the elements that the sizes passed with
+ *     it imply, in the stated dtype.  The library sees bare pointers and
+ *     cannot check this: a smaller buffer is read or written past its end.
+ *     (The Python binding checks every tensor's shape and dtype first.)
  *   - Work is enqueued on `stream` (a cudaStream_t passed as void*; NULL is the
  *     legacy default stream) and the call returns without synchronising.  The
  *     library never allocates device memory: scratch space is the caller's
