@@ -11,8 +11,8 @@
 // The products are added in rank order by fp32 fused multiply-adds and the sum
 // is rounded once (nearest-even) to the output type.
 //
-// HBM-bound: each rank's codes are read once (16-byte streaming loads, one or
-// two per rank in flight per thread), the output written once.  Because G divides H,
+// HBM-bound: each rank's codes are read once (16-byte loads with a 256-byte L2
+// fetch, one or two per rank in flight per thread), the output written once.  Because G divides H,
 // the scale of flat element e is scales_r[e / G] whatever the row, so the
 // kernel runs over the flat (bs * H) range with no row arithmetic.
 #include <atomic>
@@ -116,10 +116,25 @@ __device__ __forceinline__ void reduce_store(const uint4 (&xv)[kR], const float 
     }
 }
 
+// A 16-byte load of codes that are read once: through the read-only path, not
+// allocated in L1, with L2 asked to fetch the whole 256-byte block around it
+// from DRAM (the L2::256B prefetch-size qualifier), so a warp's 512 contiguous
+// bytes arrive as two whole blocks.  With one such stream per rank in flight
+// this measured 62.1 -> 58.5 us on qar-8x4096x8192 against evict-first loads
+// (same process, bit-identical); the widening kernels, with one or two streams,
+// gained nothing from it.
+__device__ __forceinline__ uint4 ld_code_vec(const uint4 *p) {
+    uint4 v;
+    asm("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
+        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+        : "l"(p));
+    return v;
+}
+
 template <int kS, int kR>
 __device__ __forceinline__ void load_vec(const QarPtrs &p, int64_t v, uint4 (&xv)[kR], float (&sc)[kR]) {
 #pragma unroll
-    for (int r = 0; r < kR; ++r) xv[r] = __ldcs(reinterpret_cast<const uint4 *>(p.x[r]) + v);
+    for (int r = 0; r < kR; ++r) xv[r] = ld_code_vec(reinterpret_cast<const uint4 *>(p.x[r]) + v);
 #pragma unroll
     for (int r = 0; r < kR; ++r) {
         if constexpr (kS == 0)
