@@ -219,6 +219,67 @@ def test_quant_ties_and_near_ties_on_gpu():
     assert got["q"][0, :len(want)].tolist() == want
 
 
+def _tiny_rows(dtype, K):
+    """Rows whose smooth products reach the bottom of fp32 (the smooth scale is
+    per column, so each row puts its non-zero values in one band of columns):
+    products that underflow to zero or to fp32 subnormals, a row whose absmax
+    is subnormal (scale subnormal, 1 / scale infinite: the IEEE-division
+    fallback), a row whose scale itself underflows to zero, a row of tiny
+    normal products, and a mixed row."""
+    g = torch.Generator().manual_seed(17)
+    band = K // 4
+    if dtype == torch.bfloat16:
+        # smooth bands: 1, 2^-100, 2^-120, the smallest bf16 subnormal 2^-133
+        smooth = torch.cat([torch.ones(band), torch.full((band,), 2.0 ** -100), torch.full((band,), 2.0 ** -120),
+                            torch.full((K - 3 * band,), 2.0 ** -133)])
+        sub = 2.0 ** -133 * torch.randint(1, 128, (band,), generator=g).double()   # bf16 subnormals
+    else:
+        # fp16: 1, 2^-14, 2^-20, the smallest fp16 subnormal 2^-24 (no product leaves fp32's normal range)
+        smooth = torch.cat([torch.ones(band), torch.full((band,), 2.0 ** -14), torch.full((band,), 2.0 ** -20),
+                            torch.full((K - 3 * band,), 2.0 ** -24)])
+        sub = 2.0 ** -24 * torch.randint(1, 1024, (band,), generator=g).double()   # fp16 subnormals
+    signs = torch.where(torch.rand(K, generator=g) < 0.5, -1.0, 1.0).double()
+    rnd = torch.randn(K, generator=g).double() * signs.abs()
+    rows = []
+    for b in range(4):                                  # one band at a time: normal values
+        r = torch.zeros(K, dtype=torch.float64)
+        r[b * band:(b + 1) * band] = rnd[b * band:(b + 1) * band] * 1e-3
+        rows.append(r)
+    r = torch.zeros(K, dtype=torch.float64)             # subnormal inputs in the smooth-1 band
+    r[:band] = sub * signs[:band]
+    rows.append(r)
+    r = torch.zeros(K, dtype=torch.float64)             # subnormal inputs in the smallest band
+    r[3 * band:3 * band + band] = sub * signs[:band]
+    rows.append(r)
+    rows.append(rnd * 4.0)                              # everything at once
+    P = torch.stack(rows).to(dtype)
+    return P, smooth.to(dtype)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+def test_tiny_products_and_subnormal_scales(dtype):
+    """The fused prologue at the bottom of fp32: smooth products that underflow
+    (where its mixed-precision multiply-add and the oracle's fp32 multiply must
+    round alike), subnormal absmax and scales (the IEEE-division fallback), a
+    scale that underflows to zero; q, the scales and the output bit for bit."""
+    R, h = 2, 256
+    K = R * h
+    P, smooth = _tiny_rows(dtype, K)
+    chunks = [P[:, r * h:(r + 1) * h].contiguous() for r in range(R)]
+    shape = A2A(rank_size=R, bs_local=P.shape[0], h=h, n=64, quant_mode=7, x1_dtype=dtype)
+    g = torch.Generator().manual_seed(5)
+    inp = {"chunks": chunks, "x1_scale": smooth,
+           "x2": torch.randint(-127, 128, (K, 64), generator=g, dtype=torch.int8),
+           "x2_scale": torch.rand(64, generator=g) * 1e-2, "bias": torch.randn(64, generator=g)}
+    got = run_gpu(inp, shape)
+    ref = run_oracle(inp, shape)
+    compare(got, ref, f"tiny {dtype}")
+    if dtype == torch.bfloat16:
+        sc = ref["x1_scale"]
+        assert (sc[(sc > 0)] < 2.0 ** -126).any(), "no row with a subnormal scale"
+        assert (sc == 0).any() and (P.double().abs().sum(1)[sc == 0] > 0).any(), "no non-zero row with a zero scale"
+
+
 @pytest.mark.parametrize("n,mode", [(2560, 3), (4352, 7), (4352, 3)])
 def test_partial_last_wave_exact(n, mode):
     """Shapes whose tile count is not a multiple of the co-resident CTA pairs:
