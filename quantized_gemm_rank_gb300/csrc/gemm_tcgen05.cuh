@@ -751,7 +751,11 @@ __global__ void __launch_bounds__(kNumThreads, 1) mc2_gemm_kernel(const __grid_c
         bool ok = true;
         TileWalk<kDyn> walk = walk0;
         Work w;
-        while (ok && walk.template next<kPair>(w, p, abort_flag)) {
+        while (ok) {
+            // the two warps take each tile together: with tiles obtained at run time
+            // one of them could see an abort that the other does not, and would
+            // leave the other waiting alone at the named barrier below
+            if (!ptx::bar_red_and(1, 64, walk.template next<kPair>(w, p, abort_flag))) break;
             const int kt_begin = w.kb0 * p.kblock_tiles, kt_end = min(num_k, w.kb1 * p.kblock_tiles);
             int mb, nb;
             tile_coords<kIntPath>(w.tile, num_m, num_n, mb, nb);
