@@ -208,9 +208,9 @@ constexpr int kPrologueThreads = 256;
 // Adding -0 changes no product, a zero of either sign included.  A product of
 // two bf16 or fp16 values has at most 22 significant bits, so it is exact
 // unless it underflows, and then both forms round it the same way.  Against
-// the widening and a paired multiply: 34 registers instead of 36, and the
-// prologue 47.3 -> 46.7 us on a2a-dyn, 27.1 -> 26.3 us on a2a-dyn-small
-// (same process, bit-identical).
+// the widening and a paired multiply: fewer instructions, and the prologue
+// 47.3 -> 46.7 us on a2a-dyn, 27.1 -> 26.3 us on a2a-dyn-small (same process,
+// bit-identical).
 template <bool kBF16>
 __device__ __forceinline__ float2 mul_exact2(uint32_t x, uint32_t s) {
     float2 y;
@@ -301,10 +301,11 @@ __global__ void __launch_bounds__(kPrologueThreads) a2a_prologue_kernel(
                               static_cast<const uint16_t *>(chunks.p[r]) + t * h, static_cast<uint32_t>(h) * 2u, bar);
     }
     __syncthreads();   // the barrier is initialised before anyone polls it
-    if (!ptx::mbar_wait(bar, 0, wait_limit_ns)) {
-        if (threadIdx.x == 0 && status) atomicExch(status, -7);
-        return;
-    }
+    // A thread whose bounded wait gives up raises the status word and still
+    // takes part in the row (its outputs are void then): the threads' waits can
+    // end on either side of the limit, and one that left early would strand the
+    // others at the row's block barriers.
+    if (!ptx::mbar_wait(bar, 0, wait_limit_ns) && status) atomicExch(status, -7);
     const uint4 *rowv = reinterpret_cast<const uint4 *>(prow);
     // commOut: the received pieces in their own layout (rank_size, bs_local, h)
     if (comm_out) {
