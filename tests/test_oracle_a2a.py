@@ -325,3 +325,10 @@ def test_large_composite_uses_same_steps():
     assert torch.equal(big["acc"], acc)
     assert torch.equal(big["out"].view(torch.int16),
                        oracle.dequant(acc, inp["x1_scale"], inp["x2_scale"], inp["bias"]).view(torch.int16))
+    # the same route for a row subset (all 40 rows in reverse order: still large):
+    # each output row is the full result's row, with its own token's scale
+    rows = list(range(39, -1, -1))
+    sub = oracle.alltoall_quant_mm(inp["chunks"], inp["x2"], inp["x2_scale"], inp["bias"], quant_mode=3,
+                                   x1_scale=inp["x1_scale"], rows=rows)
+    assert torch.equal(sub["x1_scale"], inp["x1_scale"][rows])
+    assert torch.equal(sub["out"].view(torch.int16), big["out"][rows].view(torch.int16))

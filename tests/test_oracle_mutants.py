@@ -9,9 +9,15 @@ force, hand-worked values and independent library routines) are run against
 it in a child process through MC2_ORACLE_LIB.  Every mutant must make at least
 one pin fail; the unchanged copy, built the same way, must pass them all.
 
+The same is done for the oracle's Python wrapper (oracle/__init__.py: the
+argument conversions and the exact fp64 route of large int8 products): a copy
+of the package with one mistake is imported first in the child process, so it
+stands in for the committed one.
+
 The mistakes are planted on the CPU only, in copies under pytest's temporary
 folder; the committed oracle is never modified.  A mutant whose mistake cannot
-change any result (an equivalent mutant) does not belong in this list.
+change any result (an equivalent mutant) does not belong in these lists, nor
+one that would make the C code write past a buffer.
 """
 import os
 import subprocess
@@ -24,6 +30,7 @@ import oracle
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SRC = os.path.join(ROOT, "oracle", "mc2_oracle.c")
+PY_SRC = os.path.join(ROOT, "oracle", "__init__.py")
 PINS = sorted(os.path.join(ROOT, "tests", f) for f in os.listdir(os.path.join(ROOT, "tests"))
               if f.startswith("test_oracle_") and f.endswith(".py") and f != "test_oracle_mutants.py")
 
@@ -162,10 +169,45 @@ MUTANTS = {
 }
 
 
-def _run_pins(lib_path):
+# name -> [(text in oracle/__init__.py, replacement), ...]; each text occurs exactly once
+PY_MUTANTS = {
+    "the fp64 route of the int8 product sums in fp32": [
+        ("    ad = ac.double()\n", "    ad = ac.float()\n"),
+        ("blk = ad @ bc[:, j0:j0 + col_block].double()", "blk = ad @ bc[:, j0:j0 + col_block].float()")],
+    "the fp64 route takes every token's scale for a row subset": [
+        ("sc = s_in if r is None else s_in[r]", "sc = s_in")],
+    "bf16 tensors passed as fp16": [
+        ("    if dtype == torch.bfloat16:\n        return 1", "    if dtype == torch.bfloat16:\n        return 0")],
+    "e4m3 and e5m2 codes swapped": [
+        ('X_KINDS = {"int8": 0, "e4m3": 1, "e5m2": 2}', 'X_KINDS = {"int8": 0, "e4m3": 2, "e5m2": 1}')],
+    "fp32 and e8m0 scales swapped": [
+        ('SCALE_KINDS = {"fp32": 0, "e8m0": 1}', 'SCALE_KINDS = {"fp32": 1, "e8m0": 0}')],
+    "fp16 and bf16 outputs swapped": [
+        ("_OUT_KINDS = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}",
+         "_OUT_KINDS = {torch.float32: 0, torch.float16: 2, torch.bfloat16: 1}")],
+    "AG bias converted to fp16 whatever the operands": [
+        ("b = None if bias is None else _c(bias.to(dt))\n    r, nr = _rows_arg(rows)\n    nrows = nr if r is not None "
+         "else len(cs) * m_local",
+         "b = None if bias is None else _c(bias.to(torch.float16))\n    r, nr = _rows_arg(rows)\n    nrows = nr if r is "
+         "not None else len(cs) * m_local")],
+    "full-quant scales rounded to bf16": [
+        ("        s_in = _c(x1_scale.float())", "        s_in = _c(x1_scale.to(torch.bfloat16).float())")],
+}
+
+
+def _run_pins(lib_path, package_dir=None):
+    """Run the pins in a child process against the oracle library `lib_path`
+    (and, with `package_dir`, the oracle package found there)."""
     env = dict(os.environ, MC2_ORACLE_LIB=lib_path, OMP_NUM_THREADS="2")
-    cmd = [sys.executable, "-m", "pytest", *PINS, "-x", "-q", "-m", "not gpu", "-p", "no:cacheprovider",
-           "-p", "no:randomly"]
+    args = [*PINS, "-x", "-q", "-m", "not gpu", "-p", "no:cacheprovider", "-p", "no:randomly"]
+    if package_dir is None:
+        cmd = [sys.executable, "-m", "pytest", *args]
+    else:
+        # import the copy first: the test modules then find it in sys.modules
+        code = ("import sys; sys.path.insert(0, %r); import oracle; "
+                "assert oracle.__file__.startswith(%r), oracle.__file__; "
+                "import pytest; sys.exit(pytest.main(%r))" % (package_dir, package_dir, args))
+        cmd = [sys.executable, "-c", code]
     r = subprocess.run(cmd, cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     return r.returncode, r.stdout[-3000:] + r.stderr[-2000:]
 
@@ -180,6 +222,16 @@ def outcomes(tmp_path_factory):
         assert src.count(old) == 1, f"mutant '{name}': its text occurs {src.count(old)} times in the oracle"
         jobs[name] = src.replace(old, new)
 
+    py_src = open(PY_SRC).read()
+    py_jobs = {}
+    for name, edits in PY_MUTANTS.items():
+        text = py_src
+        for old, new in edits:
+            assert text.count(old) == 1, f"mutant '{name}': its text occurs {text.count(old)} times in the wrapper"
+            text = text.replace(old, new)
+        py_jobs[name] = text
+    base_lib = oracle.compile_library(SRC, str(d / "libbase.so"))
+
     def one(item):
         i, (name, text) = item
         c = d / f"m{i}.c"
@@ -187,9 +239,18 @@ def outcomes(tmp_path_factory):
         lib = oracle.compile_library(str(c), str(d / f"libm{i}.so"))
         return name, _run_pins(lib)
 
+    def one_py(item):
+        i, (name, text) = item
+        pkg = d / f"py{i}"
+        (pkg / "oracle").mkdir(parents=True)
+        (pkg / "oracle" / "__init__.py").write_text(text)
+        return name, _run_pins(base_lib, str(pkg))
+
     workers = max(1, min(8, (os.cpu_count() or 2) // 2))
     with ThreadPoolExecutor(workers) as ex:
-        return dict(ex.map(one, enumerate(jobs.items())))
+        out = dict(ex.map(one, enumerate(jobs.items())))
+        out.update(ex.map(one_py, enumerate(py_jobs.items())))
+    return out
 
 
 def test_unchanged_copy_passes_the_pins(outcomes):
@@ -197,7 +258,7 @@ def test_unchanged_copy_passes_the_pins(outcomes):
     assert rc == 0, f"the pins fail on an unchanged copy of the oracle:\n{log}"
 
 
-@pytest.mark.parametrize("name", list(MUTANTS))
+@pytest.mark.parametrize("name", list(MUTANTS) + list(PY_MUTANTS))
 def test_pins_catch_the_planted_mistake(outcomes, name):
     rc, log = outcomes[name]
     # exit code 1: tests ran and at least one failed (not a collection or usage error)
